@@ -1,0 +1,48 @@
+"""Plant plausible mistakes in the oracle (on the CPU) and check that the pin
+suite catches every one: a dropped term, a wrong sign or index, a transposed
+operand, a wrong constant, a wrong rounding rule."""
+import os
+import subprocess
+import sys
+
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "zero1_oracle.c")
+
+MUTANTS = {
+    "drop_bias_correction_1": ("float mh = m1 / bc1;", "float mh = m1;"),
+    "bias_correction_off_by_one": ("pow((double)beta1, (double)t)", "pow((double)beta1, (double)(t + 1))"),
+    "betas_swapped_in_m": ("float m1 = beta1 * m[j] + omb1 * gj;", "float m1 = beta2 * m[j] + omb2 * gj;"),
+    "eps_inside_sqrt": ("float u = mh / (sqrtf(vh) + eps);", "float u = mh / sqrtf(vh + eps);"),
+    "decay_without_lr": ("out[5] = (float)(1.0 - (double)lr * (double)weight_decay);",
+                         "out[5] = (float)(1.0 - (double)weight_decay);"),
+    "update_sign": ("float w = master[j] * cdec - lr * u;", "float w = master[j] * cdec + lr * u;"),
+    "loss_scale_ignored": ("out[0] = (float)(1.0 / ((double)B * (double)S));", "out[0] = (float)(1.0 / ((double)B));"),
+    "rank0_dropped": ("s = orc_bf16_to_f32(grads[0][j]);\n            for (int32_t r = 1;",
+                      "s = 0.0f;\n            for (int32_t r = 1;"),
+    "v_not_squared": ("float v1 = beta2 * v[j] + omb2 * (gj * gj);", "float v1 = beta2 * v[j] + omb2 * gj;"),
+    "ties_round_up": ("else mag = (lo & 1u) ? hi : lo;", "else mag = hi;"),
+    "plan_overpads": ("int64_t P = ((n + unit - 1) / unit) * unit;", "int64_t P = (n / unit) * unit + unit;"),
+    "gather_not_from_master": ("params[j] = orc_f32_to_bf16(master[j]);",
+                               "params[j] = orc_f32_to_bf16(master[j] * 1.0000001f);"),
+    "sqrt_of_m": ("float u = mh / (sqrtf(vh) + eps);", "float u = vh / (sqrtf(mh) + eps);"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, tmp_path):
+    a, b = MUTANTS[name]
+    src = open(SRC).read()
+    assert a in src, "mutation anchor missing: the oracle changed, update the mutant"
+    c = tmp_path / "mutant.c"
+    c.write_text(src.replace(a, b))
+    so = tmp_path / "mutant.so"
+    subprocess.run([os.environ.get("CC", "gcc"), *oracle.CFLAGS, "-o", str(so), str(c), "-lm"], check=True)
+    env = dict(os.environ, ZERO1_ORACLE_LIB=str(so))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"mutant {name} survived the pins"

@@ -1,0 +1,400 @@
+"""Benchmark of the fused ZeRO-1 optimizer step on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                [--workload NAME] [--no-cpu-baseline] [--no-e2e]
+
+A step is one pass of the whole hot path over one batch: the M replicas'
+bf16 gradients are reduce-scattered (rank-order fp32 sum, scaled by 1/(B*S)),
+the fp32 master/m/v get the AdamW update, the overflow flag is ORed and the
+bf16 parameters are written once (all-gather) - one fused kernel launch.  The
+default workload is the GPT-2-small-sized flat buffer (124,439,808 parameters,
+M = 8 replicas, B = 512); its 5.2 GB of traffic per step is far larger than
+the 129 MB L2, so no flush is needed between steps.
+
+Under torchrun (N > 1) every rank runs an independent replica of the
+workload on its own GPU (weak scaling, no collective on the data path); the
+timed region is bracketed by a barrier and a device synchronize on every
+rank, and the slowest rank's time counts.
+
+Prints one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+METRIC = "params/s and achieved HBM GB/s (% of GB300 peak) per fused ZeRO-1 step"
+KERNEL_SOURCE = os.path.join(ROOT, "zero_sharded_mixed_zero1_gb300", "csrc", "zero1_kernels.cu")
+
+
+# ------------------------------------------------------------ helpers ------
+
+def algorithmic_bytes(n_real: int, n_pad: int, M: int) -> int:
+    """Bytes the step must move: per real parameter M bf16 gradient reads,
+    fp32 master/m/v read and written and one bf16 parameter write (2M + 26);
+    per padding element only the fp32 state (24)."""
+    return n_real * (2 * M + 24 + 2) + n_pad * 24
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def recorded_traffic(workload: str):
+    """dram read+write bytes per launch from the committed ncu summary, if it
+    was taken on the kernel source as it stands now (else None)."""
+    path = os.path.join(ROOT, "profiles", f"k_fused_step_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    tr = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+    if not sha or not tr:
+        return None
+    cur = hashlib.sha256(open(KERNEL_SOURCE, "rb").read()).hexdigest()
+    return int(tr.group(1)) if sha.group(1) == cur else None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while it runs."""
+    FIELDS = ("index,timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 100):
+        self.path = tempfile.mktemp(prefix="clocks_", suffix=".csv")
+        self.proc = None
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}", "--format=csv",
+                 "-lms", str(period_ms)], stdout=self.f, stderr=subprocess.DEVNULL)
+            deadline = time.time() + 5
+            while time.time() < deadline and os.path.getsize(self.path) < 200:
+                time.sleep(0.05)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = list(csv.reader(open(self.path)))
+        if len(rows) < 2:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        head = [h.strip() for h in rows[0]]
+        col = {h.split(" ")[0]: i for i, h in enumerate(head)}
+        sm, smax, reasons, n = [], [], set(), 0
+        for r in rows[1:]:
+            if len(r) != len(head):
+                continue
+            try:
+                ts = time.mktime(time.strptime(r[col["timestamp"]].strip().split(".")[0], "%Y/%m/%d %H:%M:%S"))
+            except ValueError:
+                continue
+            if ts < int(t0) or ts > t1 + 1:
+                continue
+            n += 1
+            sm.append(float(r[col["clocks.sm"]].split()[0]))
+            smax.append(float(r[col["clocks.max.sm"]].split()[0]))
+            for key in ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"):
+                if r[col["clocks_event_reasons." + key]].strip() == "Active":
+                    reasons.add(key)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": n}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """The slowest rank's value (the rank-0 value when world == 1)."""
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------ the oracle leg -----
+
+def oracle_sample_rate(w, elems: int, seconds: float, seed: int = 7):
+    """Time the CPU oracle (single-threaded C, as it stands) on a sample of
+    `elems` elements of workload w, repeating steps for about `seconds`.
+    Returns (elements per second, steps run)."""
+    import oracle  # test infrastructure: only this baseline leg uses it
+    from zero_sharded_mixed_zero1_gb300 import synth
+    grads = [synth.normal_bf16(elems, w.grad_std * w.S, synth.seed_of(seed, r)).view(torch.int16).numpy()
+             .view(np.uint16) for r in range(w.M)]
+    master = synth.normal_f32(elems, w.master_std, synth.seed_of(seed, 99)).numpy()
+    m = np.zeros(elems, np.float32)
+    v = np.zeros(elems, np.float32)
+    params = np.zeros(elems, np.uint16)
+    t, done, t0 = 1, 0, time.perf_counter()
+    while True:
+        hp = oracle.AdamW(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay,
+                          loss_scale=w.S, global_batch=w.B, step=t)
+        oracle.zero1_step(grads, elems, master, m, v, params, hp)
+        done += 1
+        t += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    return elems * done / (time.perf_counter() - t0), done
+
+
+def run_reference(args, w) -> None:
+    """The reference arm: the CPU oracle as it stands, on this host's cores,
+    timed on a bounded sample of the workload per step."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    # size each step's sample so the whole run stays near a minute
+    rate, _ = oracle_sample_rate(w, 1 << 16, 0.5)
+    total_steps = args.steps + args.warmup
+    elems = int(max(4096, min(w.n, rate * 60.0 / max(1, total_steps))))
+    import oracle
+    from zero_sharded_mixed_zero1_gb300 import synth
+    grads = [synth.normal_bf16(elems, w.grad_std * w.S, synth.seed_of(11, r)).view(torch.int16).numpy()
+             .view(np.uint16) for r in range(w.M)]
+    master = synth.normal_f32(elems, w.master_std, synth.seed_of(11, 99)).numpy()
+    m, v = np.zeros(elems, np.float32), np.zeros(elems, np.float32)
+    params = np.zeros(elems, np.uint16)
+
+    def step(t):
+        hp = oracle.AdamW(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay,
+                          loss_scale=w.S, global_batch=w.B, step=t)
+        oracle.zero1_step(grads, elems, master, m, v, params, hp)
+
+    for t in range(1, args.warmup + 1):
+        step(t)
+    t0 = time.perf_counter()
+    for t in range(args.warmup + 1, args.warmup + args.steps + 1):
+        step(t)
+    dt = time.perf_counter() - t0
+    value = elems * args.steps / dt
+    sample = f"{elems} of {w.n} elements per step, M={w.M} replicas, single-threaded C oracle"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": config_of(w),
+        "cpu_baseline": {"value": value, "unit": "params/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------- our arm ---------
+
+def config_of(w) -> dict:
+    return {"workload": w.name, "n": w.n, "M": w.M, "align": w.align, "global_batch": w.B,
+            "loss_scale": w.S, "shards": list(w.shards), "io": "bf16 grads and params, fp32 master/m/v",
+            "l2": "inputs larger than L2 (no flush)", "parallelism": "replicas only"}
+
+
+def run_ours(args, w) -> None:
+    import zero_sharded_mixed_zero1_gb300 as z
+    from zero_sharded_mixed_zero1_gb300 import build as zbuild
+    from zero_sharded_mixed_zero1_gb300 import synth
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    # CPU baseline first (rank 0, N = 1 only), before any GPU work
+    cpu_baseline = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sample = 1 << 22
+        rate, nsteps = oracle_sample_rate(w, sample, args.cpu_seconds)
+        cpu_baseline = {"value": rate, "unit": "params/s", "cores": 1, "kind": "oracle",
+                        "sample": f"{nsteps} steps over {sample} of {w.n} elements, M={w.M} replicas, "
+                                  f"single-threaded C oracle"}
+
+    if rank == 0 and zbuild.is_stale():
+        zbuild.build()
+    barrier(world)
+    z.load()
+
+    plan = z.zero1_plan(w.n, w.M, w.align)
+    sb, se = w.shards
+    base, L, nv = plan.shard_range(sb, se)
+    stream = torch.cuda.current_stream(dev)
+
+    # two gradient sets, alternated step to step (fresh draws per replica)
+    gsets = [[synth.normal_bf16(nv, w.grad_std * w.S, synth.seed_of(w.seed, k, r, rank), dev)
+              for r in range(w.M)] for k in range(2)]
+    master = torch.zeros(L, dtype=torch.float32, device=dev)
+    master[:nv] = synth.normal_f32(nv, w.master_std, synth.seed_of(w.seed, 1, rank), dev)
+    m = torch.zeros(L, dtype=torch.float32, device=dev)
+    v = torch.zeros(L, dtype=torch.float32, device=dev)
+    params = torch.zeros(nv, dtype=torch.bfloat16, device=dev)
+    flag = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def hp(t):
+        return z.AdamW(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay,
+                       loss_scale=w.S, global_batch=w.B, step=t)
+
+    t = 1
+    for _ in range(args.warmup):
+        z.zero1_reduce_scatter_adamw_allgather(plan, sb, se, gsets[t % 2], master, m, v, params, hp(t), flag)
+        t += 1
+    torch.cuda.synchronize(dev)
+
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+    sampler = ClockSampler(dev.index) if rank == 0 else None
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    wall0 = time.time()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        evs[2 * i].record(stream)
+        z.zero1_reduce_scatter_adamw_allgather(plan, sb, se, gsets[t % 2], master, m, v, params, hp(t), flag,
+                                               stream=stream)
+        evs[2 * i + 1].record(stream)
+        t += 1
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    wall1 = time.time()
+    ms_local = start.elapsed_time(end)
+    kernel_ms = float(np.mean([evs[2 * i].elapsed_time(evs[2 * i + 1]) for i in range(args.steps)]))
+    clocks = sampler.summary(wall0, wall1) if sampler else None
+    if sampler:
+        sampler.stop()
+    ms_total = max_over_ranks(ms_local, world)
+    overflow = int(flag.item())
+    del gsets
+
+    # end to end through the public API, from pinned host memory
+    e2e = None
+    if not args.no_e2e:
+        e2e_steps = max(3, min(args.steps, args.e2e_steps))
+        host_g = [synth.normal_bf16(nv, w.grad_std * w.S, synth.seed_of(w.seed, 7, r, rank)).pin_memory()
+                  for r in range(w.M)]
+        dev_g = [torch.empty(nv, dtype=torch.bfloat16, device=dev) for _ in range(w.M)]
+        host_p = torch.empty(nv, dtype=torch.bfloat16).pin_memory()
+        host_f = torch.empty(1, dtype=torch.int32).pin_memory()
+
+        def e2e_step(tt):
+            for r in range(w.M):
+                dev_g[r].copy_(host_g[r], non_blocking=True)
+            z.zero1_reduce_scatter_adamw_allgather(plan, sb, se, dev_g, master, m, v, params, hp(tt), flag)
+            host_p.copy_(params, non_blocking=True)
+            host_f.copy_(flag, non_blocking=True)
+            torch.cuda.current_stream(dev).synchronize()
+
+        e2e_step(t)
+        t += 1
+        barrier(world)
+        w0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            e2e_step(t)
+            t += 1
+        barrier(world)
+        e2e_s = max_over_ranks(time.perf_counter() - w0, world)
+        e2e = {"value": world * nv * e2e_steps / e2e_s, "unit": "params/s",
+               "h2d_bytes_per_step": w.M * nv * 2, "d2h_bytes_per_step": nv * 2 + 4, "steps": e2e_steps}
+
+    if rank != 0:
+        return
+    peaks = measured_peaks()
+    bytes_launch = algorithmic_bytes(nv, L - nv, w.M)
+    achieved = bytes_launch / (kernel_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": world * nv * args.steps / (ms_total * 1e-3),
+        "unit": "params/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_total / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": config_of(w),
+        "hbm_gbs": bytes_launch * args.steps / (ms_total * 1e-3) / 1e9,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "peak_source": peaks["source"],
+                     "traffic": recorded_traffic(w.name), "kernel": f"k_fused_step<M={w.M}>",
+                     "bytes_per_launch": bytes_launch, "kernel_ms": kernel_ms},
+        "cpu_baseline": cpu_baseline,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "overflow_flag": overflow,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None) -> int:
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="gpt2_small_124M_M8")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    sys.path.insert(0, ROOT)
+    from zero_sharded_mixed_zero1_gb300 import workloads as W
+    if args.workload not in W.BY_NAME:
+        ap.error(f"unknown workload {args.workload}; choose from {sorted(W.BY_NAME)}")
+    w = W.BY_NAME[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

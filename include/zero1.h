@@ -1,0 +1,214 @@
+/*
+ * zero1.h - C ABI of libzero1.so, the GB300 (sm_103a) ZeRO Stage-1 optimizer
+ * step: reduce-scatter of M data-parallel replicas' bf16 gradients, AdamW on
+ * the fp32 shard state, all-gather of the updated bf16 parameters.
+ *
+ * On one GPU the M replicas are M gradient buffers in device memory, so the
+ * "collectives" are device-memory traffic inside the kernels.
+ *
+ * Conventions for every call:
+ *  - Pointers named as device pointers must point to device (HBM) memory of
+ *    the current CUDA device; arrays of pointers (grads, outs) are HOST arrays
+ *    of M device pointers.  The caller owns all memory; the library allocates
+ *    nothing and keeps no state between calls.
+ *  - Sizes are in elements.  bf16 buffers hold IEEE binary32 values'
+ *    upper 16 bits (bfloat16); fp32 buffers hold IEEE binary32.
+ *  - Device pointers must be naturally aligned (2 bytes for bf16, 4 for fp32,
+ *    4 for the flag); 16-byte alignment at a common element phase selects the
+ *    128-bit vector path, anything else runs a per-element path.
+ *  - GPU work is enqueued on `stream` (a cudaStream_t; NULL is the legacy
+ *    default stream) and is asynchronous; nothing synchronises the host.
+ *  - Every call validates all arguments before launching anything and
+ *    returns ZERO1_OK (0) or a negative code; on error nothing was enqueued.
+ *    zero1_last_error() gives a one-line reason (per host thread).
+ *
+ * Pages cited (title, section):
+ *  [DP]   "CS336 Lecture 7: Parallelism 1", 朴素数据并行 (naive data parallelism):
+ *         theta_{t+1} = theta_t - eta (1/B) sum_{i<=B} grad L(x_i), the sum
+ *         split across M GPUs with B/M samples each.
+ *  [COLL] same page, 集合通信原语 (All-Reduce, Reduce-Scatter, All-Gather) and
+ *         the identity All-Reduce == Reduce-Scatter + All-Gather.
+ *  [MEM]  same page, 训练内存的详细分析: 16 bytes per parameter = bf16 param 2 +
+ *         bf16 grad 2 + fp32 master 4 + Adam m 4 + Adam v 4.
+ *  [Z1]   same page, ZeRO Stage 1 (优化器状态分片): Reduce-Scatter so GPU i holds
+ *         the summed gradient of shard i, local update of shard i with its
+ *         optimizer state, All-Gather of the updated parameters.
+ *  [PART] "第2章 软件程序与专用硬件的结合" 2.3.4: each of N GPUs keeps 1/N of the
+ *         optimizer state.
+ *  [OPT]  "五维并行实战" 4.2 (AdamW lr, betas, eps, weight_decay; the fp16 loss
+ *         scale block) and 3.2 trap 3 (loss becoming inf under loss scaling).
+ *
+ * Arithmetic (fixed so that results are reproducible bit for bit):
+ *  per element j, all fp32 with one round-to-nearest-even per operation, no
+ *  fused multiply-add, IEEE division and square root:
+ *    s  = f32(g_0[j]) + f32(g_1[j]) + ... + f32(g_{M-1}[j])   (left to right)
+ *    g  = s * inv                                   inv = 1/(B*S)
+ *    m' = beta1*m + (1-beta1)*g
+ *    v' = beta2*v + (1-beta2)*(g*g)
+ *    u  = (m'/(1-beta1^t)) / (sqrt(v'/(1-beta2^t)) + eps)
+ *    w' = w*(1-lr*wd) - lr*u
+ *    param = bf16_round_nearest_even(w')
+ *  The constants inv, 1-beta1, 1-beta2, 1-beta^t and 1-lr*wd are evaluated
+ *  on the host in double (beta^t by the C library's pow) and rounded once to
+ *  float.  Padding elements (global index >= n) take g = +0.
+ */
+#ifndef ZERO1_H
+#define ZERO1_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+/* A cudaStream_t. */
+typedef struct CUstream_st *zero1_stream_t;
+
+/* Status codes. */
+#define ZERO1_OK 0
+#define ZERO1_EINVAL (-1) /* null pointer, empty or out-of-range size, bad hyperparameter */
+#define ZERO1_EALIGN (-2) /* a device pointer is not naturally aligned */
+#define ZERO1_ERANGE (-3) /* M above ZERO1_MAX_REPLICAS or a size the library does not support */
+#define ZERO1_ECUDA (-4)  /* a CUDA runtime call or a kernel launch failed */
+
+/* Largest data-parallel degree M; the M gradient pointers travel by value in
+ * the kernel arguments. */
+#define ZERO1_MAX_REPLICAS 64
+
+#define ZERO1_DTYPE_BF16 0
+#define ZERO1_DTYPE_F32 1
+
+/* Shard plan [PART], [Z1].  n real parameters in one flat buffer, padded to
+ * P = ceil(n / (M*align)) * M*align; shard i is [i*s, (i+1)*s), s = P/M. */
+typedef struct zero1_plan {
+    int64_t n;        /* |theta|, real parameters, >= 1 */
+    int64_t padded_n; /* P */
+    int64_t shard;    /* s = P / M */
+    int32_t M;        /* data-parallel degree (replicas), 1..ZERO1_MAX_REPLICAS */
+    int32_t align;    /* shard alignment unit in elements, >= 1 */
+} zero1_plan_t;
+
+/* AdamW hyperparameters of one step [OPT], the batch of [DP] and the loss
+ * scale: gradients arrive multiplied by loss_scale and summed over the B/M
+ * samples of each replica. */
+typedef struct zero1_adamw {
+    float lr;            /* finite */
+    float beta1, beta2;  /* in [0, 1) */
+    float eps;           /* >= 0 */
+    float weight_decay;  /* finite; decoupled, multiplied by lr */
+    float loss_scale;    /* S > 0, finite */
+    int64_t global_batch;/* B >= M */
+    int64_t step;        /* t >= 1; a skipped step does not advance it */
+} zero1_adamw_t;
+
+/* Build a plan [PART], [Z1].  Host only.  EINVAL if n < 1, align < 1 or
+ * M < 1; ERANGE if M > ZERO1_MAX_REPLICAS or P overflows int64. */
+int zero1_plan(int64_t n, int32_t M, int32_t align, zero1_plan_t *out);
+
+/* Per-tensor pieces of shard `shard_index` when the flat buffer is the
+ * concatenation of n_tensors tensors of tensor_numels[k] elements (their sum
+ * must equal plan->n).  Host only.  Writes up to `cap` pieces: tensor index,
+ * offset inside that tensor, offset inside the shard, length; *count gets the
+ * number of pieces.  Padding belongs to no tensor.  EINVAL on bad arguments,
+ * ERANGE if more than cap pieces are needed. */
+int zero1_plan_segments(const zero1_plan_t *plan, const int64_t *tensor_numels, int32_t n_tensors,
+                        int32_t shard_index, int32_t cap, int64_t *seg_tensor,
+                        int64_t *seg_tensor_offset, int64_t *seg_shard_offset, int64_t *seg_len,
+                        int32_t *count);
+
+/* Bytes per rank [MEM], [Z1]: naive data parallelism keeps 16 bytes of every
+ * parameter on each rank; ZeRO-1 keeps the bf16 parameters and gradients
+ * whole (4 bytes per parameter) and 12 bytes of fp32 state per shard element.
+ * Host only. */
+int zero1_plan_memory(const zero1_plan_t *plan, int64_t *naive_bytes_per_rank,
+                      int64_t *zero1_bytes_per_rank);
+
+/* The fused ZeRO-1 step over shards [shard_begin, shard_end) [Z1], [DP], [MEM]:
+ * one kernel reads each replica's bf16 gradient once, sums the replicas in
+ * rank order, scales by 1/(B*S), updates the fp32 master/m/v in place and
+ * writes the bf16 parameters once.
+ *
+ * Let L = (shard_end - shard_begin) * s, base = shard_begin * s and
+ * nv = clamp(n - base, 0, L) (the real parameters in the range).
+ *  grads[r]  (r < M): device bf16, element `base` of replica r's gradient;
+ *                      nv elements are read.
+ *  master, m, v:      device fp32, the range's state, L elements each, read
+ *                      and written in place.
+ *  params:            device bf16, element `base` of the full parameter
+ *                      buffer; nv elements are written.
+ *  overflow_flag:     device uint32 or NULL.  With skip_if_flag == 0 the
+ *                      kernel ORs 1 into it if any of the nv sums is inf or
+ *                      NaN [OPT] (it never clears it).  With skip_if_flag != 0
+ *                      the kernel only reads it, and if it is nonzero on entry
+ *                      writes nothing at all (run zero1_overflow_check first
+ *                      on the same stream to skip a step globally).
+ * Buffers must not overlap, except grads may alias one another.
+ * EINVAL: NULL pointers, bad range, bad hyperparameters, skip_if_flag with a
+ * NULL flag. */
+int zero1_reduce_scatter_adamw_allgather(const zero1_plan_t *plan, int32_t shard_begin,
+                                         int32_t shard_end, const void *const *grads,
+                                         float *master, float *m, float *v, void *params,
+                                         const zero1_adamw_t *hp, uint32_t *overflow_flag,
+                                         int32_t skip_if_flag, zero1_stream_t stream);
+
+/* Overflow check [OPT]: ORs 1 into *flag (device uint32) if the rank order
+ * fp32 sum of any real element of shards [shard_begin, shard_end) is inf or
+ * NaN.  Reads the same nv elements of grads[r] as the fused step; never
+ * clears the flag. */
+int zero1_overflow_check(const zero1_plan_t *plan, int32_t shard_begin, int32_t shard_end,
+                         const void *const *grads, uint32_t *flag, zero1_stream_t stream);
+
+/* Naive data-parallel All-Reduce [COLL], [DP] over all n elements: every
+ * outs[r] receives (rank order fp32 sum) * scale, as bf16 (round to nearest
+ * even) or fp32 per out_dtype.  grads_in[r]: device bf16, n elements;
+ * outs[r]: device, n elements of out_dtype.  With ZERO1_DTYPE_BF16 outs may
+ * alias grads_in (in place); with ZERO1_DTYPE_F32 they must not overlap. */
+int dp_allreduce(const zero1_plan_t *plan, const void *const *grads_in, void *const *outs,
+                 float scale, int32_t out_dtype, zero1_stream_t stream);
+
+/* Unfused phases [Z1] (for the All-Reduce identity and for comparison with
+ * the fused step).  Same range conventions as the fused step.
+ *
+ * Reduce-scatter [COLL]: out (device, L elements of out_dtype) gets
+ * (rank order fp32 sum) * scale for the nv real elements and +0 for padding;
+ * flag (device, may be NULL) as in zero1_overflow_check. */
+int zero1_reduce_scatter(const zero1_plan_t *plan, int32_t shard_begin, int32_t shard_end,
+                         const void *const *grads, float scale, int32_t out_dtype, void *out,
+                         uint32_t *flag, zero1_stream_t stream);
+
+/* AdamW on L elements of fp32 state given the already scaled fp32 gradient g
+ * (device, L elements); hp->global_batch and hp->loss_scale are validated
+ * but not applied. */
+int zero1_adamw_update(const zero1_plan_t *plan, int32_t shard_begin, int32_t shard_end,
+                       const float *g, float *master, float *m, float *v,
+                       const zero1_adamw_t *hp, zero1_stream_t stream);
+
+/* All-gather of the updated shard range [COLL], [Z1]: params (device bf16,
+ * element `base` of the full buffer) gets bf16(master) for the nv real
+ * elements. */
+int zero1_all_gather(const zero1_plan_t *plan, int32_t shard_begin, int32_t shard_end,
+                     const float *master, void *params, zero1_stream_t stream);
+
+/* All-gather of bf16 shards [COLL]: `shards` (device bf16, the P-element
+ * concatenation of all M shards) is copied, first n elements, into each of
+ * the M outputs outs[r] (device bf16, n elements).  With zero1_reduce_scatter
+ * over all shards this is the right-hand side of All-Reduce ==
+ * Reduce-Scatter + All-Gather. */
+int zero1_all_gather_shards(const zero1_plan_t *plan, const void *shards, void *const *outs,
+                            zero1_stream_t stream);
+
+/* Text of a status code. */
+const char *zero1_strerror(int code);
+
+/* One-line reason for the last non-OK status returned on this host thread. */
+const char *zero1_last_error(void);
+
+/* ABI version, incremented on any incompatible change. */
+int zero1_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZERO1_H */

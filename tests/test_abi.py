@@ -1,0 +1,158 @@
+"""The C-ABI library without a GPU: it loads, exports every function that
+include/zero1.h declares, its host-only plan logic equals the oracle's, and
+every invalid argument is rejected before anything is launched."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import zero_sharded_mixed_zero1_gb300 as z
+from zero_sharded_mixed_zero1_gb300 import build as zbuild
+from zero_sharded_mixed_zero1_gb300 import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    zbuild.build()
+    return z.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "zero1.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^(?:int|const char \*)\s*(\w+)\s*\(", text, flags=re.M)
+
+
+def test_header_declares_the_boundary():
+    names = set(declared_functions())
+    for required in ["zero1_plan", "zero1_reduce_scatter_adamw_allgather", "dp_allreduce",
+                     "zero1_overflow_check"]:
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in zero1.h but not exported"
+    assert lib.zero1_abi_version() == 1
+
+
+@pytest.mark.parametrize("n", [1, 2, 7, 8, 9, 1000, 4099, 10**6 + 3, 1_300_000_000, 7_500_000_000])
+def test_plan_equals_oracle(lib, n):
+    for M in [1, 2, 3, 4, 5, 7, 8, 16, 63, 64]:
+        for a in [1, 8, 128, 1024]:
+            p = z.zero1_plan(n, M, a)
+            assert (p.padded_n, p.shard) == oracle.plan(n, M, a)
+            assert z.zero1_plan_memory(p) == oracle.memory(n, p.shard)
+
+
+def test_segments_equal_oracle(lib):
+    rng = np.random.default_rng(3)
+    cases = [list(W.LLAMA4.tensor_numels)]
+    for _ in range(40):
+        cases.append([int(x) for x in rng.integers(1, 50, int(rng.integers(1, 8)))])
+    for numels in cases:
+        n = sum(numels)
+        for M in [1, 3, 8]:
+            p = z.zero1_plan(n, M, int(rng.choice([1, 8, 128])))
+            for i in range(M):
+                assert z.zero1_plan_segments(p, numels, i) == oracle.segments(numels, p.shard, i)
+
+
+# --------------------------------------------------------- validation ------
+# Fake device addresses: every call below must fail validation on the host,
+# before any CUDA call.  Skipped where a GPU exists (the GPU tests cover the
+# real paths there).
+
+no_gpu = pytest.mark.skipif(torch.cuda.is_available(), reason="host-validation test uses fake pointers")
+
+A = 0x100000  # 16-byte aligned fake address
+
+
+def _ptr_array(vals):
+    return (ctypes.c_void_p * len(vals))(*vals)
+
+
+def _hp(**kw):
+    base = dict(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, loss_scale=1.0,
+                global_batch=8, step=1)
+    base.update(kw)
+    return z.AdamW(**base).c_struct()
+
+
+def _fused(lib, plan, sb=0, se=None, grads=None, master=A, m=A + 4096, v=A + 8192, params=A + 12288,
+           hp=None, flag=None, skip=0):
+    se = plan.M if se is None else se
+    grads = _ptr_array([A + 65536 * (r + 1) for r in range(plan.M)]) if grads is None else grads
+    return lib.zero1_reduce_scatter_adamw_allgather(ctypes.byref(plan), sb, se, grads, master, m, v, params,
+                                                    ctypes.byref(hp or _hp()), flag, skip, None)
+
+
+@no_gpu
+def test_plan_rejects_bad_arguments(lib):
+    p = z.Plan()
+    assert lib.zero1_plan(0, 4, 1, ctypes.byref(p)) == -1
+    assert lib.zero1_plan(10, 0, 1, ctypes.byref(p)) == -1
+    assert lib.zero1_plan(10, 4, 0, ctypes.byref(p)) == -1
+    assert lib.zero1_plan(10, 65, 1, ctypes.byref(p)) == -3
+    assert lib.zero1_plan(2**63 - 6, 64, 1024, ctypes.byref(p)) == -3  # padding overflows int64
+    assert lib.zero1_plan(10, 4, 1, None) == -1
+
+
+@no_gpu
+def test_fused_step_rejects_bad_arguments(lib):
+    plan = z.zero1_plan(1000, 4, 8)
+    assert _fused(lib, plan, sb=0, se=5) == -1            # range beyond M
+    assert _fused(lib, plan, sb=2, se=2) == -1            # empty range
+    assert _fused(lib, plan, sb=-1, se=2) == -1
+    assert _fused(lib, plan, grads=_ptr_array([A, A, None, A])) == -1
+    assert _fused(lib, plan, master=None) == -1
+    assert _fused(lib, plan, master=A + 2) == -2          # fp32 not 4-byte aligned
+    assert _fused(lib, plan, params=A + 1) == -2          # bf16 odd address
+    assert _fused(lib, plan, grads=_ptr_array([A, A + 3, A, A])) == -2
+    assert _fused(lib, plan, hp=_hp(global_batch=2)) == -1  # B < M
+    assert _fused(lib, plan, hp=_hp(step=0)) == -1
+    assert _fused(lib, plan, hp=_hp(loss_scale=0.0)) == -1
+    assert _fused(lib, plan, hp=_hp(beta1=1.0)) == -1
+    assert _fused(lib, plan, hp=_hp(eps=-1.0)) == -1
+    assert _fused(lib, plan, hp=_hp(lr=float("nan"))) == -1
+    assert _fused(lib, plan, flag=None, skip=1) == -1     # skip needs a flag
+    assert _fused(lib, plan, flag=A + 2, skip=0) == -2
+    bad = z.zero1_plan(1000, 4, 8)
+    bad.shard += 1
+    assert _fused(lib, bad) == -1                         # plan not built by zero1_plan
+    assert b"inconsistent" in lib.zero1_last_error()
+
+
+@no_gpu
+def test_other_entry_points_reject_bad_arguments(lib):
+    plan = z.zero1_plan(1000, 2, 8)
+    g = _ptr_array([A, A + 4096])
+    o = _ptr_array([A + 8192, A + 16384])
+    P = ctypes.byref(plan)
+    assert lib.dp_allreduce(P, g, o, 1.0, 7, None) == -1                      # unknown dtype
+    assert lib.dp_allreduce(P, g, o, float("inf"), 0, None) == -1
+    assert lib.dp_allreduce(P, g, _ptr_array([A + 8193, A]), 1.0, 0, None) == -2
+    assert lib.dp_allreduce(P, g, _ptr_array([A, A + 8192]), 1.0, 1, None) == -1  # fp32 out overlaps input
+    assert lib.zero1_overflow_check(P, 0, 2, g, None, None) == -1
+    assert lib.zero1_overflow_check(P, 0, 3, g, A, None) == -1
+    assert lib.zero1_overflow_check(P, 0, 2, g, A + 1, None) == -2
+    assert lib.zero1_reduce_scatter(P, 0, 2, g, 1.0, 5, A, None, None) == -1
+    assert lib.zero1_reduce_scatter(P, 0, 2, g, 1.0, 1, A + 2, None, None) == -2
+    assert lib.zero1_adamw_update(P, 0, 2, None, A, A, A, ctypes.byref(_hp()), None) == -1
+    assert lib.zero1_all_gather(P, 1, 1, A, A, None) == -1
+    assert lib.zero1_all_gather_shards(P, A + 1, o, None) == -2
+    assert lib.zero1_strerror(-2) == b"misaligned device pointer"
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    import zero_sharded_mixed_zero1_gb300._lib as L
+    monkeypatch.setattr(L, "_lib", None)
+    monkeypatch.setattr(L._build, "LIB", str(tmp_path / "missing.so"))
+    with pytest.raises(ImportError):
+        L.load()

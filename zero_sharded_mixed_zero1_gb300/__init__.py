@@ -1,0 +1,28 @@
+"""GB300 (sm_103a) ZeRO Stage-1 optimizer step.
+
+The M data-parallel replicas' bf16 gradients are reduce-scattered in rank
+order and scaled by 1/(B*S); each shard's fp32 master weights and Adam moments
+get an AdamW update; the updated bf16 parameters are all-gathered into the
+full buffer.  One fused CUDA kernel does all three phases.  The C ABI is in
+include/zero1.h; this package is its thin Python binding.
+"""
+from ._lib import (  # noqa: F401
+    ZERO1_DTYPE_BF16,
+    ZERO1_DTYPE_F32,
+    ZERO1_MAX_REPLICAS,
+    AdamW,
+    Plan,
+    Zero1Error,
+    dp_allreduce,
+    library_path,
+    load,
+    zero1_adamw_update,
+    zero1_all_gather,
+    zero1_all_gather_shards,
+    zero1_overflow_check,
+    zero1_plan,
+    zero1_plan_memory,
+    zero1_plan_segments,
+    zero1_reduce_scatter,
+    zero1_reduce_scatter_adamw_allgather,
+)

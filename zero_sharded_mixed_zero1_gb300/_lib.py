@@ -1,0 +1,257 @@
+"""ctypes binding of libzero1.so (include/zero1.h).
+
+Argument marshalling only: every step of the optimizer path runs in the
+library's CUDA kernels.  PyTorch supplies device memory and the current CUDA
+stream.  The binding checks what a C caller would have to guarantee (device,
+dtype, contiguity and that each tensor is long enough) so that a wrong tensor
+raises here instead of reaching the GPU.  There is no fallback: if the
+library is not built, loading fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+from . import build as _build
+
+ZERO1_OK, ZERO1_EINVAL, ZERO1_EALIGN, ZERO1_ERANGE, ZERO1_ECUDA = 0, -1, -2, -3, -4
+ZERO1_MAX_REPLICAS = 64
+ZERO1_DTYPE_BF16, ZERO1_DTYPE_F32 = 0, 1
+
+_lib = None
+
+
+class Zero1Error(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"[{code}] {msg}")
+        self.code = code
+
+
+class Plan(ctypes.Structure):
+    """zero1_plan_t: n real parameters padded to P = multiple of M*align,
+    shard size s = P/M."""
+    _fields_ = [("n", ctypes.c_int64), ("padded_n", ctypes.c_int64), ("shard", ctypes.c_int64),
+                ("M", ctypes.c_int32), ("align", ctypes.c_int32)]
+
+    def shard_range(self, shard_begin: int, shard_end: int) -> tuple[int, int, int]:
+        """(base element, length L, real elements nv) of shards [begin, end)."""
+        base = shard_begin * self.shard
+        L = (shard_end - shard_begin) * self.shard
+        return base, L, max(0, min(self.n - base, L))
+
+    def __repr__(self):
+        return (f"Plan(n={self.n}, padded_n={self.padded_n}, shard={self.shard}, "
+                f"M={self.M}, align={self.align})")
+
+
+class _AdamWStruct(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
+                ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float),
+                ("loss_scale", ctypes.c_float), ("global_batch", ctypes.c_int64),
+                ("step", ctypes.c_int64)]
+
+
+@dataclass(frozen=True)
+class AdamW:
+    """zero1_adamw_t: AdamW hyperparameters, global batch B, loss scale S and
+    step t of one optimizer step."""
+    lr: float = 1e-3
+    beta1: float = 0.9
+    beta2: float = 0.95
+    eps: float = 1e-8
+    weight_decay: float = 0.1
+    loss_scale: float = 1.0
+    global_batch: int = 1
+    step: int = 1
+
+    def c_struct(self) -> _AdamWStruct:
+        return _AdamWStruct(self.lr, self.beta1, self.beta2, self.eps, self.weight_decay,
+                            self.loss_scale, self.global_batch, self.step)
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load() -> ctypes.CDLL:
+    """Load libzero1.so; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise ImportError(f"libzero1.so is not built ({path}); run zero_sharded_mixed_zero1_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+    P = ctypes.POINTER(Plan)
+    A = ctypes.POINTER(_AdamWStruct)
+    sig = {
+        "zero1_plan": [i64, i32, i32, P],
+        "zero1_plan_segments": [P, vp, i32, i32, i32, vp, vp, vp, vp, vp],
+        "zero1_plan_memory": [P, vp, vp],
+        "zero1_reduce_scatter_adamw_allgather": [P, i32, i32, vp, vp, vp, vp, vp, A, vp, i32, vp],
+        "zero1_overflow_check": [P, i32, i32, vp, vp, vp],
+        "dp_allreduce": [P, vp, vp, f32, i32, vp],
+        "zero1_reduce_scatter": [P, i32, i32, vp, f32, i32, vp, vp, vp],
+        "zero1_adamw_update": [P, i32, i32, vp, vp, vp, vp, A, vp],
+        "zero1_all_gather": [P, i32, i32, vp, vp, vp],
+        "zero1_all_gather_shards": [P, vp, vp, vp],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_int
+    lib.zero1_strerror.argtypes = [ctypes.c_int]
+    lib.zero1_strerror.restype = ctypes.c_char_p
+    lib.zero1_last_error.argtypes = []
+    lib.zero1_last_error.restype = ctypes.c_char_p
+    lib.zero1_abi_version.argtypes = []
+    lib.zero1_abi_version.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _check_rc(rc: int) -> None:
+    if rc != ZERO1_OK:
+        lib = load()
+        raise Zero1Error(rc, f"{lib.zero1_strerror(rc).decode()}: {lib.zero1_last_error().decode()}")
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dev(t: torch.Tensor, dtype: torch.dtype, min_numel: int, what: str) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{what}: expected a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{what}: must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{what}: expected {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{what}: must be contiguous")
+    if t.numel() < min_numel:
+        raise ValueError(f"{what}: has {t.numel()} elements, needs at least {min_numel}")
+    return t.data_ptr()
+
+
+def _ptrs(tensors, dtype, min_numel, what) -> ctypes.Array:
+    return (ctypes.c_void_p * len(tensors))(*[_dev(t, dtype, min_numel, f"{what}[{i}]")
+                                              for i, t in enumerate(tensors)])
+
+
+def _replicas(plan: Plan, tensors, what: str) -> None:
+    if len(tensors) != plan.M:
+        raise ValueError(f"{what}: expected M = {plan.M} tensors, got {len(tensors)}")
+
+
+# -- plan ---------------------------------------------------------------------
+
+def zero1_plan(n: int, M: int, align: int = 1) -> Plan:
+    p = Plan()
+    _check_rc(load().zero1_plan(n, M, align, ctypes.byref(p)))
+    return p
+
+
+def zero1_plan_segments(plan: Plan, tensor_numels, shard_index: int):
+    """[(tensor index, offset in tensor, offset in shard, length)]."""
+    nums = (ctypes.c_int64 * len(tensor_numels))(*tensor_numels)
+    cap = len(tensor_numels) + 1
+    outs = [(ctypes.c_int64 * cap)() for _ in range(4)]
+    count = ctypes.c_int32()
+    _check_rc(load().zero1_plan_segments(ctypes.byref(plan), nums, len(tensor_numels), shard_index, cap,
+                                         *outs, ctypes.byref(count)))
+    return [tuple(int(o[i]) for o in outs) for i in range(count.value)]
+
+
+def zero1_plan_memory(plan: Plan) -> tuple[int, int]:
+    """(naive data-parallel bytes per rank, ZeRO-1 bytes per rank)."""
+    a, b = ctypes.c_int64(), ctypes.c_int64()
+    _check_rc(load().zero1_plan_memory(ctypes.byref(plan), ctypes.byref(a), ctypes.byref(b)))
+    return a.value, b.value
+
+
+# -- the step -----------------------------------------------------------------
+
+def zero1_reduce_scatter_adamw_allgather(plan: Plan, shard_begin: int, shard_end: int, grads,
+                                         master, m, v, params, hp: AdamW, overflow_flag=None,
+                                         skip_if_flag: bool = False, stream=None) -> None:
+    """Fused ZeRO-1 step over shards [shard_begin, shard_end).  grads[r] and
+    params start at the range's first global element; master/m/v hold the
+    range's fp32 state (L elements)."""
+    _replicas(plan, grads, "grads")
+    _, L, nv = plan.shard_range(shard_begin, shard_end) if 0 <= shard_begin < shard_end <= plan.M \
+        else (0, 0, 0)
+    g = _ptrs(grads, torch.bfloat16, nv, "grads")
+    flag = 0 if overflow_flag is None else _dev(overflow_flag, torch.int32, 1, "overflow_flag")
+    _check_rc(load().zero1_reduce_scatter_adamw_allgather(
+        ctypes.byref(plan), shard_begin, shard_end, g,
+        _dev(master, torch.float32, L, "master"), _dev(m, torch.float32, L, "m"),
+        _dev(v, torch.float32, L, "v"), _dev(params, torch.bfloat16, nv, "params"),
+        ctypes.byref(hp.c_struct()), flag or None, int(bool(skip_if_flag)), _stream(stream)))
+
+
+def zero1_overflow_check(plan: Plan, shard_begin: int, shard_end: int, grads, flag, stream=None) -> None:
+    _replicas(plan, grads, "grads")
+    _, _, nv = plan.shard_range(shard_begin, shard_end) if 0 <= shard_begin < shard_end <= plan.M \
+        else (0, 0, 0)
+    _check_rc(load().zero1_overflow_check(ctypes.byref(plan), shard_begin, shard_end,
+                                          _ptrs(grads, torch.bfloat16, nv, "grads"),
+                                          _dev(flag, torch.int32, 1, "flag"), _stream(stream)))
+
+
+def dp_allreduce(plan: Plan, grads_in, outs, scale: float = 1.0, stream=None) -> None:
+    """Naive All-Reduce; output dtype (bf16 or fp32) from outs."""
+    _replicas(plan, grads_in, "grads_in")
+    _replicas(plan, outs, "outs")
+    dt = outs[0].dtype
+    code = {torch.bfloat16: ZERO1_DTYPE_BF16, torch.float32: ZERO1_DTYPE_F32}.get(dt)
+    if code is None:
+        raise TypeError("outs must be bfloat16 or float32")
+    _check_rc(load().dp_allreduce(ctypes.byref(plan), _ptrs(grads_in, torch.bfloat16, plan.n, "grads_in"),
+                                  _ptrs(outs, dt, plan.n, "outs"), scale, code, _stream(stream)))
+
+
+def zero1_reduce_scatter(plan: Plan, shard_begin: int, shard_end: int, grads, scale: float, out,
+                         flag=None, stream=None) -> None:
+    _replicas(plan, grads, "grads")
+    _, L, nv = plan.shard_range(shard_begin, shard_end) if 0 <= shard_begin < shard_end <= plan.M \
+        else (0, 0, 0)
+    code = {torch.bfloat16: ZERO1_DTYPE_BF16, torch.float32: ZERO1_DTYPE_F32}.get(out.dtype)
+    if code is None:
+        raise TypeError("out must be bfloat16 or float32")
+    f = 0 if flag is None else _dev(flag, torch.int32, 1, "flag")
+    _check_rc(load().zero1_reduce_scatter(ctypes.byref(plan), shard_begin, shard_end,
+                                          _ptrs(grads, torch.bfloat16, nv, "grads"), scale, code,
+                                          _dev(out, out.dtype, L, "out"), f or None, _stream(stream)))
+
+
+def zero1_adamw_update(plan: Plan, shard_begin: int, shard_end: int, g, master, m, v, hp: AdamW,
+                       stream=None) -> None:
+    _, L, _ = plan.shard_range(shard_begin, shard_end) if 0 <= shard_begin < shard_end <= plan.M \
+        else (0, 0, 0)
+    _check_rc(load().zero1_adamw_update(ctypes.byref(plan), shard_begin, shard_end,
+                                        _dev(g, torch.float32, L, "g"), _dev(master, torch.float32, L, "master"),
+                                        _dev(m, torch.float32, L, "m"), _dev(v, torch.float32, L, "v"),
+                                        ctypes.byref(hp.c_struct()), _stream(stream)))
+
+
+def zero1_all_gather(plan: Plan, shard_begin: int, shard_end: int, master, params, stream=None) -> None:
+    _, L, nv = plan.shard_range(shard_begin, shard_end) if 0 <= shard_begin < shard_end <= plan.M \
+        else (0, 0, 0)
+    _check_rc(load().zero1_all_gather(ctypes.byref(plan), shard_begin, shard_end,
+                                      _dev(master, torch.float32, nv, "master"),
+                                      _dev(params, torch.bfloat16, nv, "params"), _stream(stream)))
+
+
+def zero1_all_gather_shards(plan: Plan, shards, outs, stream=None) -> None:
+    _replicas(plan, outs, "outs")
+    _check_rc(load().zero1_all_gather_shards(ctypes.byref(plan), _dev(shards, torch.bfloat16, plan.n, "shards"),
+                                             _ptrs(outs, torch.bfloat16, plan.n, "outs"), _stream(stream)))

@@ -1,0 +1,39 @@
+// zero1_internal.h - helpers shared by the library's host and CUDA sources
+// (library-internal; not part of the C ABI).
+#pragma once
+
+#include <stdint.h>
+
+#include "zero1.h"
+
+// The per-step constants of the AdamW update, evaluated once on the host
+// ("CS336 Lecture 7: Parallelism 1" naive DP equation for inv = 1/(B*S);
+// "五维并行实战" 4.2 for the AdamW hyperparameters).
+struct Z1Consts {
+    float inv;    // 1 / (B * S)
+    float beta1, omb1;  // beta1, 1 - beta1
+    float beta2, omb2;  // beta2, 1 - beta2
+    float bc1, bc2;     // 1 - beta1^t, 1 - beta2^t
+    float eps;
+    float lr;
+    float cdec;         // 1 - lr * weight_decay
+};
+
+// The element range of shards [shard_begin, shard_end): `base` is its first
+// global element, L its length, nv how many of its elements are real (< n).
+struct Z1Range {
+    int64_t base, L, nv;
+};
+
+// Record a one-line reason for the calling thread and return `code`.
+int z1_fail(int code, const char *fmt, ...);
+
+// Check a plan for internal consistency (as zero1_plan would build it).
+int z1_check_plan(const zero1_plan_t *plan);
+
+// Validate [shard_begin, shard_end) against the plan and fill the range.
+int z1_range(const zero1_plan_t *plan, int32_t shard_begin, int32_t shard_end, Z1Range *out);
+
+// Validate hyperparameters and evaluate the constants: double precision,
+// rounded once to float, beta^t from the C library's pow.
+int z1_adamw_constants(const zero1_adamw_t *hp, int32_t M, Z1Consts *out);

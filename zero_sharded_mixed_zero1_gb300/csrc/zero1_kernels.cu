@@ -1,0 +1,732 @@
+// zero1_kernels.cu - sm_103a kernels of the ZeRO Stage-1 optimizer step and
+// the C-ABI entry points that launch them.
+//
+// The step ("CS336 Lecture 7: Parallelism 1", ZeRO Stage 1: Reduce-Scatter of
+// the gradients so GPU i holds the summed shard i, local update of shard i,
+// All-Gather of the parameters; naive-DP equation for the 1/B mean; the
+// 16 bytes/parameter table for the dtypes) is one streaming pass per element:
+//
+//   M x 2 B bf16 gradient reads  ->  fp32 rank-order sum  ->  x 1/(B*S)
+//   12 B fp32 master/m/v read    ->  AdamW in registers   ->  12 B written
+//                                ->  bf16 parameter, 2 B written once
+//
+// 2M + 26 bytes per parameter and ~60 instructions, so the kernel is bound
+// by HBM bandwidth.  Each thread owns 8 consecutive elements per iteration:
+// one 128-bit load per replica, two per fp32 state array, one 128-bit bf16
+// store.  Gradients go through the non-coherent path without L1 allocation
+// (they are read exactly once).  All loads of an iteration are issued before
+// any arithmetic so each thread keeps (M*16 + 96) bytes in flight; the grid
+// is one resident wave (SMs x resident blocks) walking the range with a
+// grid stride.
+//
+// Arithmetic uses the explicit round-to-nearest intrinsics (__fadd_rn,
+// __fmul_rn, __fdiv_rn, __fsqrt_rn) so no multiply-add is ever contracted and
+// division and square root are IEEE: the results are reproducible bit for bit
+// against any IEEE-754 binary32 evaluation of the same operation sequence.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+#include <cmath>
+#include <type_traits>
+
+#include "zero1.h"
+#include "zero1_internal.h"
+
+namespace {
+
+constexpr int kVec = 8;      // elements per thread per iteration (16 B of bf16)
+constexpr int kBlock = 256;  // threads per block
+
+struct GradPtrs {
+    const uint16_t *p[ZERO1_MAX_REPLICAS];
+};
+struct OutPtrs {
+    void *p[ZERO1_MAX_REPLICAS];
+};
+
+// How a range of L elements is walked: [0, head) per element, then nvec
+// aligned 8-element vectors [head, head + 8*nvec) that are all real
+// parameters, then [head + 8*nvec, L) per element (real below nv, padding
+// above).
+struct Walk {
+    int64_t L, nv, head, nvec;
+};
+
+// ---------------------------------------------------------------- helpers --
+
+__device__ __forceinline__ uint4 ld_stream_u4(const void *p)
+{
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint16_t ld_stream_u16(const uint16_t *p)
+{
+    uint16_t r;
+    asm("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(r) : "l"(p));
+    return r;
+}
+
+// bf16 -> fp32 is exact: the bf16 code is the upper half of the binary32.
+__device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
+__device__ __forceinline__ float bf_one(uint16_t x) { return __uint_as_float((uint32_t)x << 16); }
+
+__device__ __forceinline__ void unpack8(const uint4 q, float s[kVec])
+{
+    s[0] = bf_lo(q.x); s[1] = bf_hi(q.x); s[2] = bf_lo(q.y); s[3] = bf_hi(q.y);
+    s[4] = bf_lo(q.z); s[5] = bf_hi(q.z); s[6] = bf_lo(q.w); s[7] = bf_hi(q.w);
+}
+
+__device__ __forceinline__ void add8(const uint4 q, float s[kVec])
+{
+    s[0] = __fadd_rn(s[0], bf_lo(q.x)); s[1] = __fadd_rn(s[1], bf_hi(q.x));
+    s[2] = __fadd_rn(s[2], bf_lo(q.y)); s[3] = __fadd_rn(s[3], bf_hi(q.y));
+    s[4] = __fadd_rn(s[4], bf_lo(q.z)); s[5] = __fadd_rn(s[5], bf_hi(q.z));
+    s[6] = __fadd_rn(s[6], bf_lo(q.w)); s[7] = __fadd_rn(s[7], bf_hi(q.w));
+}
+
+// fp32 -> bf16, round to nearest even (cvt.rn.bf16x2.f32).
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+__device__ __forceinline__ uint16_t to_bf16(float x)
+{
+    return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+// Rank-order fp32 sum of 8 consecutive elements starting at j (16-byte
+// aligned in every replica).  MT > 0: M == MT known at compile time, all M
+// loads issued before the first add.  MT == 0: any M >= 8, in groups of 8.
+template <int MT>
+__device__ __forceinline__ void sum8(const GradPtrs &g, int M, int64_t j, float s[kVec])
+{
+    if constexpr (MT > 0) {
+        uint4 q[MT];
+#pragma unroll
+        for (int r = 0; r < MT; ++r) q[r] = ld_stream_u4(g.p[r] + j);
+        unpack8(q[0], s);
+#pragma unroll
+        for (int r = 1; r < MT; ++r) add8(q[r], s);
+    } else {
+        uint4 q[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) q[r] = ld_stream_u4(g.p[r] + j);
+        unpack8(q[0], s);
+#pragma unroll
+        for (int r = 1; r < 8; ++r) add8(q[r], s);
+        for (int r0 = 8; r0 < M; r0 += 8) {
+            const int cnt = M - r0 < 8 ? M - r0 : 8;
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                if (k < cnt) q[k] = ld_stream_u4(g.p[r0 + k] + j);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                if (k < cnt) add8(q[k], s);
+        }
+    }
+}
+
+__device__ __forceinline__ float sum1(const GradPtrs &g, int M, int64_t j)
+{
+    float s = bf_one(ld_stream_u16(g.p[0] + j));
+    for (int r = 1; r < M; ++r) s = __fadd_rn(s, bf_one(ld_stream_u16(g.p[r] + j)));
+    return s;
+}
+
+// One AdamW update in fp32, one rounding per operation
+// ("五维并行实战" 4.2 names the optimizer and its hyperparameters):
+//   m' = beta1*m + (1-beta1)*g ; v' = beta2*v + (1-beta2)*(g*g)
+//   u = (m'/bc1) / (sqrt(v'/bc2) + eps) ; w' = w*(1-lr*wd) - lr*u
+__device__ __forceinline__ void adamw1(float g, const Z1Consts &c, float &w, float &m, float &v)
+{
+    const float m1 = __fadd_rn(__fmul_rn(c.beta1, m), __fmul_rn(c.omb1, g));
+    const float v1 = __fadd_rn(__fmul_rn(c.beta2, v), __fmul_rn(c.omb2, __fmul_rn(g, g)));
+    const float mh = __fdiv_rn(m1, c.bc1);
+    const float vh = __fdiv_rn(v1, c.bc2);
+    const float u = __fdiv_rn(mh, __fadd_rn(__fsqrt_rn(vh), c.eps));
+    w = __fsub_rn(__fmul_rn(w, c.cdec), __fmul_rn(c.lr, u));
+    m = m1;
+    v = v1;
+}
+
+__device__ __forceinline__ bool finite(float x) { return isfinite(x); }
+
+// Set *flag |= 1 if any thread of the warp saw a non-finite sum: one vote and
+// at most one atomic per warp.  Called by all threads of every warp.
+__device__ __forceinline__ void warp_flag(uint32_t *flag, bool bad)
+{
+    const unsigned any = __ballot_sync(0xffffffffu, bad);
+    if (any && (threadIdx.x & 31) == 0) atomicOr(flag, 1u);
+}
+
+__device__ __forceinline__ int64_t scalar_index(const Walk &w, int64_t q)
+{
+    return q < w.head ? q : q + w.nvec * kVec;
+}
+
+// ---------------------------------------------------------------- kernels --
+
+// The fused reduce-scatter + AdamW + all-gather.
+template <int MT>
+__global__ void __launch_bounds__(kBlock)
+k_fused_step(const __grid_constant__ GradPtrs g, int M, float *__restrict__ master,
+             float *__restrict__ mom, float *__restrict__ var, uint16_t *__restrict__ params,
+             const Walk w, const Z1Consts c, uint32_t *flag, int skip)
+{
+    if (skip && *reinterpret_cast<volatile uint32_t *>(flag) != 0u) return;
+    const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
+    const int64_t nthr = (int64_t)gridDim.x * kBlock;
+    bool bad = false;
+    for (int64_t i = tid; i < w.nvec; i += nthr) {
+        const int64_t j = w.head + i * kVec;
+        float4 *pw = reinterpret_cast<float4 *>(master + j);
+        float4 *pm = reinterpret_cast<float4 *>(mom + j);
+        float4 *pv = reinterpret_cast<float4 *>(var + j);
+        const float4 w0 = pw[0], w1 = pw[1], m0 = pm[0], m1 = pm[1], v0 = pv[0], v1 = pv[1];
+        float s[kVec];
+        sum8<MT>(g, M, j, s);
+        float ww[kVec] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        float mm[kVec] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+        float vv[kVec] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+        for (int k = 0; k < kVec; ++k) {
+            bad |= !finite(s[k]);
+            adamw1(__fmul_rn(s[k], c.inv), c, ww[k], mm[k], vv[k]);
+        }
+        pw[0] = make_float4(ww[0], ww[1], ww[2], ww[3]);
+        pw[1] = make_float4(ww[4], ww[5], ww[6], ww[7]);
+        pm[0] = make_float4(mm[0], mm[1], mm[2], mm[3]);
+        pm[1] = make_float4(mm[4], mm[5], mm[6], mm[7]);
+        pv[0] = make_float4(vv[0], vv[1], vv[2], vv[3]);
+        pv[1] = make_float4(vv[4], vv[5], vv[6], vv[7]);
+        *reinterpret_cast<uint4 *>(params + j) =
+            make_uint4(pack_bf16x2(ww[0], ww[1]), pack_bf16x2(ww[2], ww[3]),
+                       pack_bf16x2(ww[4], ww[5]), pack_bf16x2(ww[6], ww[7]));
+    }
+    const int64_t ns = w.L - w.nvec * kVec;
+    for (int64_t q = tid; q < ns; q += nthr) {
+        const int64_t j = scalar_index(w, q);
+        float s = 0.0f;
+        if (j < w.nv) {
+            s = sum1(g, M, j);
+            bad |= !finite(s);
+        }
+        float ww = master[j], mm = mom[j], vv = var[j];
+        adamw1(__fmul_rn(s, c.inv), c, ww, mm, vv);
+        master[j] = ww;
+        mom[j] = mm;
+        var[j] = vv;
+        if (j < w.nv) params[j] = to_bf16(ww);
+    }
+    if (flag && !skip) warp_flag(flag, bad);
+}
+
+// Overflow check: flag |= any non-finite rank-order sum over real elements.
+template <int MT>
+__global__ void __launch_bounds__(kBlock)
+k_overflow(const __grid_constant__ GradPtrs g, int M, const Walk w, uint32_t *flag)
+{
+    const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
+    const int64_t nthr = (int64_t)gridDim.x * kBlock;
+    bool bad = false;
+    for (int64_t i = tid; i < w.nvec; i += nthr) {
+        float s[kVec];
+        sum8<MT>(g, M, w.head + i * kVec, s);
+#pragma unroll
+        for (int k = 0; k < kVec; ++k) bad |= !finite(s[k]);
+    }
+    const int64_t ns = w.L - w.nvec * kVec;
+    for (int64_t q = tid; q < ns; q += nthr) {
+        const int64_t j = scalar_index(w, q);
+        if (j < w.nv) bad |= !finite(sum1(g, M, j));
+    }
+    warp_flag(flag, bad);
+}
+
+// Reduce-scatter: out[j] = sum * scale (fp32 or bf16), +0 on padding.
+template <int MT, bool BF16>
+__global__ void __launch_bounds__(kBlock)
+k_reduce_scatter(const __grid_constant__ GradPtrs g, int M, const Walk w, float scale, void *out,
+                 uint32_t *flag)
+{
+    const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
+    const int64_t nthr = (int64_t)gridDim.x * kBlock;
+    bool bad = false;
+    for (int64_t i = tid; i < w.nvec; i += nthr) {
+        const int64_t j = w.head + i * kVec;
+        float s[kVec];
+        sum8<MT>(g, M, j, s);
+#pragma unroll
+        for (int k = 0; k < kVec; ++k) {
+            bad |= !finite(s[k]);
+            s[k] = __fmul_rn(s[k], scale);
+        }
+        if constexpr (BF16) {
+            *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(out) + j) =
+                make_uint4(pack_bf16x2(s[0], s[1]), pack_bf16x2(s[2], s[3]),
+                           pack_bf16x2(s[4], s[5]), pack_bf16x2(s[6], s[7]));
+        } else {
+            float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(out) + j);
+            o[0] = make_float4(s[0], s[1], s[2], s[3]);
+            o[1] = make_float4(s[4], s[5], s[6], s[7]);
+        }
+    }
+    const int64_t ns = w.L - w.nvec * kVec;
+    for (int64_t q = tid; q < ns; q += nthr) {
+        const int64_t j = scalar_index(w, q);
+        float s = 0.0f;
+        if (j < w.nv) {
+            s = sum1(g, M, j);
+            bad |= !finite(s);
+        }
+        s = __fmul_rn(s, scale);
+        if constexpr (BF16) static_cast<uint16_t *>(out)[j] = to_bf16(s);
+        else static_cast<float *>(out)[j] = s;
+    }
+    if (flag) warp_flag(flag, bad);
+}
+
+// AdamW on fp32 state given the scaled fp32 gradient.
+__global__ void __launch_bounds__(kBlock)
+k_adamw(const float *__restrict__ gin, float *__restrict__ master, float *__restrict__ mom,
+        float *__restrict__ var, const Walk w, const Z1Consts c)
+{
+    const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
+    const int64_t nthr = (int64_t)gridDim.x * kBlock;
+    for (int64_t i = tid; i < w.nvec; i += nthr) {
+        const int64_t j = w.head + i * kVec;
+        const float4 *pg = reinterpret_cast<const float4 *>(gin + j);
+        float4 *pw = reinterpret_cast<float4 *>(master + j);
+        float4 *pm = reinterpret_cast<float4 *>(mom + j);
+        float4 *pv = reinterpret_cast<float4 *>(var + j);
+        const float4 g0 = __ldcs(pg), g1 = __ldcs(pg + 1);
+        const float4 w0 = pw[0], w1 = pw[1], m0 = pm[0], m1 = pm[1], v0 = pv[0], v1 = pv[1];
+        float gg[kVec] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+        float ww[kVec] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        float mm[kVec] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+        float vv[kVec] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+        for (int k = 0; k < kVec; ++k) adamw1(gg[k], c, ww[k], mm[k], vv[k]);
+        pw[0] = make_float4(ww[0], ww[1], ww[2], ww[3]);
+        pw[1] = make_float4(ww[4], ww[5], ww[6], ww[7]);
+        pm[0] = make_float4(mm[0], mm[1], mm[2], mm[3]);
+        pm[1] = make_float4(mm[4], mm[5], mm[6], mm[7]);
+        pv[0] = make_float4(vv[0], vv[1], vv[2], vv[3]);
+        pv[1] = make_float4(vv[4], vv[5], vv[6], vv[7]);
+    }
+    const int64_t ns = w.L - w.nvec * kVec;
+    for (int64_t q = tid; q < ns; q += nthr) {
+        const int64_t j = scalar_index(w, q);
+        float ww = master[j], mm = mom[j], vv = var[j];
+        adamw1(gin[j], c, ww, mm, vv);
+        master[j] = ww;
+        mom[j] = mm;
+        var[j] = vv;
+    }
+}
+
+// All-gather of the updated shard: params[j] = bf16(master[j]), real only.
+__global__ void __launch_bounds__(kBlock)
+k_all_gather(const float *__restrict__ master, uint16_t *__restrict__ params, const Walk w)
+{
+    const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
+    const int64_t nthr = (int64_t)gridDim.x * kBlock;
+    for (int64_t i = tid; i < w.nvec; i += nthr) {
+        const int64_t j = w.head + i * kVec;
+        const float4 *pw = reinterpret_cast<const float4 *>(master + j);
+        const float4 a = __ldcs(pw), b = __ldcs(pw + 1);
+        *reinterpret_cast<uint4 *>(params + j) =
+            make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y),
+                       pack_bf16x2(b.z, b.w));
+    }
+    const int64_t ns = w.L - w.nvec * kVec;
+    for (int64_t q = tid; q < ns; q += nthr) {
+        const int64_t j = scalar_index(w, q);
+        if (j < w.nv) params[j] = to_bf16(master[j]);
+    }
+}
+
+// All-gather of bf16 shards into M outputs (real elements only).
+__global__ void __launch_bounds__(kBlock)
+k_all_gather_shards(const uint16_t *__restrict__ shards, const __grid_constant__ OutPtrs o, int M,
+                    const Walk w)
+{
+    const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
+    const int64_t nthr = (int64_t)gridDim.x * kBlock;
+    for (int64_t i = tid; i < w.nvec; i += nthr) {
+        const int64_t j = w.head + i * kVec;
+        const uint4 q = ld_stream_u4(shards + j);
+        for (int r = 0; r < M; ++r) *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(o.p[r]) + j) = q;
+    }
+    const int64_t ns = w.L - w.nvec * kVec;
+    for (int64_t q = tid; q < ns; q += nthr) {
+        const int64_t j = scalar_index(w, q);
+        if (j < w.nv) {
+            const uint16_t x = shards[j];
+            for (int r = 0; r < M; ++r) static_cast<uint16_t *>(o.p[r])[j] = x;
+        }
+    }
+}
+
+// Naive All-Reduce: every output gets sum * scale.  Element j's inputs are
+// all read before any output of j is written (outputs may alias inputs).
+template <int MT, bool BF16>
+__global__ void __launch_bounds__(kBlock)
+k_allreduce(const __grid_constant__ GradPtrs g, const __grid_constant__ OutPtrs o, int M,
+            const Walk w, float scale)
+{
+    const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
+    const int64_t nthr = (int64_t)gridDim.x * kBlock;
+    for (int64_t i = tid; i < w.nvec; i += nthr) {
+        const int64_t j = w.head + i * kVec;
+        float s[kVec];
+        sum8<MT>(g, M, j, s);
+#pragma unroll
+        for (int k = 0; k < kVec; ++k) s[k] = __fmul_rn(s[k], scale);
+        if constexpr (BF16) {
+            const uint4 q = make_uint4(pack_bf16x2(s[0], s[1]), pack_bf16x2(s[2], s[3]),
+                                       pack_bf16x2(s[4], s[5]), pack_bf16x2(s[6], s[7]));
+            for (int r = 0; r < M; ++r) *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(o.p[r]) + j) = q;
+        } else {
+            const float4 a = make_float4(s[0], s[1], s[2], s[3]), b = make_float4(s[4], s[5], s[6], s[7]);
+            for (int r = 0; r < M; ++r) {
+                float4 *op = reinterpret_cast<float4 *>(static_cast<float *>(o.p[r]) + j);
+                op[0] = a;
+                op[1] = b;
+            }
+        }
+    }
+    const int64_t ns = w.L - w.nvec * kVec;
+    for (int64_t q = tid; q < ns; q += nthr) {
+        const int64_t j = scalar_index(w, q);
+        const float s = __fmul_rn(sum1(g, M, j), scale);
+        for (int r = 0; r < M; ++r) {
+            if constexpr (BF16) static_cast<uint16_t *>(o.p[r])[j] = to_bf16(s);
+            else static_cast<float *>(o.p[r])[j] = s;
+        }
+    }
+}
+
+// ------------------------------------------------------------ host side ----
+
+struct ArrayRef {
+    const void *p;
+    int esize;
+};
+
+// Choose the per-element head h in [0, 8) at which every array is 16-byte
+// aligned; if there is none, the whole range runs per element.
+Walk make_walk(int64_t L, int64_t nv, const ArrayRef *a, int count)
+{
+    Walk w{L, nv, 0, 0};
+    for (int h = 0; h < kVec; ++h) {
+        bool ok = true;
+        for (int k = 0; k < count && ok; ++k)
+            ok = (((uintptr_t)a[k].p + (uintptr_t)h * a[k].esize) & 15u) == 0;
+        if (ok) {
+            w.head = h < nv ? h : nv;
+            w.nvec = nv > h ? (nv - h) / kVec : 0;
+            return w;
+        }
+    }
+    return w;
+}
+
+int check_natural(const void *p, int esize, const char *what)
+{
+    if (((uintptr_t)p & (uintptr_t)(esize - 1)) != 0)
+        return z1_fail(ZERO1_EALIGN, "%s is not %d-byte aligned", what, esize);
+    return ZERO1_OK;
+}
+
+int sm_count()
+{
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev < 64) {
+        int c = cache[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev < 64) cache[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+// One resident wave: SMs x resident blocks of this kernel (cached per kernel
+// and device), capped by the work.
+template <class K>
+int grid_for(K kernel, int64_t work_items)
+{
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int per_sm = dev < 64 ? cache[dev].load(std::memory_order_relaxed) : 0;
+    if (per_sm <= 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kBlock, 0) != cudaSuccess ||
+            per_sm <= 0)
+            per_sm = 1;
+        if (dev < 64) cache[dev].store(per_sm, std::memory_order_relaxed);
+    }
+    const int64_t wave = (int64_t)sm_count() * per_sm;
+    int64_t need = (work_items + kBlock - 1) / kBlock;
+    if (need < 1) need = 1;
+    return (int)(need < wave ? need : (wave > 0 ? wave : 1));
+}
+
+int launch_status(const char *what)
+{
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return z1_fail(ZERO1_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+    return ZERO1_OK;
+}
+
+int64_t work_of(const Walk &w)
+{
+    const int64_t ns = w.L - w.nvec * kVec;
+    return w.nvec > ns ? w.nvec : ns;
+}
+
+int load_grads(const zero1_plan_t *plan, const void *const *grads, GradPtrs *g, const char *what)
+{
+    if (!grads) return z1_fail(ZERO1_EINVAL, "%s: grads array is NULL", what);
+    for (int r = 0; r < plan->M; ++r) {
+        if (!grads[r]) return z1_fail(ZERO1_EINVAL, "%s: grads[%d] is NULL", what, r);
+        int rc = check_natural(grads[r], 2, "a gradient pointer");
+        if (rc != ZERO1_OK) return rc;
+        g->p[r] = static_cast<const uint16_t *>(grads[r]);
+    }
+    return ZERO1_OK;
+}
+
+// Call f with std::integral_constant<int, MT>: MT = M for 1..8 (all loads of
+// an 8-element vector issued at once), MT = 0 for M > 8 (groups of 8).
+template <class F>
+void dispatch_m(int M, F &&f)
+{
+    switch (M) {
+    case 1: f(std::integral_constant<int, 1>{}); break;
+    case 2: f(std::integral_constant<int, 2>{}); break;
+    case 3: f(std::integral_constant<int, 3>{}); break;
+    case 4: f(std::integral_constant<int, 4>{}); break;
+    case 5: f(std::integral_constant<int, 5>{}); break;
+    case 6: f(std::integral_constant<int, 6>{}); break;
+    case 7: f(std::integral_constant<int, 7>{}); break;
+    case 8: f(std::integral_constant<int, 8>{}); break;
+    default: f(std::integral_constant<int, 0>{}); break;
+    }
+}
+
+}  // namespace
+
+// ------------------------------------------------------------ C ABI -------
+
+extern "C" int zero1_reduce_scatter_adamw_allgather(const zero1_plan_t *plan, int32_t shard_begin,
+                                                    int32_t shard_end, const void *const *grads,
+                                                    float *master, float *m, float *v, void *params,
+                                                    const zero1_adamw_t *hp, uint32_t *overflow_flag,
+                                                    int32_t skip_if_flag, zero1_stream_t stream)
+{
+    Z1Range r;
+    int rc = z1_range(plan, shard_begin, shard_end, &r);
+    if (rc != ZERO1_OK) return rc;
+    Z1Consts c;
+    if ((rc = z1_adamw_constants(hp, plan->M, &c)) != ZERO1_OK) return rc;
+    if (!master || !m || !v || !params)
+        return z1_fail(ZERO1_EINVAL, "fused step: master, m, v and params must be non-NULL");
+    if (skip_if_flag && !overflow_flag)
+        return z1_fail(ZERO1_EINVAL, "fused step: skip_if_flag needs an overflow flag");
+    GradPtrs g{};
+    if ((rc = load_grads(plan, grads, &g, "fused step")) != ZERO1_OK) return rc;
+    if ((rc = check_natural(master, 4, "master")) || (rc = check_natural(m, 4, "m")) ||
+        (rc = check_natural(v, 4, "v")) || (rc = check_natural(params, 2, "params")) ||
+        (overflow_flag && (rc = check_natural(overflow_flag, 4, "overflow_flag"))))
+        return rc;
+    ArrayRef arr[ZERO1_MAX_REPLICAS + 4] = {{master, 4}, {m, 4}, {v, 4}, {params, 2}};
+    for (int k = 0; k < plan->M; ++k) arr[4 + k] = {grads[k], 2};
+    const Walk w = make_walk(r.L, r.nv, arr, 4 + plan->M);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint16_t *pp = static_cast<uint16_t *>(params);
+    const int M = plan->M;
+    const int skip = skip_if_flag ? 1 : 0;
+    dispatch_m(M, [&](auto mt) {
+        constexpr int MT = decltype(mt)::value;
+        const int grid = grid_for(k_fused_step<MT>, work_of(w));
+        k_fused_step<MT><<<grid, kBlock, 0, st>>>(g, M, master, m, v, pp, w, c, overflow_flag, skip);
+    });
+    return launch_status("fused step launch");
+}
+
+extern "C" int zero1_overflow_check(const zero1_plan_t *plan, int32_t shard_begin, int32_t shard_end,
+                                    const void *const *grads, uint32_t *flag, zero1_stream_t stream)
+{
+    Z1Range r;
+    int rc = z1_range(plan, shard_begin, shard_end, &r);
+    if (rc != ZERO1_OK) return rc;
+    if (!flag) return z1_fail(ZERO1_EINVAL, "overflow check: flag is NULL");
+    if ((rc = check_natural(flag, 4, "flag")) != ZERO1_OK) return rc;
+    GradPtrs g{};
+    if ((rc = load_grads(plan, grads, &g, "overflow check")) != ZERO1_OK) return rc;
+    ArrayRef arr[ZERO1_MAX_REPLICAS];
+    for (int k = 0; k < plan->M; ++k) arr[k] = {grads[k], 2};
+    const Walk w = make_walk(r.nv, r.nv, arr, plan->M);
+    if (w.L == 0) return ZERO1_OK;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int M = plan->M;
+    dispatch_m(M, [&](auto mt) {
+        constexpr int MT = decltype(mt)::value;
+        const int grid = grid_for(k_overflow<MT>, work_of(w));
+        k_overflow<MT><<<grid, kBlock, 0, st>>>(g, M, w, flag);
+    });
+    return launch_status("overflow check launch");
+}
+
+extern "C" int dp_allreduce(const zero1_plan_t *plan, const void *const *grads_in, void *const *outs,
+                            float scale, int32_t out_dtype, zero1_stream_t stream)
+{
+    int rc = z1_check_plan(plan);
+    if (rc != ZERO1_OK) return rc;
+    if (out_dtype != ZERO1_DTYPE_BF16 && out_dtype != ZERO1_DTYPE_F32)
+        return z1_fail(ZERO1_EINVAL, "all-reduce: unknown output dtype %d", out_dtype);
+    if (!std::isfinite(scale)) return z1_fail(ZERO1_EINVAL, "all-reduce: scale is not finite");
+    GradPtrs g{};
+    if ((rc = load_grads(plan, grads_in, &g, "all-reduce")) != ZERO1_OK) return rc;
+    if (!outs) return z1_fail(ZERO1_EINVAL, "all-reduce: outs is NULL");
+    const int M = plan->M;
+    const int osz = out_dtype == ZERO1_DTYPE_BF16 ? 2 : 4;
+    OutPtrs o{};
+    ArrayRef arr[2 * ZERO1_MAX_REPLICAS];
+    for (int k = 0; k < M; ++k) {
+        if (!outs[k]) return z1_fail(ZERO1_EINVAL, "all-reduce: outs[%d] is NULL", k);
+        if ((rc = check_natural(outs[k], osz, "an all-reduce output")) != ZERO1_OK) return rc;
+        if (osz == 4) {
+            const uintptr_t a = (uintptr_t)outs[k], b = a + (uintptr_t)plan->n * 4;
+            for (int q = 0; q < M; ++q) {
+                const uintptr_t c0 = (uintptr_t)grads_in[q], c1 = c0 + (uintptr_t)plan->n * 2;
+                if (a < c1 && c0 < b)
+                    return z1_fail(ZERO1_EINVAL, "all-reduce: fp32 output %d overlaps input %d", k, q);
+            }
+        }
+        o.p[k] = outs[k];
+        arr[k] = {grads_in[k], 2};
+        arr[M + k] = {outs[k], osz};
+    }
+    const Walk w = make_walk(plan->n, plan->n, arr, 2 * M);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    dispatch_m(M, [&](auto mt) {
+        constexpr int MT = decltype(mt)::value;
+        if (osz == 2) {
+            const int grid = grid_for(k_allreduce<MT, true>, work_of(w));
+            k_allreduce<MT, true><<<grid, kBlock, 0, st>>>(g, o, M, w, scale);
+        } else {
+            const int grid = grid_for(k_allreduce<MT, false>, work_of(w));
+            k_allreduce<MT, false><<<grid, kBlock, 0, st>>>(g, o, M, w, scale);
+        }
+    });
+    return launch_status("all-reduce launch");
+}
+
+extern "C" int zero1_reduce_scatter(const zero1_plan_t *plan, int32_t shard_begin, int32_t shard_end,
+                                    const void *const *grads, float scale, int32_t out_dtype, void *out,
+                                    uint32_t *flag, zero1_stream_t stream)
+{
+    Z1Range r;
+    int rc = z1_range(plan, shard_begin, shard_end, &r);
+    if (rc != ZERO1_OK) return rc;
+    if (out_dtype != ZERO1_DTYPE_BF16 && out_dtype != ZERO1_DTYPE_F32)
+        return z1_fail(ZERO1_EINVAL, "reduce-scatter: unknown output dtype %d", out_dtype);
+    if (!std::isfinite(scale)) return z1_fail(ZERO1_EINVAL, "reduce-scatter: scale is not finite");
+    if (!out) return z1_fail(ZERO1_EINVAL, "reduce-scatter: out is NULL");
+    const int osz = out_dtype == ZERO1_DTYPE_BF16 ? 2 : 4;
+    if ((rc = check_natural(out, osz, "reduce-scatter output")) != ZERO1_OK) return rc;
+    if (flag && (rc = check_natural(flag, 4, "flag")) != ZERO1_OK) return rc;
+    GradPtrs g{};
+    if ((rc = load_grads(plan, grads, &g, "reduce-scatter")) != ZERO1_OK) return rc;
+    ArrayRef arr[ZERO1_MAX_REPLICAS + 1] = {{out, osz}};
+    for (int k = 0; k < plan->M; ++k) arr[1 + k] = {grads[k], 2};
+    const Walk w = make_walk(r.L, r.nv, arr, 1 + plan->M);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int M = plan->M;
+    dispatch_m(M, [&](auto mt) {
+        constexpr int MT = decltype(mt)::value;
+        if (osz == 2) {
+            const int grid = grid_for(k_reduce_scatter<MT, true>, work_of(w));
+            k_reduce_scatter<MT, true><<<grid, kBlock, 0, st>>>(g, M, w, scale, out, flag);
+        } else {
+            const int grid = grid_for(k_reduce_scatter<MT, false>, work_of(w));
+            k_reduce_scatter<MT, false><<<grid, kBlock, 0, st>>>(g, M, w, scale, out, flag);
+        }
+    });
+    return launch_status("reduce-scatter launch");
+}
+
+extern "C" int zero1_adamw_update(const zero1_plan_t *plan, int32_t shard_begin, int32_t shard_end,
+                                  const float *gin, float *master, float *m, float *v,
+                                  const zero1_adamw_t *hp, zero1_stream_t stream)
+{
+    Z1Range r;
+    int rc = z1_range(plan, shard_begin, shard_end, &r);
+    if (rc != ZERO1_OK) return rc;
+    Z1Consts c;
+    if ((rc = z1_adamw_constants(hp, plan->M, &c)) != ZERO1_OK) return rc;
+    if (!gin || !master || !m || !v) return z1_fail(ZERO1_EINVAL, "adamw: NULL array");
+    if ((rc = check_natural(gin, 4, "g")) || (rc = check_natural(master, 4, "master")) ||
+        (rc = check_natural(m, 4, "m")) || (rc = check_natural(v, 4, "v")))
+        return rc;
+    const ArrayRef arr[4] = {{gin, 4}, {master, 4}, {m, 4}, {v, 4}};
+    // every element of the range is updated: walk it as if all were real
+    const Walk w = make_walk(r.L, r.L, arr, 4);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int grid = grid_for(k_adamw, work_of(w));
+    k_adamw<<<grid, kBlock, 0, st>>>(gin, master, m, v, w, c);
+    return launch_status("adamw launch");
+}
+
+extern "C" int zero1_all_gather(const zero1_plan_t *plan, int32_t shard_begin, int32_t shard_end,
+                                const float *master, void *params, zero1_stream_t stream)
+{
+    Z1Range r;
+    int rc = z1_range(plan, shard_begin, shard_end, &r);
+    if (rc != ZERO1_OK) return rc;
+    if (!master || !params) return z1_fail(ZERO1_EINVAL, "all-gather: NULL array");
+    if ((rc = check_natural(master, 4, "master")) || (rc = check_natural(params, 2, "params"))) return rc;
+    const ArrayRef arr[2] = {{master, 4}, {params, 2}};
+    const Walk w = make_walk(r.nv, r.nv, arr, 2);
+    if (w.L == 0) return ZERO1_OK;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int grid = grid_for(k_all_gather, work_of(w));
+    k_all_gather<<<grid, kBlock, 0, st>>>(master, static_cast<uint16_t *>(params), w);
+    return launch_status("all-gather launch");
+}
+
+extern "C" int zero1_all_gather_shards(const zero1_plan_t *plan, const void *shards, void *const *outs,
+                                       zero1_stream_t stream)
+{
+    int rc = z1_check_plan(plan);
+    if (rc != ZERO1_OK) return rc;
+    if (!shards || !outs) return z1_fail(ZERO1_EINVAL, "all-gather shards: NULL argument");
+    if ((rc = check_natural(shards, 2, "shards")) != ZERO1_OK) return rc;
+    OutPtrs o{};
+    ArrayRef arr[ZERO1_MAX_REPLICAS + 1] = {{shards, 2}};
+    for (int k = 0; k < plan->M; ++k) {
+        if (!outs[k]) return z1_fail(ZERO1_EINVAL, "all-gather shards: outs[%d] is NULL", k);
+        if ((rc = check_natural(outs[k], 2, "an all-gather output")) != ZERO1_OK) return rc;
+        o.p[k] = outs[k];
+        arr[1 + k] = {outs[k], 2};
+    }
+    const Walk w = make_walk(plan->n, plan->n, arr, 1 + plan->M);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int grid = grid_for(k_all_gather_shards, work_of(w));
+    k_all_gather_shards<<<grid, kBlock, 0, st>>>(static_cast<const uint16_t *>(shards), o, plan->M, w);
+    return launch_status("all-gather shards launch");
+}

@@ -107,8 +107,10 @@ class ClockSampler:
         rows = list(csv.reader(open(self.path)))
         if len(rows) < 2:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        head = [h.strip() for h in rows[0]]
-        col = {h.split(" ")[0]: i for i, h in enumerate(head)}
+        head = rows[0]
+        # nvidia-smi renames some columns in its header (clocks.sm becomes
+        # clocks.current.sm): map by position in the query instead
+        col = {name: i for i, name in enumerate(self.FIELDS.split(","))}
         sm, smax, reasons, n = [], [], set(), 0
         for r in rows[1:]:
             if len(r) != len(head):
@@ -119,9 +121,14 @@ class ClockSampler:
                 continue
             if ts < int(t0) or ts > t1 + 1:
                 continue
+            try:
+                sm_now = float(r[col["clocks.sm"]].split()[0])
+                sm_max = float(r[col["clocks.max.sm"]].split()[0])
+            except (ValueError, IndexError):
+                continue
             n += 1
-            sm.append(float(r[col["clocks.sm"]].split()[0]))
-            smax.append(float(r[col["clocks.max.sm"]].split()[0]))
+            sm.append(sm_now)
+            smax.append(sm_max)
             for key in ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"):
                 if r[col["clocks_event_reasons." + key]].strip() == "Active":
                     reasons.add(key)

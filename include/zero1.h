@@ -143,7 +143,9 @@ int zero1_plan_memory(const zero1_plan_t *plan, int64_t *naive_bytes_per_rank,
  *                      the kernel only reads it, and if it is nonzero on entry
  *                      writes nothing at all (run zero1_overflow_check first
  *                      on the same stream to skip a step globally).
- * Buffers must not overlap, except grads may alias one another.
+ * Buffers must not overlap, except grads may alias one another.  When the
+ * range holds no real parameter (nv == 0: all padding) grads and params are
+ * not touched and may be NULL.
  * EINVAL: NULL pointers, bad range, bad hyperparameters, skip_if_flag with a
  * NULL flag. */
 int zero1_reduce_scatter_adamw_allgather(const zero1_plan_t *plan, int32_t shard_begin,
@@ -154,8 +156,8 @@ int zero1_reduce_scatter_adamw_allgather(const zero1_plan_t *plan, int32_t shard
 
 /* Overflow check [OPT]: ORs 1 into *flag (device uint32) if the rank order
  * fp32 sum of any real element of shards [shard_begin, shard_end) is inf or
- * NaN.  Reads the same nv elements of grads[r] as the fused step; never
- * clears the flag. */
+ * NaN.  Reads the same nv elements of grads[r] as the fused step (none, and
+ * grads may be NULL, when nv == 0); never clears the flag. */
 int zero1_overflow_check(const zero1_plan_t *plan, int32_t shard_begin, int32_t shard_end,
                          const void *const *grads, uint32_t *flag, zero1_stream_t stream);
 

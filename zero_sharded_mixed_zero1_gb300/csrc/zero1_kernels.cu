@@ -542,18 +542,20 @@ extern "C" int zero1_reduce_scatter_adamw_allgather(const zero1_plan_t *plan, in
     if (rc != ZERO1_OK) return rc;
     Z1Consts c;
     if ((rc = z1_adamw_constants(hp, plan->M, &c)) != ZERO1_OK) return rc;
-    if (!master || !m || !v || !params)
-        return z1_fail(ZERO1_EINVAL, "fused step: master, m, v and params must be non-NULL");
+    if (!master || !m || !v)
+        return z1_fail(ZERO1_EINVAL, "fused step: master, m and v must be non-NULL");
+    if (r.nv > 0 && !params)
+        return z1_fail(ZERO1_EINVAL, "fused step: params must be non-NULL when the range holds parameters");
     if (skip_if_flag && !overflow_flag)
         return z1_fail(ZERO1_EINVAL, "fused step: skip_if_flag needs an overflow flag");
     GradPtrs g{};
-    if ((rc = load_grads(plan, grads, &g, "fused step")) != ZERO1_OK) return rc;
+    if (r.nv > 0 && (rc = load_grads(plan, grads, &g, "fused step")) != ZERO1_OK) return rc;
     if ((rc = check_natural(master, 4, "master")) || (rc = check_natural(m, 4, "m")) ||
         (rc = check_natural(v, 4, "v")) || (rc = check_natural(params, 2, "params")) ||
         (overflow_flag && (rc = check_natural(overflow_flag, 4, "overflow_flag"))))
         return rc;
     ArrayRef arr[ZERO1_MAX_REPLICAS + 4] = {{master, 4}, {m, 4}, {v, 4}, {params, 2}};
-    for (int k = 0; k < plan->M; ++k) arr[4 + k] = {grads[k], 2};
+    for (int k = 0; k < plan->M; ++k) arr[4 + k] = {g.p[k], 2};
     const Walk w = make_walk(r.L, r.nv, arr, 4 + plan->M);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     uint16_t *pp = static_cast<uint16_t *>(params);
@@ -575,12 +577,12 @@ extern "C" int zero1_overflow_check(const zero1_plan_t *plan, int32_t shard_begi
     if (rc != ZERO1_OK) return rc;
     if (!flag) return z1_fail(ZERO1_EINVAL, "overflow check: flag is NULL");
     if ((rc = check_natural(flag, 4, "flag")) != ZERO1_OK) return rc;
+    if (r.nv == 0) return ZERO1_OK;
     GradPtrs g{};
     if ((rc = load_grads(plan, grads, &g, "overflow check")) != ZERO1_OK) return rc;
     ArrayRef arr[ZERO1_MAX_REPLICAS];
     for (int k = 0; k < plan->M; ++k) arr[k] = {grads[k], 2};
     const Walk w = make_walk(r.nv, r.nv, arr, plan->M);
-    if (w.L == 0) return ZERO1_OK;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const int M = plan->M;
     dispatch_m(M, [&](auto mt) {
@@ -651,9 +653,9 @@ extern "C" int zero1_reduce_scatter(const zero1_plan_t *plan, int32_t shard_begi
     if ((rc = check_natural(out, osz, "reduce-scatter output")) != ZERO1_OK) return rc;
     if (flag && (rc = check_natural(flag, 4, "flag")) != ZERO1_OK) return rc;
     GradPtrs g{};
-    if ((rc = load_grads(plan, grads, &g, "reduce-scatter")) != ZERO1_OK) return rc;
+    if (r.nv > 0 && (rc = load_grads(plan, grads, &g, "reduce-scatter")) != ZERO1_OK) return rc;
     ArrayRef arr[ZERO1_MAX_REPLICAS + 1] = {{out, osz}};
-    for (int k = 0; k < plan->M; ++k) arr[1 + k] = {grads[k], 2};
+    for (int k = 0; k < plan->M; ++k) arr[1 + k] = {g.p[k], 2};
     const Walk w = make_walk(r.L, r.nv, arr, 1 + plan->M);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const int M = plan->M;
@@ -698,11 +700,11 @@ extern "C" int zero1_all_gather(const zero1_plan_t *plan, int32_t shard_begin, i
     Z1Range r;
     int rc = z1_range(plan, shard_begin, shard_end, &r);
     if (rc != ZERO1_OK) return rc;
+    if (r.nv == 0) return ZERO1_OK;
     if (!master || !params) return z1_fail(ZERO1_EINVAL, "all-gather: NULL array");
     if ((rc = check_natural(master, 4, "master")) || (rc = check_natural(params, 2, "params"))) return rc;
     const ArrayRef arr[2] = {{master, 4}, {params, 2}};
     const Walk w = make_walk(r.nv, r.nv, arr, 2);
-    if (w.L == 0) return ZERO1_OK;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const int grid = grid_for(k_all_gather, work_of(w));
     k_all_gather<<<grid, kBlock, 0, st>>>(master, static_cast<uint16_t *>(params), w);

@@ -175,43 +175,87 @@ __device__ __forceinline__ int64_t scalar_index(const Walk &w, int64_t q)
 
 // ---------------------------------------------------------------- kernels --
 
-// The fused reduce-scatter + AdamW + all-gather.
-template <int MT>
-__global__ void __launch_bounds__(kBlock)
-k_fused_step(const __grid_constant__ GradPtrs g, int M, float *__restrict__ master,
-             float *__restrict__ mom, float *__restrict__ var, uint16_t *__restrict__ params,
-             const Walk w, const Z1Consts c, uint32_t *flag, int skip)
+// fp32 state loads that do not allocate in L1 (each line is read once) and
+// streaming stores (.cs: the written lines are not read again by this kernel).
+__device__ __forceinline__ float4 ld_state(const float *p)
 {
-    if (skip && *reinterpret_cast<volatile uint32_t *>(flag) != 0u) return;
-    const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
-    const int64_t nthr = (int64_t)gridDim.x * kBlock;
-    bool bad = false;
-    for (int64_t i = tid; i < w.nvec; i += nthr) {
-        const int64_t j = w.head + i * kVec;
-        float4 *pw = reinterpret_cast<float4 *>(master + j);
-        float4 *pm = reinterpret_cast<float4 *>(mom + j);
-        float4 *pv = reinterpret_cast<float4 *>(var + j);
-        const float4 w0 = pw[0], w1 = pw[1], m0 = pm[0], m1 = pm[1], v0 = pv[0], v1 = pv[1];
-        float s[kVec];
-        sum8<MT>(g, M, j, s);
-        float ww[kVec] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-        float mm[kVec] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-        float vv[kVec] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    float4 r;
+    asm("ld.global.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
+        : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+        : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ void st_stream(float *p, float a, float b, float c, float d)
+{
+    __stcs(reinterpret_cast<float4 *>(p), make_float4(a, b, c, d));
+}
+
+// AdamW on one 8-element vector whose replica sums are in s, then the
+// streaming stores of master/m/v and the bf16 parameters.
+__device__ __forceinline__ void store_vec(const float s[kVec], float4 w0, float4 w1, float4 m0, float4 m1,
+                                          float4 v0, float4 v1, float *pw, float *pm, float *pv, uint16_t *pp,
+                                          const Z1Consts &c, bool &bad)
+{
+    float ww[kVec] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+    float mm[kVec] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+    float vv[kVec] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
-        for (int k = 0; k < kVec; ++k) {
-            bad |= !finite(s[k]);
-            adamw1(__fmul_rn(s[k], c.inv), c, ww[k], mm[k], vv[k]);
-        }
-        pw[0] = make_float4(ww[0], ww[1], ww[2], ww[3]);
-        pw[1] = make_float4(ww[4], ww[5], ww[6], ww[7]);
-        pm[0] = make_float4(mm[0], mm[1], mm[2], mm[3]);
-        pm[1] = make_float4(mm[4], mm[5], mm[6], mm[7]);
-        pv[0] = make_float4(vv[0], vv[1], vv[2], vv[3]);
-        pv[1] = make_float4(vv[4], vv[5], vv[6], vv[7]);
-        *reinterpret_cast<uint4 *>(params + j) =
-            make_uint4(pack_bf16x2(ww[0], ww[1]), pack_bf16x2(ww[2], ww[3]),
-                       pack_bf16x2(ww[4], ww[5]), pack_bf16x2(ww[6], ww[7]));
+    for (int k = 0; k < kVec; ++k) {
+        bad |= !finite(s[k]);
+        adamw1(__fmul_rn(s[k], c.inv), c, ww[k], mm[k], vv[k]);
     }
+    st_stream(pw, ww[0], ww[1], ww[2], ww[3]);
+    st_stream(pw + 4, ww[4], ww[5], ww[6], ww[7]);
+    st_stream(pm, mm[0], mm[1], mm[2], mm[3]);
+    st_stream(pm + 4, mm[4], mm[5], mm[6], mm[7]);
+    st_stream(pv, vv[0], vv[1], vv[2], vv[3]);
+    st_stream(pv + 4, vv[4], vv[5], vv[6], vv[7]);
+    __stcs(reinterpret_cast<uint4 *>(pp),
+           make_uint4(pack_bf16x2(ww[0], ww[1]), pack_bf16x2(ww[2], ww[3]), pack_bf16x2(ww[4], ww[5]),
+                      pack_bf16x2(ww[6], ww[7])));
+}
+
+// One 8-element vector of the fused step for M = MT <= 8 whose loads are in q
+// and the six state registers.
+template <int MT>
+__device__ __forceinline__ void fused_vec(const GradPtrs &, int, int64_t j, const uint4 *q, float4 w0, float4 w1,
+                                          float4 m0, float4 m1, float4 v0, float4 v1, float *master, float *mom,
+                                          float *var, uint16_t *params, const Z1Consts &c, bool &bad)
+{
+    float s[kVec];
+    unpack8(q[0], s);
+#pragma unroll
+    for (int r = 1; r < MT; ++r) add8(q[r], s);
+    store_vec(s, w0, w1, m0, m1, v0, v1, master + j, mom + j, var + j, params + j, c, bad);
+}
+
+// The loads of one 8-element vector for M <= 8: every replica's gradient
+// vector, then the fp32 state.
+template <int MT>
+struct VecLoads {
+    uint4 q[MT];
+    float4 w0, w1, m0, m1, v0, v1;
+    __device__ __forceinline__ void load(const GradPtrs &g, const float *master, const float *mom,
+                                         const float *var, int64_t j)
+    {
+#pragma unroll
+        for (int r = 0; r < MT; ++r) q[r] = ld_stream_u4(g.p[r] + j);
+        w0 = ld_state(master + j);
+        w1 = ld_state(master + j + 4);
+        m0 = ld_state(mom + j);
+        m1 = ld_state(mom + j + 4);
+        v0 = ld_state(var + j);
+        v1 = ld_state(var + j + 4);
+    }
+};
+
+// Per-element remainder of the fused step: [0, head) and the tail after the
+// vector body (real elements below nv, padding above).
+__device__ __forceinline__ void fused_scalar_rest(const GradPtrs &g, int M, float *master, float *mom,
+                                                  float *var, uint16_t *params, const Walk &w,
+                                                  const Z1Consts &c, int64_t tid, int64_t nthr, bool &bad)
+{
     const int64_t ns = w.L - w.nvec * kVec;
     for (int64_t q = tid; q < ns; q += nthr) {
         const int64_t j = scalar_index(w, q);
@@ -227,6 +271,80 @@ k_fused_step(const __grid_constant__ GradPtrs g, int M, float *__restrict__ mast
         var[j] = vv;
         if (j < w.nv) params[j] = to_bf16(ww);
     }
+}
+
+// The fused reduce-scatter + AdamW + all-gather for M <= 8 (M = MT known at
+// compile time).
+//
+// Shape chosen by measurement on GB300 (CUDA events through this entry point
+// on the 124M-parameter M = 8 workload): each thread issues all loads of its
+// next vector before computing the current one, so two vectors - 2 x
+// (16M + 96) bytes - are in flight per thread; the register budget this needs
+// (launch bounds of one block per SM) beat higher occupancy with one vector
+// in flight.  fp32 state is read with L1::no_allocate and every store is .cs.
+template <int MT>
+__global__ void __launch_bounds__(kBlock, 1)
+k_fused_step(const __grid_constant__ GradPtrs g, int M, float *__restrict__ master,
+             float *__restrict__ mom, float *__restrict__ var, uint16_t *__restrict__ params,
+             const Walk w, const Z1Consts c, uint32_t *flag, int skip)
+{
+    if (skip && *reinterpret_cast<volatile uint32_t *>(flag) != 0u) return;
+    const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
+    const int64_t nthr = (int64_t)gridDim.x * kBlock;
+    bool bad = false;
+    VecLoads<MT> cur, nxt;
+    int64_t i = tid;
+    if (i < w.nvec) cur.load(g, master, mom, var, w.head + i * kVec);
+    for (; i < w.nvec; i += nthr) {
+        const int64_t j = w.head + i * kVec;
+        const bool more = i + nthr < w.nvec;
+        if (more) nxt.load(g, master, mom, var, j + nthr * kVec);
+        fused_vec<MT>(g, M, j, cur.q, cur.w0, cur.w1, cur.m0, cur.m1, cur.v0, cur.v1, master, mom, var,
+                      params, c, bad);
+        if (more) cur = nxt;
+    }
+    fused_scalar_rest(g, M, master, mom, var, params, w, c, tid, nthr, bad);
+    if (flag && !skip) warp_flag(flag, bad);
+}
+
+// The fused step for M > 8: the state is read first with the default
+// policy, then the replicas in groups of 8 into the same registers; stores
+// are .cs.  Three resident blocks per SM (at most 85 registers).  Measured on
+// the 64-replica shard: this shape beat deeper pipelining, fewer resident
+// blocks and L1::no_allocate state loads.
+__global__ void __launch_bounds__(kBlock, 3)
+k_fused_step_grouped(const __grid_constant__ GradPtrs g, int M, float *__restrict__ master,
+                     float *__restrict__ mom, float *__restrict__ var, uint16_t *__restrict__ params,
+                     const Walk w, const Z1Consts c, uint32_t *flag, int skip)
+{
+    if (skip && *reinterpret_cast<volatile uint32_t *>(flag) != 0u) return;
+    const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
+    const int64_t nthr = (int64_t)gridDim.x * kBlock;
+    bool bad = false;
+    for (int64_t i = tid; i < w.nvec; i += nthr) {
+        const int64_t j = w.head + i * kVec;
+        const float4 *pw = reinterpret_cast<const float4 *>(master + j);
+        const float4 *pm = reinterpret_cast<const float4 *>(mom + j);
+        const float4 *pv = reinterpret_cast<const float4 *>(var + j);
+        const float4 w0 = pw[0], w1 = pw[1], m0 = pm[0], m1 = pm[1], v0 = pv[0], v1 = pv[1];
+        float s[kVec];
+        uint4 q[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) q[r] = ld_stream_u4(g.p[r] + j);
+        unpack8(q[0], s);
+#pragma unroll
+        for (int r = 1; r < 8; ++r) add8(q[r], s);
+        for (int r0 = 8; r0 < M; r0 += 8) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                if (r0 + k < M) q[k] = ld_stream_u4(g.p[r0 + k] + j);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                if (r0 + k < M) add8(q[k], s);
+        }
+        store_vec(s, w0, w1, m0, m1, v0, v1, master + j, mom + j, var + j, params + j, c, bad);
+    }
+    fused_scalar_rest(g, M, master, mom, var, params, w, c, tid, nthr, bad);
     if (flag && !skip) warp_flag(flag, bad);
 }
 
@@ -561,11 +679,18 @@ extern "C" int zero1_reduce_scatter_adamw_allgather(const zero1_plan_t *plan, in
     uint16_t *pp = static_cast<uint16_t *>(params);
     const int M = plan->M;
     const int skip = skip_if_flag ? 1 : 0;
-    dispatch_m(M, [&](auto mt) {
-        constexpr int MT = decltype(mt)::value;
-        const int grid = grid_for(k_fused_step<MT>, work_of(w));
-        k_fused_step<MT><<<grid, kBlock, 0, st>>>(g, M, master, m, v, pp, w, c, overflow_flag, skip);
-    });
+    if (M > 8) {
+        const int grid = grid_for(k_fused_step_grouped, work_of(w));
+        k_fused_step_grouped<<<grid, kBlock, 0, st>>>(g, M, master, m, v, pp, w, c, overflow_flag, skip);
+    } else {
+        dispatch_m(M, [&](auto mt) {
+            constexpr int MT = decltype(mt)::value;
+            if constexpr (MT > 0) {
+                const int grid = grid_for(k_fused_step<MT>, work_of(w));
+                k_fused_step<MT><<<grid, kBlock, 0, st>>>(g, M, master, m, v, pp, w, c, overflow_flag, skip);
+            }
+        });
+    }
     return launch_status("fused step launch");
 }
 

@@ -230,10 +230,13 @@ def run_reference(args, w) -> None:
 
 # --------------------------------------------------------- our arm ---------
 
-def config_of(w) -> dict:
-    return {"workload": w.name, "n": w.n, "M": w.M, "align": w.align, "global_batch": w.B,
-            "loss_scale": w.S, "shards": list(w.shards), "io": "bf16 grads and params, fp32 master/m/v",
-            "l2": "inputs larger than L2 (no flush)", "parallelism": "replicas only"}
+def config_of(w, state_on_host: bool = False) -> dict:
+    c = {"workload": w.name, "n": w.n, "M": w.M, "align": w.align, "global_batch": w.B,
+         "loss_scale": w.S, "shards": list(w.shards), "io": "bf16 grads and params, fp32 master/m/v",
+         "l2": "inputs larger than L2 (no flush)", "parallelism": "replicas only"}
+    if state_on_host:
+        c["state"] = "fp32 master/m/v in pinned host memory (offload)"
+    return c
 
 
 def run_ours(args, w) -> None:
@@ -275,6 +278,8 @@ def run_ours(args, w) -> None:
     master[:nv] = synth.normal_f32(nv, w.master_std, synth.seed_of(w.seed, 1, rank), dev)
     m = torch.zeros(L, dtype=torch.float32, device=dev)
     v = torch.zeros(L, dtype=torch.float32, device=dev)
+    if args.state_on_host:        # optimizer-state offload: master/m/v in pinned host memory
+        master, m, v = (x.cpu().pin_memory() for x in (master, m, v))
     params = torch.zeros(nv, dtype=torch.bfloat16, device=dev)
     flag = torch.zeros(1, dtype=torch.int32, device=dev)
 
@@ -314,17 +319,26 @@ def run_ours(args, w) -> None:
     overflow = int(flag.item())
     del gsets
 
-    # end to end through the public API, from pinned host memory
-    e2e = None
+    # end to end through the public API, from pinned host memory: the kernel
+    # reads each step's gradients from pinned host buffers over the host link
+    # (no staging copy) and writes the bf16 parameters to a pinned host
+    # buffer; the flag is read back; the step ends with a stream synchronize.
+    e2e = e2e_copy = None
     if not args.no_e2e:
         e2e_steps = max(3, min(args.steps, args.e2e_steps))
         host_g = [synth.normal_bf16(nv, w.grad_std * w.S, synth.seed_of(w.seed, 7, r, rank)).pin_memory()
                   for r in range(w.M)]
-        dev_g = [torch.empty(nv, dtype=torch.bfloat16, device=dev) for _ in range(w.M)]
         host_p = torch.empty(nv, dtype=torch.bfloat16).pin_memory()
         host_f = torch.empty(1, dtype=torch.int32).pin_memory()
 
         def e2e_step(tt):
+            z.zero1_reduce_scatter_adamw_allgather(plan, sb, se, host_g, master, m, v, host_p, hp(tt), flag)
+            host_f.copy_(flag, non_blocking=True)
+            torch.cuda.current_stream(dev).synchronize()
+
+        dev_g = [torch.empty(nv, dtype=torch.bfloat16, device=dev) for _ in range(w.M)]
+
+        def copy_step(tt):
             for r in range(w.M):
                 dev_g[r].copy_(host_g[r], non_blocking=True)
             z.zero1_reduce_scatter_adamw_allgather(plan, sb, se, dev_g, master, m, v, params, hp(tt), flag)
@@ -332,17 +346,26 @@ def run_ours(args, w) -> None:
             host_f.copy_(flag, non_blocking=True)
             torch.cuda.current_stream(dev).synchronize()
 
-        e2e_step(t)
-        t += 1
-        barrier(world)
-        w0 = time.perf_counter()
-        for _ in range(e2e_steps):
-            e2e_step(t)
+        def timed(fn):
+            nonlocal t
+            fn(t)
             t += 1
-        barrier(world)
-        e2e_s = max_over_ranks(time.perf_counter() - w0, world)
+            barrier(world)
+            w0 = time.perf_counter()
+            for _ in range(e2e_steps):
+                fn(t)
+                t += 1
+            barrier(world)
+            return max_over_ranks(time.perf_counter() - w0, world)
+
+        e2e_s = timed(e2e_step)
+        copy_s = timed(copy_step)
         e2e = {"value": world * nv * e2e_steps / e2e_s, "unit": "params/s",
-               "h2d_bytes_per_step": w.M * nv * 2, "d2h_bytes_per_step": nv * 2 + 4, "steps": e2e_steps}
+               "h2d_bytes_per_step": w.M * nv * 2, "d2h_bytes_per_step": nv * 2 + 4, "steps": e2e_steps,
+               "transfer": "kernel reads pinned host gradients and writes pinned host params over the host link"}
+        e2e_copy = {"value": world * nv * e2e_steps / copy_s, "unit": "params/s",
+                    "transfer": "cudaMemcpyAsync of the gradients to HBM, step, copy of the params back"}
+        del dev_g, host_g
 
     if rank != 0:
         return
@@ -362,7 +385,7 @@ def run_ours(args, w) -> None:
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
-        "config": config_of(w),
+        "config": config_of(w, args.state_on_host),
         "hbm_gbs": bytes_launch * args.steps / (ms_total * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "peak_source": peaks["source"],
@@ -370,6 +393,7 @@ def run_ours(args, w) -> None:
                      "bytes_per_launch": bytes_launch, "kernel_ms": kernel_ms},
         "cpu_baseline": cpu_baseline,
         "e2e": e2e,
+        "e2e_copy_then_step": e2e_copy,
         "gpu_launches": args.steps,
         "clocks": clocks,
         "overflow_flag": overflow,
@@ -388,6 +412,8 @@ def main(argv=None) -> int:
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--state-on-host", action="store_true",
+                    help="keep fp32 master/m/v in pinned host memory (optimizer-state offload)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

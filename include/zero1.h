@@ -7,9 +7,15 @@
  * "collectives" are device-memory traffic inside the kernels.
  *
  * Conventions for every call:
- *  - Pointers named as device pointers must point to device (HBM) memory of
- *    the current CUDA device; arrays of pointers (grads, outs) are HOST arrays
- *    of M device pointers.  The caller owns all memory; the library allocates
+ *  - Pointers named as device pointers must be addressable by the current
+ *    CUDA device: HBM of that device, or pinned (page-locked) host memory,
+ *    which the unified address space maps at the same address.  On GB300 the
+ *    kernels then read and write host memory directly over NVLink-C2C: the
+ *    gradients can stream from host memory without a staging copy, the bf16
+ *    parameters can land in host memory, and master/m/v can live in host
+ *    memory (optimizer-state offload).  Such accesses run at the host link's
+ *    speed instead of HBM's.  Arrays of pointers (grads, outs) are HOST arrays
+ *    of M such pointers.  The caller owns all memory; the library allocates
  *    nothing and keeps no state between calls.
  *  - Sizes are in elements.  bf16 buffers hold IEEE binary32 values'
  *    upper 16 bits (bfloat16); fp32 buffers hold IEEE binary32.

@@ -1,0 +1,78 @@
+"""Pinned host buffers passed straight to the kernels (read and written over
+the host link, no staging copy): the results must be bit-identical to the
+same step on HBM buffers, and to the oracle.
+
+Covers gradients streamed from host memory (the end-to-end path), bf16
+parameters written to host memory, and fp32 master/m/v kept in host memory
+(optimizer-state offload, "五维并行实战" section 4.2 offload_optimizer)."""
+import numpy as np
+import pytest
+import torch
+
+import zero_sharded_mixed_zero1_gb300 as z
+from zero_sharded_mixed_zero1_gb300 import synth
+from gpu_helpers import assert_bf16_bits, assert_f32_bits, f32, oracle_hp, u16
+from test_gpu_parity import make_grads, make_state, oracle_step
+
+pytestmark = pytest.mark.gpu
+
+
+def pinned(t: torch.Tensor) -> torch.Tensor:
+    return t.cpu().pin_memory()
+
+
+@pytest.mark.parametrize("M,n,align", [(8, 100_003, 128), (4, 2048 * 5 + 3, 1), (64, 20_000, 8), (13, 4099, 1)])
+@pytest.mark.parametrize("where", ["grads", "grads_params", "state", "everything"])
+def test_host_buffers_match_hbm(cuda_device, M, n, align, where):
+    dev = cuda_device
+    plan = z.zero1_plan(n, M, align)
+    P = plan.padded_n
+    a_state = make_state(n, P, 800 + M, dev, nonzero_moments=True)
+    b_state = [t.clone() for t in a_state]
+    o_state = [f32(t) for t in a_state]
+    if where in ("state", "everything"):
+        b_state = [pinned(t) for t in b_state]
+    pa = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+    pb = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+    if where in ("grads_params", "everything"):
+        pb = pinned(pb)
+    fa = torch.zeros(1, dtype=torch.int32, device=dev)
+    fb = torch.zeros(1, dtype=torch.int32, device=dev)
+    for t in (1, 2):
+        hp = z.AdamW(global_batch=max(M, 64), step=t)
+        grads = make_grads(M, n, 1e-2, 810 + M, t, dev)
+        gb = [pinned(g) for g in grads] if where != "state" else grads
+        z.zero1_reduce_scatter_adamw_allgather(plan, 0, M, grads, *a_state, pa, hp, fa)
+        z.zero1_reduce_scatter_adamw_allgather(plan, 0, M, gb, *b_state, pb, hp, fb)
+        torch.cuda.synchronize()
+        want_p = oracle_step(plan, [u16(g) for g in grads], *o_state, oracle_hp(hp))
+        for x, y, o, what in zip(a_state, b_state, o_state, ("master", "m", "v")):
+            assert_f32_bits(f32(y), f32(x), f"{where}: {what} t={t}")
+            assert_f32_bits(f32(x), o, f"{what} t={t} vs oracle")
+        assert_bf16_bits(u16(pb), u16(pa), f"{where}: params t={t}")
+        assert_bf16_bits(u16(pa), want_p, f"params t={t} vs oracle")
+    assert int(fa.item()) == int(fb.item()) == 0
+
+
+def test_overflow_check_reads_host_gradients(cuda_device):
+    dev = cuda_device
+    M, n = 8, 50_000
+    plan = z.zero1_plan(n, M, 8)
+    grads = [pinned(g) for g in make_grads(M, n, 1e-3, 820, 1, dev)]
+    flag = torch.zeros(1, dtype=torch.int32, device=dev)
+    z.zero1_overflow_check(plan, 0, M, grads, flag)
+    torch.cuda.synchronize()
+    assert int(flag.item()) == 0
+    grads[3][40_000] = float("inf")
+    z.zero1_overflow_check(plan, 0, M, grads, flag)
+    torch.cuda.synchronize()
+    assert int(flag.item()) == 1
+
+
+def test_pageable_host_tensor_is_rejected(cuda_device):
+    plan = z.zero1_plan(100, 1, 1)
+    master, m, v = make_state(100, plan.padded_n, 1, cuda_device)
+    params = torch.zeros(100, dtype=torch.bfloat16, device=cuda_device)
+    grads = [torch.zeros(100, dtype=torch.bfloat16)]       # pageable: not accepted
+    with pytest.raises(ValueError):
+        z.zero1_reduce_scatter_adamw_allgather(plan, 0, 1, grads, master, m, v, params, z.AdamW())

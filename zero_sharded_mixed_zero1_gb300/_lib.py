@@ -129,10 +129,13 @@ def _stream(stream) -> int:
 
 
 def _dev(t: torch.Tensor, dtype: torch.dtype, min_numel: int, what: str) -> int:
+    """Pointer of a tensor the GPU can address: a CUDA tensor, or a pinned
+    host tensor (mapped at the same address; the kernels reach it over the
+    host link)."""
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{what}: expected a torch.Tensor")
-    if t.device.type != "cuda":
-        raise ValueError(f"{what}: must be a CUDA tensor")
+    if t.device.type != "cuda" and not (t.device.type == "cpu" and t.is_pinned()):
+        raise ValueError(f"{what}: must be a CUDA tensor or a pinned host tensor")
     if t.dtype != dtype:
         raise TypeError(f"{what}: expected {dtype}, got {t.dtype}")
     if not t.is_contiguous():

@@ -55,8 +55,10 @@
  *    w' = w*(1-lr*wd) - lr*u
  *    param = bf16_round_nearest_even(w')
  *  The constants inv, 1-beta1, 1-beta2, 1-beta^t and 1-lr*wd are evaluated
- *  on the host in double (beta^t by the C library's pow) and rounded once to
- *  float.  Padding elements (global index >= n) take g = +0.
+ *  in double and rounded once to float; beta^t is square-and-multiply over
+ *  the bits of t (least significant first), so the host and the device
+ *  produce the same constants.  Padding elements (global index >= n) take
+ *  g = +0.
  */
 #ifndef ZERO1_H
 #define ZERO1_H

@@ -65,6 +65,8 @@ def _L():
         lib.orc_segments.restype = ctypes.c_int
         lib.orc_memory.argtypes = [i64, i64, vp, vp]
         lib.orc_adamw_constants.argtypes = [f32, f32, f32, f32, i64, f32, i64, vp]
+        lib.orc_pow_int.argtypes = [ctypes.c_double, i64]
+        lib.orc_pow_int.restype = ctypes.c_double
         lib.orc_reduce_scatter.argtypes = [i32, vp, i64, i64, f32, vp, vp]
         lib.orc_adamw.argtypes = [i64, vp, vp, vp, vp, f32, f32, f32, f32, vp]
         lib.orc_all_gather.argtypes = [i64, vp, vp]
@@ -149,6 +151,11 @@ def memory(n: int, shard: int) -> tuple[int, int]:
     b = ctypes.c_int64()
     _L().orc_memory(n, shard, ctypes.byref(a), ctypes.byref(b))
     return a.value, b.value
+
+
+def pow_int(b: float, t: int) -> float:
+    """b^t in double by square-and-multiply (the bias-correction power)."""
+    return _L().orc_pow_int(b, t)
 
 
 def adamw_constants(hp: AdamW) -> dict:

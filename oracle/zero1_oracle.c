@@ -38,7 +38,9 @@
  *  - The replica sum is a left fold in rank order 0..M-1 starting from rank 0's
  *    value, in fp32; unscaling by 1/(B*S) follows the sum.
  *  - Host constants are evaluated in double and rounded once to float; the
- *    powers beta^t come from the C library's pow().
+ *    power beta^t is evaluated in double by square-and-multiply over the bits
+ *    of t, least significant first (orc_pow_int), so that any IEEE-754
+ *    implementation - the GPU included - reproduces it exactly.
  *  - Padding elements (global index >= n) have gradient +0 and are updated
  *    like any other element.
  *  - The overflow flag is the OR over real elements of !isfinite(sum).
@@ -152,14 +154,27 @@ void orc_memory(int64_t n, int64_t shard, int64_t *naive_bytes, int64_t *zero1_b
 /*      [4] 1-beta2^t      [5] 1-lr*wd                                        */
 /* ------------------------------------------------------------------------ */
 
+/* b^t for t >= 0 in double: square-and-multiply over the bits of t, least
+ * significant bit first; one rounding per multiplication. */
+double orc_pow_int(double b, int64_t t)
+{
+    double r = 1.0, x = b;
+    while (t > 0) {
+        if (t & 1) r = r * x;
+        x = x * x;
+        t >>= 1;
+    }
+    return r;
+}
+
 void orc_adamw_constants(float lr, float beta1, float beta2, float weight_decay,
                          int64_t B, float S, int64_t t, float *out)
 {
     out[0] = (float)(1.0 / ((double)B * (double)S));
     out[1] = (float)(1.0 - (double)beta1);
     out[2] = (float)(1.0 - (double)beta2);
-    out[3] = (float)(1.0 - pow((double)beta1, (double)t));
-    out[4] = (float)(1.0 - pow((double)beta2, (double)t));
+    out[3] = (float)(1.0 - orc_pow_int((double)beta1, t));
+    out[4] = (float)(1.0 - orc_pow_int((double)beta2, t));
     out[5] = (float)(1.0 - (double)lr * (double)weight_decay);
 }
 

@@ -14,7 +14,8 @@ SRC = os.path.join(ROOT, "oracle", "zero1_oracle.c")
 
 MUTANTS = {
     "drop_bias_correction_1": ("float mh = m1 / bc1;", "float mh = m1;"),
-    "bias_correction_off_by_one": ("pow((double)beta1, (double)t)", "pow((double)beta1, (double)(t + 1))"),
+    "bias_correction_off_by_one": ("orc_pow_int((double)beta1, t)", "orc_pow_int((double)beta1, t + 1)"),
+    "power_skips_a_bit": ("        if (t & 1) r = r * x;", "        if ((t & 1) && t > 1) r = r * x;"),
     "betas_swapped_in_m": ("float m1 = beta1 * m[j] + omb1 * gj;", "float m1 = beta2 * m[j] + omb2 * gj;"),
     "eps_inside_sqrt": ("float u = mh / (sqrtf(vh) + eps);", "float u = mh / sqrtf(vh + eps);"),
     "decay_without_lr": ("out[5] = (float)(1.0 - (double)lr * (double)weight_decay);",

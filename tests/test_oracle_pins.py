@@ -476,6 +476,23 @@ def test_overflow_ignores_padding_and_skip_writes_nothing():
     assert flag[0] == 0 and not np.array_equal(master, snap[0])
 
 
+def test_bias_correction_power():
+    """beta^t: exact for powers of two, t = 0 and t = 1; otherwise within the
+    square-and-multiply error bound of the exact rational power: each squaring
+    doubles the relative error, so it is at most about (t + 2 log2 t) units
+    of 2^-53."""
+    for t in [0, 1, 2, 3, 7, 64, 1000, 1023, 10**6]:
+        assert oracle.pow_int(0.5, t) == math.ldexp(1.0, -t)
+    assert oracle.pow_int(0.9, 0) == 1.0 and oracle.pow_int(0.9, 1) == 0.9
+    for b in [float(f32(0.9)), float(f32(0.95)), float(f32(0.999))]:
+        for t in [2, 3, 5, 10, 17, 100, 999, 1000, 4097]:
+            exact = Fraction(b) ** t
+            got = Fraction(oracle.pow_int(b, t))
+            rounds = t + 2 * t.bit_length() + 1
+            assert abs(got - exact) <= exact * Fraction(rounds, 2 ** 53)
+            assert abs(got - exact) > 0 or t < 3      # not trivially exact
+
+
 def test_deepspeed_hyperparameters_from_the_pages():
     """The pages' AdamW block (lr 1e-3, betas 0.9/0.999, eps 1e-8, wd 0.01)
     runs through the constants: 1-beta^t in fp32 and the decay factor."""

@@ -135,6 +135,17 @@ extern "C" int zero1_plan_memory(const zero1_plan_t *plan, int64_t *naive_bytes,
     return ZERO1_OK;
 }
 
+double z1_pow_int(double b, int64_t t)
+{
+    // square-and-multiply over the bits of t, least significant first
+    double r = 1.0, x = b;
+    for (; t > 0; t >>= 1) {
+        if (t & 1) r *= x;
+        x *= x;
+    }
+    return r;
+}
+
 int z1_adamw_constants(const zero1_adamw_t *hp, int32_t M, Z1Consts *c)
 {
     if (!hp) return z1_fail(ZERO1_EINVAL, "hyperparameters are NULL");
@@ -148,14 +159,14 @@ int z1_adamw_constants(const zero1_adamw_t *hp, int32_t M, Z1Consts *c)
     if (hp->global_batch < M)
         return z1_fail(ZERO1_EINVAL, "global batch B = %lld is smaller than M = %d", (long long)hp->global_batch, M);
     if (hp->step < 1) return z1_fail(ZERO1_EINVAL, "step t = %lld < 1", (long long)hp->step);
-    const double b1 = hp->beta1, b2 = hp->beta2, t = (double)hp->step;
+    const double b1 = hp->beta1, b2 = hp->beta2;
     c->inv = (float)(1.0 / ((double)hp->global_batch * (double)hp->loss_scale));
     c->beta1 = hp->beta1;
     c->omb1 = (float)(1.0 - b1);
     c->beta2 = hp->beta2;
     c->omb2 = (float)(1.0 - b2);
-    c->bc1 = (float)(1.0 - std::pow(b1, t));
-    c->bc2 = (float)(1.0 - std::pow(b2, t));
+    c->bc1 = (float)(1.0 - z1_pow_int(b1, hp->step));
+    c->bc2 = (float)(1.0 - z1_pow_int(b2, hp->step));
     c->eps = hp->eps;
     c->lr = hp->lr;
     c->cdec = (float)(1.0 - (double)hp->lr * (double)hp->weight_decay);

@@ -34,6 +34,11 @@ int z1_check_plan(const zero1_plan_t *plan);
 // Validate [shard_begin, shard_end) against the plan and fill the range.
 int z1_range(const zero1_plan_t *plan, int32_t shard_begin, int32_t shard_end, Z1Range *out);
 
+// b^t in double by square-and-multiply over the bits of t (least significant
+// first), one rounding per multiplication: reproducible on any IEEE-754
+// implementation, the device included.
+double z1_pow_int(double b, int64_t t);
+
 // Validate hyperparameters and evaluate the constants: double precision,
-// rounded once to float, beta^t from the C library's pow.
+// rounded once to float, beta^t from z1_pow_int.
 int z1_adamw_constants(const zero1_adamw_t *hp, int32_t M, Z1Consts *out);

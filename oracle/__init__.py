@@ -74,6 +74,11 @@ def _L():
                                        f32, f32, f32, f32, f32, f32, i64, i64, vp, i32]
         lib.orc_zero1_step.restype = ctypes.c_int
         lib.orc_allreduce.argtypes = [i32, vp, i64, f32, i32, vp]
+        lib.orc_scaler_init.argtypes = [vp, f32, i32, i64]
+        lib.orc_scaler_update.argtypes = [vp, ctypes.c_uint32, f32, i32, i32, f32]
+        lib.orc_zero1_dynamic_attempt.argtypes = [i32, vp, i64, i64, vp, vp, vp, vp, f32, f32, f32, f32, f32,
+                                                  i64, vp, f32, i32, i32, f32, vp]
+        lib.orc_zero1_dynamic_attempt.restype = ctypes.c_int
         lib.orc_overflow_check.argtypes = [i32, vp, i64, vp]
         _lib = lib
     return _lib
@@ -239,3 +244,52 @@ def overflow_check(grads, n_valid: int) -> int:
     flag = np.zeros(1, np.uint32)
     _L().orc_overflow_check(len(grads), _ptr_array(grads), n_valid, _ptr(flag))
     return int(flag[0])
+
+
+# -- dynamic loss scaling ("五维并行实战" 4.2, fp16 block) ---------------------
+
+@dataclass(frozen=True)
+class LossScalePolicy:
+    """The fp16 block's keys: the initial scale (2^initial_scale_power), the
+    growth/back-off factor, loss_scale_window, hysteresis, min_loss_scale."""
+    initial_scale: float = 2.0 ** 12
+    factor: float = 2.0
+    window: int = 1000
+    hysteresis: int = 2
+    min_scale: float = 1.0
+
+
+class Scaler(ctypes.Structure):
+    _fields_ = [("scale", ctypes.c_float), ("good", ctypes.c_int32), ("hyst_left", ctypes.c_int32),
+                ("step", ctypes.c_int64), ("attempts", ctypes.c_int64), ("skipped", ctypes.c_int64)]
+
+    @classmethod
+    def start(cls, policy: LossScalePolicy, first_step: int = 1) -> "Scaler":
+        sc = cls()
+        _L().orc_scaler_init(ctypes.byref(sc), policy.initial_scale, policy.hysteresis, first_step)
+        return sc
+
+    def update(self, overflow: int, policy: LossScalePolicy) -> None:
+        _L().orc_scaler_update(ctypes.byref(self), int(overflow), policy.factor, policy.window,
+                               policy.hysteresis, policy.min_scale)
+
+
+def zero1_dynamic_attempt(grads, n_valid: int, master, m, v, params, hp: AdamW, scaler: Scaler,
+                          policy: LossScalePolicy) -> int:
+    """One attempt of the dynamically scaled step over a whole range (hp's
+    loss_scale and step are ignored: the scaler's are used).  Returns the
+    attempt's overflow flag."""
+    for g in grads:
+        _check(g, np.uint16)
+    for a in (master, m, v):
+        _check(a, np.float32)
+    _check(params, np.uint16)
+    f = ctypes.c_uint32()
+    rc = _L().orc_zero1_dynamic_attempt(len(grads), _ptr_array(grads), master.size, n_valid, _ptr(master),
+                                        _ptr(m), _ptr(v), _ptr(params), hp.lr, hp.beta1, hp.beta2, hp.eps,
+                                        hp.weight_decay, hp.global_batch, ctypes.byref(scaler),
+                                        policy.factor, policy.window, policy.hysteresis, policy.min_scale,
+                                        ctypes.byref(f))
+    if rc != 0:
+        raise MemoryError("oracle step could not allocate its gradient buffer")
+    return int(f.value)

@@ -30,6 +30,10 @@ MUTANTS = {
     "gather_not_from_master": ("params[j] = orc_f32_to_bf16(master[j]);",
                                "params[j] = orc_f32_to_bf16(master[j] * 1.0000001f);"),
     "sqrt_of_m": ("float u = mh / (sqrtf(vh) + eps);", "float u = vh / (sqrtf(mh) + eps);"),
+    "scaler_ignores_hysteresis": ("        sc->hyst_left -= 1;", "        sc->hyst_left -= 2;"),
+    "scaler_window_off_by_one": ("        if (sc->good >= window) {", "        if (sc->good > window) {"),
+    "skip_advances_t": ("        sc->skipped += 1;", "        sc->skipped += 1;\n        sc->step += 1;"),
+    "scaler_no_floor": ("            sc->scale = down < min_scale ? min_scale : down;", "            sc->scale = down;"),
 }
 
 
@@ -44,6 +48,7 @@ def test_pins_catch_mutant(name, tmp_path):
     subprocess.run([os.environ.get("CC", "gcc"), *oracle.CFLAGS, "-o", str(so), str(c), "-lm"], check=True)
     env = dict(os.environ, ZERO1_ORACLE_LIB=str(so))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_loss_scale.py")],
                        env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} survived the pins"

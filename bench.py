@@ -230,12 +230,14 @@ def run_reference(args, w) -> None:
 
 # --------------------------------------------------------- our arm ---------
 
-def config_of(w, state_on_host: bool = False) -> dict:
+def config_of(w, state_on_host: bool = False, dynamic: bool = False) -> dict:
     c = {"workload": w.name, "n": w.n, "M": w.M, "align": w.align, "global_batch": w.B,
          "loss_scale": w.S, "shards": list(w.shards), "io": "bf16 grads and params, fp32 master/m/v",
          "l2": "inputs larger than L2 (no flush)", "parallelism": "replicas only"}
     if state_on_host:
         c["state"] = "fp32 master/m/v in pinned host memory (offload)"
+    if dynamic:
+        c["loss_scaling"] = "dynamic, device-resident (window 1000, hysteresis 2, factor 2)"
     return c
 
 
@@ -287,9 +289,24 @@ def run_ours(args, w) -> None:
         return z.AdamW(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay,
                        loss_scale=w.S, global_batch=w.B, step=t)
 
+    if args.dynamic_loss_scale:
+        policy = z.LossScalePolicy(initial_scale=w.S if w.S > 1 else 2.0 ** 12, factor=2.0, window=1000,
+                                   hysteresis=2, min_scale=1.0)
+        scaler = z.new_scaler(dev)
+        z.zero1_scaler_init(scaler, policy, hp(1))
+        sums = torch.empty(L, dtype=torch.float32, device=dev)
+
+        def launch(gr, tt, st=None):
+            z.zero1_step_dynamic(plan, sb, se, gr, master, m, v, params, hp(tt), scaler, policy, sums, stream=st)
+        launches_per_step = 3
+    else:
+        def launch(gr, tt, st=None):
+            z.zero1_reduce_scatter_adamw_allgather(plan, sb, se, gr, master, m, v, params, hp(tt), flag, stream=st)
+        launches_per_step = 1
+
     t = 1
     for _ in range(args.warmup):
-        z.zero1_reduce_scatter_adamw_allgather(plan, sb, se, gsets[t % 2], master, m, v, params, hp(t), flag)
+        launch(gsets[t % 2], t)
         t += 1
     torch.cuda.synchronize(dev)
 
@@ -302,8 +319,7 @@ def run_ours(args, w) -> None:
     start.record(stream)
     for i in range(args.steps):
         evs[2 * i].record(stream)
-        z.zero1_reduce_scatter_adamw_allgather(plan, sb, se, gsets[t % 2], master, m, v, params, hp(t), flag,
-                                               stream=stream)
+        launch(gsets[t % 2], t, stream)
         evs[2 * i + 1].record(stream)
         t += 1
     end.record(stream)
@@ -324,7 +340,7 @@ def run_ours(args, w) -> None:
     # (no staging copy) and writes the bf16 parameters to a pinned host
     # buffer; the flag is read back; the step ends with a stream synchronize.
     e2e = e2e_copy = None
-    if not args.no_e2e:
+    if not args.no_e2e and not args.dynamic_loss_scale:
         e2e_steps = max(3, min(args.steps, args.e2e_steps))
         host_g = [synth.normal_bf16(nv, w.grad_std * w.S, synth.seed_of(w.seed, 7, r, rank)).pin_memory()
                   for r in range(w.M)]
@@ -371,6 +387,8 @@ def run_ours(args, w) -> None:
         return
     peaks = measured_peaks()
     bytes_launch = algorithmic_bytes(nv, L - nv, w.M)
+    if args.dynamic_loss_scale:      # fp32 sums written and read back: +8 B per element
+        bytes_launch += 8 * L
     achieved = bytes_launch / (kernel_ms * 1e-3) / 1e9
     line = {
         "metric": METRIC,
@@ -385,16 +403,19 @@ def run_ours(args, w) -> None:
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
-        "config": config_of(w, args.state_on_host),
+        "config": config_of(w, args.state_on_host, args.dynamic_loss_scale),
         "hbm_gbs": bytes_launch * args.steps / (ms_total * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "peak_source": peaks["source"],
-                     "traffic": recorded_traffic(w.name), "kernel": f"k_fused_step<M={w.M}>",
+                     "traffic": None if args.dynamic_loss_scale else recorded_traffic(w.name),
+                     "kernel": ("dynamic step: k_reduce_scatter + k_apply_sums + k_scaler_update"
+                                if args.dynamic_loss_scale else
+                                (f"k_fused_step<M={w.M}>" if w.M <= 8 else "k_fused_step_grouped")),
                      "bytes_per_launch": bytes_launch, "kernel_ms": kernel_ms},
         "cpu_baseline": cpu_baseline,
         "e2e": e2e,
         "e2e_copy_then_step": e2e_copy,
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks,
         "overflow_flag": overflow,
     }
@@ -412,6 +433,9 @@ def main(argv=None) -> int:
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--dynamic-loss-scale", action="store_true",
+                    help="time the dynamically scaled step (reduce-scatter to fp32 sums, update, scaler) "
+                         "with the fp16 block's policy instead of the fused step")
     ap.add_argument("--state-on-host", action="store_true",
                     help="keep fp32 master/m/v in pinned host memory (optimizer-state offload)")
     args = ap.parse_args(argv)

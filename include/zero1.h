@@ -208,6 +208,74 @@ int zero1_all_gather(const zero1_plan_t *plan, int32_t shard_begin, int32_t shar
 int zero1_all_gather_shards(const zero1_plan_t *plan, const void *shards, void *const *outs,
                             zero1_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * Dynamic loss scaling with the skip decided on the device [OPT]
+ *
+ * The fp16 block of [OPT] names the policy's keys: loss_scale 0 (dynamic),
+ * initial_scale_power, loss_scale_window, hysteresis, min_loss_scale.  The
+ * rule taken from them: an attempt whose summed gradients overflow writes
+ * nothing and leaves t unchanged; it uses up one unit of hysteresis, and when
+ * none is left S is divided by `factor` (not below min_scale) and the
+ * hysteresis is refilled; the clean-attempt count restarts.  A clean attempt
+ * applies the step and advances t; after `window` clean attempts in a row S
+ * is multiplied by `factor` (unless that overflows fp32), the count restarts
+ * and the hysteresis is refilled.
+ *
+ * S, t and the counters live in device memory (zero1_scaler_t), so a training
+ * loop never has to read the flag on the host: the caller scales its loss by
+ * the device-resident `scale` and calls zero1_step_dynamic each iteration.
+ * ------------------------------------------------------------------------- */
+
+typedef struct zero1_loss_scale_policy {
+    float initial_scale; /* S at the first attempt (2^initial_scale_power), finite, > 0 */
+    float factor;        /* growth and back-off factor, finite, > 1 */
+    int32_t window;      /* loss_scale_window, >= 1 */
+    int32_t hysteresis;  /* overflowing attempts tolerated before S shrinks, >= 1 */
+    float min_scale;     /* min_loss_scale, finite, > 0 */
+} zero1_loss_scale_policy_t;
+
+/* Device-resident scaler state (56 bytes, 8-byte aligned, in device memory). */
+typedef struct zero1_scaler {
+    float scale;             /* S of the next attempt */
+    float inv;               /* 1/(B*S) of the next attempt */
+    float bc1, bc2;          /* 1 - beta1^t, 1 - beta2^t of the next attempt */
+    int64_t step;            /* t of the next applied step */
+    int64_t attempts;        /* attempts so far */
+    int64_t skipped;         /* attempts skipped because their gradients overflowed */
+    int32_t good_steps;      /* clean attempts in a row since S last changed */
+    int32_t hysteresis_left; /* overflowing attempts still tolerated */
+    uint32_t overflow;       /* flag of the attempt in progress; 0 between attempts */
+    uint32_t reserved;
+} zero1_scaler_t;
+
+/* Start a scaler (one tiny kernel on `stream`): S = policy->initial_scale,
+ * t = hp->step, the derived constants for hp->global_batch and hp->beta1/2.
+ * scaler: device pointer to a zero1_scaler_t.  hp->loss_scale is not used. */
+int zero1_scaler_init(zero1_scaler_t *scaler, const zero1_loss_scale_policy_t *policy,
+                      const zero1_adamw_t *hp, zero1_stream_t stream);
+
+/* One attempt of the dynamically scaled ZeRO-1 step over shards
+ * [shard_begin, shard_end) [Z1], [OPT], three kernels on `stream`:
+ *  1. reduce-scatter: sums[j] = rank-order fp32 sum of the M replicas for
+ *     the nv real elements (+0 on padding), ORing the overflow flag into
+ *     scaler->overflow;
+ *  2. if scaler->overflow is clear: the AdamW update with g = sums * (1/(B*S))
+ *     and the bias corrections of the scaler's t, then the bf16 parameters -
+ *     bit for bit the fused step with S and t taken from the scaler; if it is
+ *     set: nothing is written;
+ *  3. the scaler advances by the rule above and its flag is cleared.
+ * The gradients are read once: 2M + 4 + 4 + 24 + 2 bytes per parameter.
+ * Arguments as for zero1_reduce_scatter_adamw_allgather, plus:
+ *  hp:      lr, betas, eps, weight decay and global batch (its loss_scale and
+ *           step are ignored: the scaler's are used);
+ *  scaler:  device pointer, started with zero1_scaler_init;
+ *  sums:    device fp32 workspace of at least L elements (scratch; its
+ *           contents on return are the last attempt's sums). */
+int zero1_step_dynamic(const zero1_plan_t *plan, int32_t shard_begin, int32_t shard_end,
+                       const void *const *grads, float *master, float *m, float *v, void *params,
+                       const zero1_adamw_t *hp, zero1_scaler_t *scaler,
+                       const zero1_loss_scale_policy_t *policy, float *sums, zero1_stream_t stream);
+
 /* Text of a status code. */
 const char *zero1_strerror(int code);
 

@@ -10,12 +10,16 @@ from ._lib import (  # noqa: F401
     ZERO1_DTYPE_BF16,
     ZERO1_DTYPE_F32,
     ZERO1_MAX_REPLICAS,
+    SCALER_BYTES,
     AdamW,
+    LossScalePolicy,
     Plan,
     Zero1Error,
     dp_allreduce,
     library_path,
     load,
+    new_scaler,
+    scaler_state,
     zero1_adamw_update,
     zero1_all_gather,
     zero1_all_gather_shards,
@@ -25,4 +29,6 @@ from ._lib import (  # noqa: F401
     zero1_plan_segments,
     zero1_reduce_scatter,
     zero1_reduce_scatter_adamw_allgather,
+    zero1_scaler_init,
+    zero1_step_dynamic,
 )

@@ -11,6 +11,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import struct
 from dataclasses import dataclass
 
 import torch
@@ -72,6 +73,42 @@ class AdamW:
                             self.loss_scale, self.global_batch, self.step)
 
 
+class _PolicyStruct(ctypes.Structure):
+    _fields_ = [("initial_scale", ctypes.c_float), ("factor", ctypes.c_float), ("window", ctypes.c_int32),
+                ("hysteresis", ctypes.c_int32), ("min_scale", ctypes.c_float)]
+
+
+@dataclass(frozen=True)
+class LossScalePolicy:
+    """zero1_loss_scale_policy_t: initial scale (2^initial_scale_power),
+    growth/back-off factor, loss_scale_window, hysteresis, min_loss_scale."""
+    initial_scale: float = 2.0 ** 12
+    factor: float = 2.0
+    window: int = 1000
+    hysteresis: int = 2
+    min_scale: float = 1.0
+
+    def c_struct(self) -> _PolicyStruct:
+        return _PolicyStruct(self.initial_scale, self.factor, self.window, self.hysteresis, self.min_scale)
+
+
+SCALER_BYTES = 56
+_SCALER_FMT = "<ffffqqqiiII"
+
+
+def new_scaler(device) -> torch.Tensor:
+    """Device storage for one zero1_scaler_t (56 bytes)."""
+    return torch.zeros(SCALER_BYTES, dtype=torch.uint8, device=device)
+
+
+def scaler_state(scaler: torch.Tensor) -> dict:
+    """Read a zero1_scaler_t back to the host (synchronises with its stream)."""
+    raw = bytes(scaler.cpu().numpy().tobytes())
+    k = ["scale", "inv", "bc1", "bc2", "step", "attempts", "skipped", "good_steps", "hysteresis_left",
+         "overflow", "reserved"]
+    return dict(zip(k, struct.unpack(_SCALER_FMT, raw)))
+
+
 def library_path() -> str:
     return _build.LIB
 
@@ -99,6 +136,8 @@ def load() -> ctypes.CDLL:
         "zero1_adamw_update": [P, i32, i32, vp, vp, vp, vp, A, vp],
         "zero1_all_gather": [P, i32, i32, vp, vp, vp],
         "zero1_all_gather_shards": [P, vp, vp, vp],
+        "zero1_scaler_init": [vp, ctypes.POINTER(_PolicyStruct), A, vp],
+        "zero1_step_dynamic": [P, i32, i32, vp, vp, vp, vp, vp, A, vp, ctypes.POINTER(_PolicyStruct), vp, vp],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -258,3 +297,31 @@ def zero1_all_gather_shards(plan: Plan, shards, outs, stream=None) -> None:
     _replicas(plan, outs, "outs")
     _check_rc(load().zero1_all_gather_shards(ctypes.byref(plan), _dev(shards, torch.bfloat16, plan.n, "shards"),
                                              _ptrs(outs, torch.bfloat16, plan.n, "outs"), _stream(stream)))
+
+
+# -- dynamic loss scaling -------------------------------------------------------
+
+def _scaler_ptr(scaler: torch.Tensor) -> int:
+    if scaler.dtype != torch.uint8 or scaler.numel() < SCALER_BYTES or scaler.device.type != "cuda":
+        raise ValueError("scaler must be a CUDA uint8 tensor of at least 56 bytes (new_scaler)")
+    return scaler.data_ptr()
+
+
+def zero1_scaler_init(scaler: torch.Tensor, policy: LossScalePolicy, hp: AdamW, stream=None) -> None:
+    """Start a device-resident scaler: S = policy.initial_scale, t = hp.step."""
+    _check_rc(load().zero1_scaler_init(_scaler_ptr(scaler), ctypes.byref(policy.c_struct()),
+                                       ctypes.byref(hp.c_struct()), _stream(stream)))
+
+
+def zero1_step_dynamic(plan: Plan, shard_begin: int, shard_end: int, grads, master, m, v, params, hp: AdamW,
+                       scaler: torch.Tensor, policy: LossScalePolicy, sums, stream=None) -> None:
+    """One dynamically scaled attempt (S and t from the device scaler);
+    sums: fp32 workspace of at least L elements."""
+    _replicas(plan, grads, "grads")
+    _, L, nv = plan.shard_range(shard_begin, shard_end) if 0 <= shard_begin < shard_end <= plan.M \
+        else (0, 0, 0)
+    _check_rc(load().zero1_step_dynamic(
+        ctypes.byref(plan), shard_begin, shard_end, _ptrs(grads, torch.bfloat16, nv, "grads"),
+        _dev(master, torch.float32, L, "master"), _dev(m, torch.float32, L, "m"), _dev(v, torch.float32, L, "v"),
+        _dev(params, torch.bfloat16, nv, "params"), ctypes.byref(hp.c_struct()), _scaler_ptr(scaler),
+        ctypes.byref(policy.c_struct()), _dev(sums, torch.float32, L, "sums"), _stream(stream)))

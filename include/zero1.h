@@ -276,6 +276,37 @@ int zero1_step_dynamic(const zero1_plan_t *plan, int32_t shard_begin, int32_t sh
                        const zero1_adamw_t *hp, zero1_scaler_t *scaler,
                        const zero1_loss_scale_policy_t *policy, float *sums, zero1_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * The dynamically scaled step without any device allocation by the caller.
+ *
+ * The pages have no counterpart to this call; it exists for callers that
+ * cannot call cudaMalloc: programs whose own pool allocator takes the device
+ * memory at start-up (a library cudaMalloc then fails or splits that pool),
+ * and code that must not allocate or free because cudaMalloc/cudaFree can
+ * synchronise the device and stall work on other streams.
+ *
+ * It is zero1_step_dynamic with the fp32 sums workspace replaced by an array
+ * inside the library: ZERO1_NOALLOC_MAX_ELEMS floats (64 MiB) that every GPU
+ * loading libzero1.so holds until the process exits.  The caller still
+ * passes gradients, state, parameters, scaler and policy.
+ *  - The range must satisfy L = (shard_end - shard_begin) * s <=
+ *    ZERO1_NOALLOC_MAX_ELEMS; larger ranges return ZERO1_ERANGE before
+ *    anything is launched (call it once per group of shards instead).
+ *  - The first call on a device looks up the array's device address on that
+ *    device (cudaGetSymbolAddress, with that device current); make that first
+ *    call before any stream capture.  No cudaMalloc, cudaFree or other
+ *    allocating routine is called.
+ *  - All calls share the one array and it keeps the last call's sums; nothing
+ *    in it needs to start at zero (each call writes all L sums before reading
+ *    them).  Calls that overlap on the GPU (other streams, other threads) race
+ *    on it: serialise them.
+ * Results are bit for bit those of zero1_step_dynamic. */
+#define ZERO1_NOALLOC_MAX_ELEMS (16 * 1024 * 1024)
+int zero1_step_dynamic_noalloc(const zero1_plan_t *plan, int32_t shard_begin, int32_t shard_end,
+                               const void *const *grads, float *master, float *m, float *v, void *params,
+                               const zero1_adamw_t *hp, zero1_scaler_t *scaler,
+                               const zero1_loss_scale_policy_t *policy, zero1_stream_t stream);
+
 /* Text of a status code. */
 const char *zero1_strerror(int code);
 

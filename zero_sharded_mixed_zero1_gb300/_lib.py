@@ -325,3 +325,30 @@ def zero1_step_dynamic(plan: Plan, shard_begin: int, shard_end: int, grads, mast
         _dev(master, torch.float32, L, "master"), _dev(m, torch.float32, L, "m"), _dev(v, torch.float32, L, "v"),
         _dev(params, torch.bfloat16, nv, "params"), ctypes.byref(hp.c_struct()), _scaler_ptr(scaler),
         ctypes.byref(policy.c_struct()), _dev(sums, torch.float32, L, "sums"), _stream(stream)))
+
+
+# -- the dynamically scaled step with the library's own workspace --------------
+
+ZERO1_NOALLOC_MAX_ELEMS = 16 * 1024 * 1024
+
+
+def zero1_step_dynamic_noalloc(plan: Plan, shard_begin: int, shard_end: int, grads, master, m, v, params,
+                               hp: AdamW, scaler: torch.Tensor, policy: LossScalePolicy, stream=None) -> None:
+    """zero1_step_dynamic without a caller-provided workspace (the library's
+    built-in 64 MiB array; ranges of at most ZERO1_NOALLOC_MAX_ELEMS
+    elements).  For callers that cannot allocate device memory."""
+    lib = load()
+    fn = lib.zero1_step_dynamic_noalloc
+    if fn.argtypes is None:
+        vp, i32 = ctypes.c_void_p, ctypes.c_int32
+        fn.argtypes = [ctypes.POINTER(Plan), i32, i32, vp, vp, vp, vp, vp, ctypes.POINTER(_AdamWStruct), vp,
+                       ctypes.POINTER(_PolicyStruct), vp]
+        fn.restype = ctypes.c_int
+    _replicas(plan, grads, "grads")
+    _, L, nv = plan.shard_range(shard_begin, shard_end) if 0 <= shard_begin < shard_end <= plan.M \
+        else (0, 0, 0)
+    _check_rc(fn(ctypes.byref(plan), shard_begin, shard_end, _ptrs(grads, torch.bfloat16, nv, "grads"),
+                 _dev(master, torch.float32, L, "master"), _dev(m, torch.float32, L, "m"),
+                 _dev(v, torch.float32, L, "v"), _dev(params, torch.bfloat16, nv, "params"),
+                 ctypes.byref(hp.c_struct()), _scaler_ptr(scaler), ctypes.byref(policy.c_struct()),
+                 _stream(stream)))

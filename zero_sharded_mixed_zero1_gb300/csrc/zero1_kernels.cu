@@ -1065,3 +1065,59 @@ extern "C" int zero1_step_dynamic(const zero1_plan_t *plan, int32_t shard_begin,
     k_scaler_update<<<1, 32, 0, st>>>(scaler, pol, hp->global_batch, hp->beta1, hp->beta2);
     return launch_status("dynamic step launch");
 }
+
+// ------------------------------------------- step without caller allocation --
+//
+// For callers that cannot call cudaMalloc (their pool allocator owns the
+// device memory, or allocation would synchronise the device): the sums
+// workspace of zero1_step_dynamic is this file-scope array, which exists on
+// every device that loads the library until the process exits.  Its name is a
+// host-side stand-in in host code; the device address comes from
+// cudaGetSymbolAddress, looked up once per device with that device current.
+static __device__ __align__(256) float g_noalloc_sums[ZERO1_NOALLOC_MAX_ELEMS];
+
+namespace {
+
+std::atomic<float *> g_noalloc_addr[64];
+
+// Device address of g_noalloc_sums on the current device (looked up on the
+// first call on each device).
+int noalloc_sums(float **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return z1_fail(ZERO1_ECUDA, "no-alloc step: cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= 64) return z1_fail(ZERO1_ERANGE, "no-alloc step: device %d beyond 64 devices", dev);
+    float *p = g_noalloc_addr[dev].load(std::memory_order_acquire);
+    if (!p) {
+        void *addr = nullptr;
+        e = cudaGetSymbolAddress(&addr, g_noalloc_sums);
+        if (e != cudaSuccess || !addr)
+            return z1_fail(ZERO1_ECUDA, "no-alloc step: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+        p = static_cast<float *>(addr);
+        g_noalloc_addr[dev].store(p, std::memory_order_release);
+    }
+    *out = p;
+    return ZERO1_OK;
+}
+
+}  // namespace
+
+extern "C" int zero1_step_dynamic_noalloc(const zero1_plan_t *plan, int32_t shard_begin, int32_t shard_end,
+                                          const void *const *grads, float *master, float *m, float *v,
+                                          void *params, const zero1_adamw_t *hp, zero1_scaler_t *scaler,
+                                          const zero1_loss_scale_policy_t *policy, zero1_stream_t stream)
+{
+    Z1Range r;
+    int rc = z1_range(plan, shard_begin, shard_end, &r);
+    if (rc != ZERO1_OK) return rc;
+    if (r.L > (int64_t)ZERO1_NOALLOC_MAX_ELEMS)
+        return z1_fail(ZERO1_ERANGE,
+                       "no-alloc step: range of %lld elements exceeds the built-in workspace of %d elements "
+                       "(64 MiB); split the call by shards",
+                       (long long)r.L, ZERO1_NOALLOC_MAX_ELEMS);
+    float *sums = nullptr;
+    if ((rc = noalloc_sums(&sums)) != ZERO1_OK) return rc;
+    return zero1_step_dynamic(plan, shard_begin, shard_end, grads, master, m, v, params, hp, scaler, policy,
+                              sums, stream);
+}

@@ -230,14 +230,16 @@ def run_reference(args, w) -> None:
 
 # --------------------------------------------------------- our arm ---------
 
-def config_of(w, state_on_host: bool = False, dynamic: bool = False) -> dict:
+def config_of(w, state_on_host: bool = False, op: str = "step") -> dict:
     c = {"workload": w.name, "n": w.n, "M": w.M, "align": w.align, "global_batch": w.B,
          "loss_scale": w.S, "shards": list(w.shards), "io": "bf16 grads and params, fp32 master/m/v",
          "l2": "inputs larger than L2 (no flush)", "parallelism": "replicas only"}
     if state_on_host:
         c["state"] = "fp32 master/m/v in pinned host memory (offload)"
-    if dynamic:
+    if op == "dynamic":
         c["loss_scaling"] = "dynamic, device-resident (window 1000, hysteresis 2, factor 2)"
+    elif op != "step":
+        c["op"] = op + " (component measurement, not the step)"
     return c
 
 
@@ -289,7 +291,8 @@ def run_ours(args, w) -> None:
         return z.AdamW(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay,
                        loss_scale=w.S, global_batch=w.B, step=t)
 
-    if args.dynamic_loss_scale:
+    op = "dynamic" if args.dynamic_loss_scale else args.op
+    if op == "dynamic":
         policy = z.LossScalePolicy(initial_scale=w.S if w.S > 1 else 2.0 ** 12, factor=2.0, window=1000,
                                    hysteresis=2, min_scale=1.0)
         scaler = z.new_scaler(dev)
@@ -298,11 +301,51 @@ def run_ours(args, w) -> None:
 
         def launch(gr, tt, st=None):
             z.zero1_step_dynamic(plan, sb, se, gr, master, m, v, params, hp(tt), scaler, policy, sums, stream=st)
+        launches_per_step, op_bytes, op_kernel = 3, algorithmic_bytes(nv, L - nv, w.M) + 8 * L, \
+            "dynamic step: k_reduce_scatter + k_apply_sums + k_scaler_update"
+    elif op == "overflow_check":
+        def launch(gr, tt, st=None):
+            z.zero1_overflow_check(plan, sb, se, gr, flag, stream=st)
+        launches_per_step, op_bytes, op_kernel = 1, 2 * w.M * nv, "k_overflow"
+    elif op == "allreduce":
+        if (sb, se) != (0, w.M):
+            raise SystemExit("--op allreduce needs a workload over all shards")
+        outs = [torch.empty(nv, dtype=torch.bfloat16, device=dev) for _ in range(w.M)]
+
+        def launch(gr, tt, st=None):
+            z.dp_allreduce(plan, gr, outs, 1.0 / (w.B * w.S), stream=st)
+        launches_per_step, op_bytes, op_kernel = 1, 4 * w.M * nv, "k_allreduce (bf16 out)"
+    elif op == "unfused":
+        gbuf = torch.empty(L, dtype=torch.float32, device=dev)
+
+        def launch(gr, tt, st=None):
+            h = hp(tt)
+            inv = 1.0 / (w.B * w.S)
+            z.zero1_reduce_scatter(plan, sb, se, gr, inv, gbuf, flag, stream=st)
+            z.zero1_adamw_update(plan, sb, se, gbuf, master, m, v, h, stream=st)
+            z.zero1_all_gather(plan, sb, se, master, params, stream=st)
         launches_per_step = 3
+        op_bytes = nv * (2 * w.M + 4) + (L - nv) * 4 + 28 * L + 6 * nv
+        op_kernel = "unfused: k_reduce_scatter (fp32) + k_adamw + k_all_gather"
+    elif op == "bucketed":
+        # reduce_bucket_size 5e7 elements, as in the pages' DeepSpeed config
+        bucket = args.bucket_elems
+        cuts = list(range(0, L, bucket)) + [L]
+        base_e = sb * plan.shard
+
+        def launch(gr, tt, st=None):
+            h = hp(tt)
+            for e0, e1 in zip(cuts[:-1], cuts[1:]):
+                k = max(0, min(nv, e1) - e0)
+                z.zero1_step_bucket(plan, base_e + e0, base_e + e1, [g[e0:e0 + k] for g in gr], master[e0:],
+                                    m[e0:], v[e0:], params[e0:] if e0 < nv else params[:0], h, flag, stream=st)
+        launches_per_step, op_bytes = len(cuts) - 1, algorithmic_bytes(nv, L - nv, w.M)
+        op_kernel = f"k_fused_step per bucket of {bucket} elements"
     else:
         def launch(gr, tt, st=None):
             z.zero1_reduce_scatter_adamw_allgather(plan, sb, se, gr, master, m, v, params, hp(tt), flag, stream=st)
-        launches_per_step = 1
+        launches_per_step, op_bytes = 1, algorithmic_bytes(nv, L - nv, w.M)
+        op_kernel = f"k_fused_step<M={w.M}>" if w.M <= 8 else "k_fused_step_grouped"
 
     t = 1
     for _ in range(args.warmup):
@@ -340,7 +383,7 @@ def run_ours(args, w) -> None:
     # (no staging copy) and writes the bf16 parameters to a pinned host
     # buffer; the flag is read back; the step ends with a stream synchronize.
     e2e = e2e_copy = None
-    if not args.no_e2e and not args.dynamic_loss_scale:
+    if not args.no_e2e and op == "step":
         e2e_steps = max(3, min(args.steps, args.e2e_steps))
         host_g = [synth.normal_bf16(nv, w.grad_std * w.S, synth.seed_of(w.seed, 7, r, rank)).pin_memory()
                   for r in range(w.M)]
@@ -386,9 +429,7 @@ def run_ours(args, w) -> None:
     if rank != 0:
         return
     peaks = measured_peaks()
-    bytes_launch = algorithmic_bytes(nv, L - nv, w.M)
-    if args.dynamic_loss_scale:      # fp32 sums written and read back: +8 B per element
-        bytes_launch += 8 * L
+    bytes_launch = op_bytes
     achieved = bytes_launch / (kernel_ms * 1e-3) / 1e9
     line = {
         "metric": METRIC,
@@ -403,14 +444,12 @@ def run_ours(args, w) -> None:
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
-        "config": config_of(w, args.state_on_host, args.dynamic_loss_scale),
+        "config": config_of(w, args.state_on_host, op),
         "hbm_gbs": bytes_launch * args.steps / (ms_total * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "peak_source": peaks["source"],
-                     "traffic": None if args.dynamic_loss_scale else recorded_traffic(w.name),
-                     "kernel": ("dynamic step: k_reduce_scatter + k_apply_sums + k_scaler_update"
-                                if args.dynamic_loss_scale else
-                                (f"k_fused_step<M={w.M}>" if w.M <= 8 else "k_fused_step_grouped")),
+                     "traffic": recorded_traffic(w.name) if op == "step" else None,
+                     "kernel": op_kernel,
                      "bytes_per_launch": bytes_launch, "kernel_ms": kernel_ms},
         "cpu_baseline": cpu_baseline,
         "e2e": e2e,
@@ -433,6 +472,12 @@ def main(argv=None) -> int:
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--op", default="step",
+                    choices=["step", "dynamic", "overflow_check", "allreduce", "unfused", "bucketed"],
+                    help="what one timed step runs: the fused ZeRO-1 step (default) or one of the other "
+                         "entry points, for component measurements")
+    ap.add_argument("--bucket-elems", type=int, default=50_000_000,
+                    help="bucket size for --op bucketed (the pages' reduce_bucket_size: 5e7)")
     ap.add_argument("--dynamic-loss-scale", action="store_true",
                     help="time the dynamically scaled step (reduce-scatter to fp32 sums, update, scaler) "
                          "with the fp16 block's policy instead of the fused step")

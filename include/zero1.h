@@ -162,6 +162,29 @@ int zero1_reduce_scatter_adamw_allgather(const zero1_plan_t *plan, int32_t shard
                                          const zero1_adamw_t *hp, uint32_t *overflow_flag,
                                          int32_t skip_if_flag, zero1_stream_t stream);
 
+/* Bucketed step: the fused step on the element range [elem_begin, elem_end)
+ * of the padded flat buffer (0 <= elem_begin < elem_end <= P) - one bucket of
+ * gradients as it arrives during the backward pass [OPT] (reduce_bucket_size,
+ * contiguous_gradients, overlap_comm; "CS336 Lecture 7: Parallelism 1", ZeRO
+ * Stage 2: gradients handed off bucket by bucket instead of held whole).
+ * The step is element-wise, so calls over disjoint buckets that cover [0, P)
+ * give bit for bit one zero1_reduce_scatter_adamw_allgather over all shards,
+ * and a bucket's gradient buffers can be reused once its launch has run: the
+ * full gradient never has to exist at once.
+ *  grads[r]:     device bf16, replica r's gradients of the bucket (the real
+ *                elements, below n, are read; nv = clamp(n - elem_begin, 0,
+ *                elem_end - elem_begin));
+ *  master, m, v: device fp32, element elem_begin of the state holding the
+ *                bucket; elem_end - elem_begin elements are updated;
+ *  params:       device bf16, element elem_begin of the parameters; nv written;
+ *  overflow_flag: device uint32 or NULL, ORed as in the fused step.  A bucket
+ *                cannot wait for later buckets' flags: when steps must be
+ *                skipped on overflow, use zero1_step_dynamic.
+ * EINVAL on a bad range or arguments (as the fused step). */
+int zero1_step_bucket(const zero1_plan_t *plan, int64_t elem_begin, int64_t elem_end,
+                      const void *const *grads, float *master, float *m, float *v, void *params,
+                      const zero1_adamw_t *hp, uint32_t *overflow_flag, zero1_stream_t stream);
+
 /* Overflow check [OPT]: ORs 1 into *flag (device uint32) if the rank order
  * fp32 sum of any real element of shards [shard_begin, shard_end) is inf or
  * NaN.  Reads the same nv elements of grads[r] as the fused step (none, and

@@ -1,0 +1,80 @@
+"""Checkpoint and resume: the optimizer state of a shard is its fp32
+master/m/v, the step counter and (for the dynamic path) the scaler.  Ten
+steps in a row must equal five steps, a save to disk, a load into fresh
+buffers and five more steps, bit for bit ("CS336 Lecture 7: Parallelism 1"
+case studies: long runs are interrupted and resumed)."""
+import pytest
+import torch
+
+import zero_sharded_mixed_zero1_gb300 as z
+from test_gpu_parity import make_grads, make_state
+
+pytestmark = pytest.mark.gpu
+
+
+def test_ten_steps_equal_five_save_load_five(cuda_device, tmp_path):
+    dev = cuda_device
+    M, n = 8, 200_003
+    plan = z.zero1_plan(n, M, 128)
+    P = plan.padded_n
+    grads = [make_grads(M, n, 1e-3, 41, t, dev) for t in range(1, 11)]
+    run = make_state(n, P, 40, dev)
+    ref = [t.clone() for t in run]
+    p_ref = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+    for t in range(1, 11):
+        z.zero1_reduce_scatter_adamw_allgather(plan, 0, M, grads[t - 1], *ref, p_ref, z.AdamW(global_batch=512, step=t))
+    p = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+    for t in range(1, 6):
+        z.zero1_reduce_scatter_adamw_allgather(plan, 0, M, grads[t - 1], *run, p, z.AdamW(global_batch=512, step=t))
+    torch.save({"master": run[0].cpu(), "m": run[1].cpu(), "v": run[2].cpu(), "params": p.cpu(), "next_step": 6,
+                "plan": (plan.n, plan.M, plan.align)}, tmp_path / "shard.pt")
+    del run, p
+    ck = torch.load(tmp_path / "shard.pt")
+    plan2 = z.zero1_plan(*ck["plan"])
+    state = [ck[k].to(dev) for k in ("master", "m", "v")]
+    p2 = ck["params"].to(dev)
+    for t in range(ck["next_step"], 11):
+        z.zero1_reduce_scatter_adamw_allgather(plan2, 0, M, grads[t - 1], *state, p2, z.AdamW(global_batch=512, step=t))
+    torch.cuda.synchronize()
+    for a, b in zip(state, ref):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    assert torch.equal(p2.view(torch.int16), p_ref.view(torch.int16))
+
+
+def test_dynamic_scaler_resumes(cuda_device, tmp_path):
+    dev = cuda_device
+    M, n = 4, 50_000
+    plan = z.zero1_plan(n, M, 8)
+    P = plan.padded_n
+    policy = z.LossScalePolicy(initial_scale=256.0, window=3, hysteresis=1)
+    hp = z.AdamW(global_batch=64, step=1)
+    grads = [make_grads(M, n, 1e-3 * 256, 51, t, dev) for t in range(8)]
+    grads[2][1][7] = float("inf")
+    grads[6][0][9] = float("inf")
+
+    def fresh():
+        st = make_state(n, P, 50, dev)
+        sc = z.new_scaler(dev)
+        z.zero1_scaler_init(sc, policy, hp)
+        return st, sc, torch.zeros(n, dtype=torch.bfloat16, device=dev), torch.empty(P, dtype=torch.float32,
+                                                                                      device=dev)
+
+    ref, sref, pref, sums = fresh()
+    for k in range(8):
+        z.zero1_step_dynamic(plan, 0, M, grads[k], *ref, pref, hp, sref, policy, sums)
+    run, srun, prun, sums2 = fresh()
+    for k in range(4):
+        z.zero1_step_dynamic(plan, 0, M, grads[k], *run, prun, hp, srun, policy, sums2)
+    torch.save({"state": [x.cpu() for x in run], "scaler": srun.cpu(), "params": prun.cpu()}, tmp_path / "dyn.pt")
+    ck = torch.load(tmp_path / "dyn.pt")
+    state = [x.to(dev) for x in ck["state"]]
+    sc = ck["scaler"].to(dev)
+    p = ck["params"].to(dev)
+    for k in range(4, 8):
+        z.zero1_step_dynamic(plan, 0, M, grads[k], *state, p, hp, sc, policy, sums2)
+    torch.cuda.synchronize()
+    for a, b in zip(state, ref):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    assert torch.equal(p.view(torch.int16), pref.view(torch.int16))
+    assert z.scaler_state(sc) == z.scaler_state(sref)
+    assert z.scaler_state(sc)["skipped"] == 2

@@ -137,6 +137,7 @@ def load() -> ctypes.CDLL:
         "zero1_all_gather": [P, i32, i32, vp, vp, vp],
         "zero1_all_gather_shards": [P, vp, vp, vp],
         "zero1_scaler_init": [vp, ctypes.POINTER(_PolicyStruct), A, vp],
+        "zero1_step_bucket": [P, i64, i64, vp, vp, vp, vp, vp, A, vp, vp],
         "zero1_step_dynamic": [P, i32, i32, vp, vp, vp, vp, vp, A, vp, ctypes.POINTER(_PolicyStruct), vp, vp],
     }
     for name, args in sig.items():
@@ -238,6 +239,21 @@ def zero1_reduce_scatter_adamw_allgather(plan: Plan, shard_begin: int, shard_end
         _dev(master, torch.float32, L, "master"), _dev(m, torch.float32, L, "m"),
         _dev(v, torch.float32, L, "v"), _dev(params, torch.bfloat16, nv, "params"),
         ctypes.byref(hp.c_struct()), flag or None, int(bool(skip_if_flag)), _stream(stream)))
+
+
+def zero1_step_bucket(plan: Plan, elem_begin: int, elem_end: int, grads, master, m, v, params, hp: AdamW,
+                      overflow_flag=None, stream=None) -> None:
+    """The fused step on the element range [elem_begin, elem_end) of the
+    padded flat buffer (one gradient bucket).  grads[r]: the bucket's
+    gradients; master/m/v/params: tensors starting at element elem_begin."""
+    _replicas(plan, grads, "grads")
+    L = max(0, elem_end - elem_begin)
+    nv = max(0, min(plan.n - elem_begin, L))
+    flag = 0 if overflow_flag is None else _dev(overflow_flag, torch.int32, 1, "overflow_flag")
+    _check_rc(load().zero1_step_bucket(
+        ctypes.byref(plan), elem_begin, elem_end, _ptrs(grads, torch.bfloat16, nv, "grads"),
+        _dev(master, torch.float32, L, "master"), _dev(m, torch.float32, L, "m"), _dev(v, torch.float32, L, "v"),
+        _dev(params, torch.bfloat16, nv, "params"), ctypes.byref(hp.c_struct()), flag or None, _stream(stream)))
 
 
 def zero1_overflow_check(plan: Plan, shard_begin: int, shard_end: int, grads, flag, stream=None) -> None:

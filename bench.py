@@ -79,10 +79,10 @@ class ClockSampler:
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index: int, period_ms: int = 100):
-        self.path = tempfile.mktemp(prefix="clocks_", suffix=".csv")
         self.proc = None
         try:
-            self.f = open(self.path, "w")
+            self.f = tempfile.NamedTemporaryFile("w", prefix="clocks_", suffix=".csv", delete=False)
+            self.path = self.f.name
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}", "--format=csv",
                  "-lms", str(period_ms)], stdout=self.f, stderr=subprocess.DEVNULL)

@@ -136,3 +136,36 @@ def test_two_gloo_ranks_assemble_the_single_process_result():
         p.join(timeout=60)
     assert res == {0: True, 1: True}
     assert all(p.exitcode == 0 for p in procs)
+
+
+def _worker_dies(rank, world, port, q):
+    import datetime
+    import time
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world, timeout=datetime.timedelta(seconds=5))
+    if rank == 1:
+        os._exit(3)                       # a rank that fails between steps, no collective in flight
+    t0 = time.time()
+    try:
+        out = [torch.zeros(4, dtype=torch.int32) for _ in range(world)]
+        dist.all_gather(out, torch.ones(4, dtype=torch.int32))
+        q.put((rank, "no error"))
+    except Exception as e:                # the survivor learns of it from its next collective
+        q.put((rank, f"detected after {time.time() - t0:.1f}s: {type(e).__name__}"))
+
+
+def test_a_failed_rank_is_detected_not_waited_for():
+    """A rank that dies between steps: the surviving rank's next collective
+    ends with an error within the process group's short timeout instead of
+    hanging (the pages' NCCL-timeout trap, exercised on CPU ranks)."""
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker_dies, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    rank, msg = q.get(timeout=120)
+    for p in procs:
+        p.join(timeout=60)
+    assert rank == 0 and msg.startswith("detected"), msg
+    assert procs[1].exitcode == 3

@@ -188,3 +188,51 @@ def test_flat_1p3b_allreduce_equals_reduce_scatter_plus_all_gather(cuda_device):
         assert torch.equal(gathered[r].view(torch.int16), shards[:n].view(torch.int16))
     del grads, gathered, shards
     free()
+
+
+def test_buffers_beyond_two_to_the_31_elements(cuda_device):
+    """One flat buffer longer than 2^31 elements (ragged, M = 2): 64-bit
+    element indices and byte offsets above 8 GB in the fused step, the
+    overflow check and a bucket crossing 2^31; checked on samples around
+    2^31, the end and at random."""
+    dev = cuda_device
+    M, n, align = 2, 2 ** 31 + 2 ** 20 + 13, 8
+    plan = z.zero1_plan(n, M, align)
+    P = plan.padded_n
+    grads = [synth.normal_bf16(n, 1e-3, synth.seed_of(31, r), dev) for r in range(M)]
+    master = torch.zeros(P, dtype=torch.float32, device=dev)
+    master[:n] = synth.normal_f32(n, 0.02, synth.seed_of(31, 9), dev)
+    m = torch.zeros(P, dtype=torch.float32, device=dev)
+    v = torch.zeros(P, dtype=torch.float32, device=dev)
+    params = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+    rng = np.random.default_rng(31)
+    idx_np = np.unique(np.concatenate([rng.integers(0, n, 1 << 14), np.arange(2 ** 31 - 64, 2 ** 31 + 64),
+                                       np.arange(n - 64, n), np.arange(plan.shard - 32, plan.shard + 32)]))
+    idx = torch.from_numpy(idx_np).to(dev)
+    g_s = [u16(g[idx]) for g in grads]
+    o = [f32(t[idx]) for t in (master, m, v)]
+    op = np.zeros(idx_np.size, np.uint16)
+    hp = z.AdamW(global_batch=64, step=1)
+    flag = torch.zeros(1, dtype=torch.int32, device=dev)
+    z.zero1_overflow_check(plan, 0, M, grads, flag)
+    z.zero1_reduce_scatter_adamw_allgather(plan, 0, M, grads, master, m, v, params, hp, flag)
+    torch.cuda.synchronize()
+    assert int(flag.item()) == 0
+    oracle.zero1_step(g_s, idx_np.size, *o, op, oracle_hp(hp))
+    assert_f32_bits(f32(master[idx]), o[0], "master")
+    assert_f32_bits(f32(v[idx]), o[2], "v")
+    assert_bf16_bits(u16(params[idx]), op, "params")
+    # a bucket across 2^31 (second step), against the oracle on the samples inside it
+    e0, e1 = 2 ** 31 - 1000, 2 ** 31 + 1003
+    hp2 = z.AdamW(global_batch=64, step=2)
+    z.zero1_step_bucket(plan, e0, e1, [g[e0:e1] for g in grads], master[e0:], m[e0:], v[e0:], params[e0:], hp2)
+    torch.cuda.synchronize()
+    inside = (idx_np >= e0) & (idx_np < e1)
+    sel = np.flatnonzero(inside)
+    w2, m2, v2 = (a[sel].copy() for a in o)
+    p2 = np.zeros(sel.size, np.uint16)
+    oracle.zero1_step([g[sel].copy() for g in g_s], sel.size, w2, m2, v2, p2, oracle_hp(hp2))
+    assert_f32_bits(f32(master[idx][torch.from_numpy(sel).to(dev)]), w2, "master in the bucket")
+    assert_bf16_bits(u16(params[idx][torch.from_numpy(sel).to(dev)]), p2, "params in the bucket")
+    del grads, master, m, v, params
+    free()

@@ -301,8 +301,27 @@ def run_ours(args, w) -> None:
 
         def launch(gr, tt, st=None):
             z.zero1_step_dynamic(plan, sb, se, gr, master, m, v, params, hp(tt), scaler, policy, sums, stream=st)
-        launches_per_step, op_bytes, op_kernel = 3, algorithmic_bytes(nv, L - nv, w.M) + 8 * L, \
-            "dynamic step: k_reduce_scatter + k_apply_sums + k_scaler_update"
+        op_kernel = "dynamic step: k_reduce_scatter + k_apply_sums + k_scaler_update"
+        if args.graph:
+            # S and t live on the device: one attempt per gradient set is
+            # captured once and replayed every step
+            for gs in gsets:
+                launch(gs, 1)
+            torch.cuda.synchronize(dev)
+            z.zero1_scaler_init(scaler, policy, hp(1))
+            graphs = {}
+            for gs in gsets:
+                gr_ = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gr_):
+                    launch(gs, 1)
+                graphs[id(gs)] = gr_
+            z.zero1_scaler_init(scaler, policy, hp(1))
+            torch.cuda.synchronize(dev)
+
+            def launch(gr, tt, st=None):      # noqa: F811 - replay instead of the eager call
+                graphs[id(gr)].replay()
+            op_kernel += " (replayed from a CUDA graph)"
+        launches_per_step, op_bytes = 3, algorithmic_bytes(nv, L - nv, w.M) + 8 * L
     elif op == "overflow_check":
         def launch(gr, tt, st=None):
             z.zero1_overflow_check(plan, sb, se, gr, flag, stream=st)
@@ -342,8 +361,13 @@ def run_ours(args, w) -> None:
         launches_per_step, op_bytes = len(cuts) - 1, algorithmic_bytes(nv, L - nv, w.M)
         op_kernel = f"k_fused_step per bucket of {bucket} elements"
     else:
+        # one prepared step per gradient set: buffers validated once, then each
+        # call passes only the hyperparameters (a few microseconds of host time)
+        prepared = {id(gs): z.FusedStep(plan, sb, se, gs, master, m, v, params, flag, stream=stream)
+                    for gs in gsets}
+
         def launch(gr, tt, st=None):
-            z.zero1_reduce_scatter_adamw_allgather(plan, sb, se, gr, master, m, v, params, hp(tt), flag, stream=st)
+            prepared[id(gr)](hp(tt))
         launches_per_step, op_bytes = 1, algorithmic_bytes(nv, L - nv, w.M)
         op_kernel = f"k_fused_step<M={w.M}>" if w.M <= 8 else "k_fused_step_grouped"
 
@@ -476,6 +500,8 @@ def main(argv=None) -> int:
                     choices=["step", "dynamic", "overflow_check", "allreduce", "unfused", "bucketed"],
                     help="what one timed step runs: the fused ZeRO-1 step (default) or one of the other "
                          "entry points, for component measurements")
+    ap.add_argument("--graph", action="store_true",
+                    help="with --op dynamic: capture one attempt in a CUDA graph and replay it each step")
     ap.add_argument("--bucket-elems", type=int, default=50_000_000,
                     help="bucket size for --op bucketed (the pages' reduce_bucket_size: 5e7)")
     ap.add_argument("--dynamic-loss-scale", action="store_true",

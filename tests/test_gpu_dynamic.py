@@ -149,3 +149,53 @@ def test_llama_layers_dynamic_with_pages_policy(cuda_device):
     assert st["step"] == 4 and st["skipped"] == 1 and st["scale"] == w.S and st["hysteresis_left"] == 1
     del grads, master, m, v, params, sums
     torch.cuda.empty_cache()
+
+
+def test_dynamic_step_replays_from_a_cuda_graph(cuda_device):
+    """S and t live on the device, so one dynamically scaled attempt can be
+    captured once and replayed each iteration (new gradients written into
+    the same buffers); the replays give the eager calls' bits, overflow
+    skips included."""
+    dev = cuda_device
+    M, n = 4, 70_001
+    plan = z.zero1_plan(n, M, 128)
+    P = plan.padded_n
+    policy = z.LossScalePolicy(initial_scale=512.0, window=2, hysteresis=1, min_scale=1.0)
+    hp = z.AdamW(global_batch=64, step=1)
+    eager = make_state(n, P, 61, dev)
+    graphed = [t.clone() for t in eager]
+    pe = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+    pg = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+    se, sg = z.new_scaler(dev), z.new_scaler(dev)
+    z.zero1_scaler_init(se, policy, hp)
+    z.zero1_scaler_init(sg, policy, hp)
+    sums_e = torch.empty(P, dtype=torch.float32, device=dev)
+    sums_g = torch.empty(P, dtype=torch.float32, device=dev)
+    gbuf = [torch.zeros(n, dtype=torch.bfloat16, device=dev) for _ in range(M)]
+    torch.cuda.synchronize()
+    # warm up on a side stream (occupancy queries are cached), then capture
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        spare = z.new_scaler(dev)
+        z.zero1_scaler_init(spare, policy, hp)
+        z.zero1_step_dynamic(plan, 0, M, gbuf, *[t.clone() for t in graphed], pg.clone(), hp, spare, policy, sums_g)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        z.zero1_step_dynamic(plan, 0, M, gbuf, *graphed, pg, hp, sg, policy, sums_g)
+    for k in range(7):
+        fresh = [synth.normal_bf16(n, 1e-3 * 512, synth.seed_of(62, k, r), dev) for r in range(M)]
+        if k in (2, 5):
+            fresh[k % M][100 + k] = float("inf")
+        for g, f in zip(gbuf, fresh):
+            g.copy_(f)
+        graph.replay()
+        z.zero1_step_dynamic(plan, 0, M, fresh, *eager, pe, hp, se, policy, sums_e)
+    torch.cuda.synchronize()
+    for x, y, what in zip(eager, graphed, ("master", "m", "v")):
+        assert_f32_bits(f32(y), f32(x), what)
+    assert_bf16_bits(u16(pg), u16(pe), "params")
+    assert z.scaler_state(sg) == z.scaler_state(se)
+    assert z.scaler_state(sg)["skipped"] == 2 and z.scaler_state(sg)["step"] == 6

@@ -296,3 +296,27 @@ def test_unfused_phases_equal_fused_step(cuda_device, M, n, align):
     for x, y, what in zip(a, b, ("master", "m", "v")):
         assert_f32_bits(f32(y), f32(x), what)
     assert_bf16_bits(u16(pb), u16(pa), "params")
+
+
+def test_prepared_step_equals_one_shot_calls(cuda_device):
+    """FusedStep (buffers validated once) gives the one-shot call's bits."""
+    dev = cuda_device
+    M, n = 8, 50_003
+    plan = z.zero1_plan(n, M, 8)
+    a = make_state(n, plan.padded_n, 71, dev, nonzero_moments=True)
+    b = [t.clone() for t in a]
+    pa = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+    pb = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+    grads = make_grads(M, n, 1e-3, 72, 1, dev)
+    fa = torch.zeros(1, dtype=torch.int32, device=dev)
+    step = z.FusedStep(plan, 0, M, grads, *b, pb)
+    for t in range(1, 5):
+        for g, g2 in zip(grads, make_grads(M, n, 1e-3, 72, t, dev)):
+            g.copy_(g2)
+        hp = z.AdamW(global_batch=512, step=t)
+        z.zero1_reduce_scatter_adamw_allgather(plan, 0, M, grads, *a, pa, hp, fa)
+        step(hp)
+    torch.cuda.synchronize()
+    for x, y, what in zip(a, b, ("master", "m", "v")):
+        assert_f32_bits(f32(y), f32(x), what)
+    assert_bf16_bits(u16(pb), u16(pa), "params")

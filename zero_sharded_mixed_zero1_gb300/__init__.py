@@ -12,6 +12,7 @@ from ._lib import (  # noqa: F401
     ZERO1_MAX_REPLICAS,
     SCALER_BYTES,
     AdamW,
+    FusedStep,
     LossScalePolicy,
     Plan,
     Zero1Error,

@@ -368,3 +368,41 @@ def zero1_step_dynamic_noalloc(plan: Plan, shard_begin: int, shard_end: int, gra
                  _dev(v, torch.float32, L, "v"), _dev(params, torch.bfloat16, nv, "params"),
                  ctypes.byref(hp.c_struct()), _scaler_ptr(scaler), ctypes.byref(policy.c_struct()),
                  _stream(stream)))
+
+
+# -- a step bound to fixed buffers ---------------------------------------------
+
+class FusedStep:
+    """The fused ZeRO-1 step bound to fixed buffers, for training loops.
+
+    The tensors are validated and their addresses marshalled once, here; each
+    call then only fills in the step's hyperparameters and calls
+    zero1_reduce_scatter_adamw_allgather, so the host cost per step is a few
+    microseconds (the one-shot function re-checks every tensor each time,
+    which dominates on small problems).  The tensors must stay alive and in
+    place while the object is used.  Launches go to `stream` (default: the
+    stream current when the object is made)."""
+
+    def __init__(self, plan: Plan, shard_begin: int, shard_end: int, grads, master, m, v, params,
+                 overflow_flag=None, skip_if_flag: bool = False, stream=None):
+        _replicas(plan, grads, "grads")
+        _, L, nv = plan.shard_range(shard_begin, shard_end) if 0 <= shard_begin < shard_end <= plan.M \
+            else (0, 0, 0)
+        self._plan = plan
+        self._keep = (grads, master, m, v, params, overflow_flag)
+        self._grads = _ptrs(grads, torch.bfloat16, nv, "grads")
+        flag = 0 if overflow_flag is None else _dev(overflow_flag, torch.int32, 1, "overflow_flag")
+        self._args = (ctypes.byref(plan), shard_begin, shard_end, self._grads,
+                      _dev(master, torch.float32, L, "master"), _dev(m, torch.float32, L, "m"),
+                      _dev(v, torch.float32, L, "v"), _dev(params, torch.bfloat16, nv, "params"))
+        self._hp = _AdamWStruct()
+        self._tail = (flag or None, int(bool(skip_if_flag)), _stream(stream))
+        self._fn = load().zero1_reduce_scatter_adamw_allgather
+
+    def __call__(self, hp: AdamW) -> None:
+        h = self._hp
+        h.lr, h.beta1, h.beta2, h.eps, h.weight_decay = hp.lr, hp.beta1, hp.beta2, hp.eps, hp.weight_decay
+        h.loss_scale, h.global_batch, h.step = hp.loss_scale, hp.global_batch, hp.step
+        rc = self._fn(*self._args, ctypes.byref(h), *self._tail)
+        if rc != ZERO1_OK:
+            _check_rc(rc)

@@ -336,6 +336,33 @@ k_fused_step(const __grid_constant__ GradPtrs g, int M, float *__restrict__ mast
     if (flag && !skip) warp_flag(flag, bad);
 }
 
+// The fused step for M <= 8 on small ranges (at most kWideMaxVec vectors):
+// one vector per thread and iteration at up to four blocks per SM.  Few
+// vectors per thread means the two-deep pipeline has nothing to overlap, and
+// the chain of dependent iterations per thread, not bandwidth, sets the time;
+// four times the threads shortens that chain.
+constexpr int64_t kWideMaxVec = 1 << 18;  // 2M elements
+
+template <int MT>
+__global__ void __launch_bounds__(kBlock, 4)
+k_fused_step_wide(const __grid_constant__ GradPtrs g, int M, float *__restrict__ master,
+                  float *__restrict__ mom, float *__restrict__ var, uint16_t *__restrict__ params,
+                  const Walk w, const Z1Consts c, uint32_t *flag, int skip)
+{
+    if (skip && *reinterpret_cast<volatile uint32_t *>(flag) != 0u) return;
+    const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
+    const int64_t nthr = (int64_t)gridDim.x * kBlock;
+    bool bad = false;
+    for (int64_t i = tid; i < w.nvec; i += nthr) {
+        const int64_t j = w.head + i * kVec;
+        VecLoads<MT> x;
+        x.load(g, master, mom, var, j);
+        fused_vec<MT>(g, M, j, x.q, x.w0, x.w1, x.m0, x.m1, x.v0, x.v1, master, mom, var, params, c, bad);
+    }
+    fused_scalar_rest(g, M, master, mom, var, params, w, c, tid, nthr, bad);
+    if (flag && !skip) warp_flag(flag, bad);
+}
+
 // The fused step for M > 8: the state is read first with the default
 // policy, then the replicas in groups of 8 into the same registers; stores
 // are .cs.  Three resident blocks per SM (at most 85 registers).  Measured on
@@ -967,8 +994,14 @@ int launch_fused_range(const zero1_plan_t *plan, int64_t L, int64_t nv, const vo
         dispatch_m(M, [&](auto mt) {
             constexpr int MT = decltype(mt)::value;
             if constexpr (MT > 0) {
-                const int grid = grid_for(k_fused_step<MT>, work_of(w));
-                k_fused_step<MT><<<grid, kBlock, 0, st>>>(g, M, master, m, v, pp, w, c, overflow_flag, skip);
+                if (w.nvec <= kWideMaxVec) {
+                    const int grid = grid_for(k_fused_step_wide<MT>, work_of(w));
+                    k_fused_step_wide<MT><<<grid, kBlock, 0, st>>>(g, M, master, m, v, pp, w, c, overflow_flag,
+                                                                   skip);
+                } else {
+                    const int grid = grid_for(k_fused_step<MT>, work_of(w));
+                    k_fused_step<MT><<<grid, kBlock, 0, st>>>(g, M, master, m, v, pp, w, c, overflow_flag, skip);
+                }
             }
         });
     }

@@ -248,9 +248,9 @@ __device__ __forceinline__ void store_vec(const float s[kVec], float4 w0, float4
 // One 8-element vector of the fused step for M = MT <= 8 whose loads are in q
 // and the six state registers.
 template <int MT>
-__device__ __forceinline__ void fused_vec(const GradPtrs &, int, int64_t j, const uint4 *q, float4 w0, float4 w1,
-                                          float4 m0, float4 m1, float4 v0, float4 v1, float *master, float *mom,
-                                          float *var, uint16_t *params, const Z1Consts &c, bool &bad)
+__device__ __forceinline__ void fused_vec(int64_t j, const uint4 *q, float4 w0, float4 w1, float4 m0, float4 m1,
+                                          float4 v0, float4 v1, float *master, float *mom, float *var,
+                                          uint16_t *params, const Z1Consts &c, bool &bad)
 {
     float s[kVec];
     unpack8(q[0], s);
@@ -328,7 +328,7 @@ k_fused_step(const __grid_constant__ GradPtrs g, int M, float *__restrict__ mast
         const int64_t j = w.head + i * kVec;
         const bool more = i + nthr < w.nvec;
         if (more) nxt.load(g, master, mom, var, j + nthr * kVec);
-        fused_vec<MT>(g, M, j, cur.q, cur.w0, cur.w1, cur.m0, cur.m1, cur.v0, cur.v1, master, mom, var,
+        fused_vec<MT>(j, cur.q, cur.w0, cur.w1, cur.m0, cur.m1, cur.v0, cur.v1, master, mom, var,
                       params, c, bad);
         if (more) cur = nxt;
     }
@@ -357,7 +357,7 @@ k_fused_step_wide(const __grid_constant__ GradPtrs g, int M, float *__restrict__
         const int64_t j = w.head + i * kVec;
         VecLoads<MT> x;
         x.load(g, master, mom, var, j);
-        fused_vec<MT>(g, M, j, x.q, x.w0, x.w1, x.m0, x.m1, x.v0, x.v1, master, mom, var, params, c, bad);
+        fused_vec<MT>(j, x.q, x.w0, x.w1, x.m0, x.m1, x.v0, x.v1, master, mom, var, params, c, bad);
     }
     fused_scalar_rest(g, M, master, mom, var, params, w, c, tid, nthr, bad);
     if (flag && !skip) warp_flag(flag, bad);

@@ -190,6 +190,14 @@ def _ptrs(tensors, dtype, min_numel, what) -> ctypes.Array:
                                               for i, t in enumerate(tensors)])
 
 
+def _range(plan: Plan, shard_begin: int, shard_end: int) -> tuple[int, int, int]:
+    """(base, L, nv) of a shard range, or zeros for an invalid range (which
+    the library then rejects with its own message)."""
+    if 0 <= shard_begin < shard_end <= plan.M:
+        return plan.shard_range(shard_begin, shard_end)
+    return 0, 0, 0
+
+
 def _replicas(plan: Plan, tensors, what: str) -> None:
     if len(tensors) != plan.M:
         raise ValueError(f"{what}: expected M = {plan.M} tensors, got {len(tensors)}")
@@ -230,8 +238,7 @@ def zero1_reduce_scatter_adamw_allgather(plan: Plan, shard_begin: int, shard_end
     params start at the range's first global element; master/m/v hold the
     range's fp32 state (L elements)."""
     _replicas(plan, grads, "grads")
-    _, L, nv = plan.shard_range(shard_begin, shard_end) if 0 <= shard_begin < shard_end <= plan.M \
-        else (0, 0, 0)
+    _, L, nv = _range(plan, shard_begin, shard_end)
     g = _ptrs(grads, torch.bfloat16, nv, "grads")
     flag = 0 if overflow_flag is None else _dev(overflow_flag, torch.int32, 1, "overflow_flag")
     _check_rc(load().zero1_reduce_scatter_adamw_allgather(
@@ -258,8 +265,7 @@ def zero1_step_bucket(plan: Plan, elem_begin: int, elem_end: int, grads, master,
 
 def zero1_overflow_check(plan: Plan, shard_begin: int, shard_end: int, grads, flag, stream=None) -> None:
     _replicas(plan, grads, "grads")
-    _, _, nv = plan.shard_range(shard_begin, shard_end) if 0 <= shard_begin < shard_end <= plan.M \
-        else (0, 0, 0)
+    _, _, nv = _range(plan, shard_begin, shard_end)
     _check_rc(load().zero1_overflow_check(ctypes.byref(plan), shard_begin, shard_end,
                                           _ptrs(grads, torch.bfloat16, nv, "grads"),
                                           _dev(flag, torch.int32, 1, "flag"), _stream(stream)))
@@ -280,8 +286,7 @@ def dp_allreduce(plan: Plan, grads_in, outs, scale: float = 1.0, stream=None) ->
 def zero1_reduce_scatter(plan: Plan, shard_begin: int, shard_end: int, grads, scale: float, out,
                          flag=None, stream=None) -> None:
     _replicas(plan, grads, "grads")
-    _, L, nv = plan.shard_range(shard_begin, shard_end) if 0 <= shard_begin < shard_end <= plan.M \
-        else (0, 0, 0)
+    _, L, nv = _range(plan, shard_begin, shard_end)
     code = {torch.bfloat16: ZERO1_DTYPE_BF16, torch.float32: ZERO1_DTYPE_F32}.get(out.dtype)
     if code is None:
         raise TypeError("out must be bfloat16 or float32")
@@ -293,8 +298,7 @@ def zero1_reduce_scatter(plan: Plan, shard_begin: int, shard_end: int, grads, sc
 
 def zero1_adamw_update(plan: Plan, shard_begin: int, shard_end: int, g, master, m, v, hp: AdamW,
                        stream=None) -> None:
-    _, L, _ = plan.shard_range(shard_begin, shard_end) if 0 <= shard_begin < shard_end <= plan.M \
-        else (0, 0, 0)
+    _, L, _ = _range(plan, shard_begin, shard_end)
     _check_rc(load().zero1_adamw_update(ctypes.byref(plan), shard_begin, shard_end,
                                         _dev(g, torch.float32, L, "g"), _dev(master, torch.float32, L, "master"),
                                         _dev(m, torch.float32, L, "m"), _dev(v, torch.float32, L, "v"),
@@ -302,8 +306,7 @@ def zero1_adamw_update(plan: Plan, shard_begin: int, shard_end: int, g, master, 
 
 
 def zero1_all_gather(plan: Plan, shard_begin: int, shard_end: int, master, params, stream=None) -> None:
-    _, L, nv = plan.shard_range(shard_begin, shard_end) if 0 <= shard_begin < shard_end <= plan.M \
-        else (0, 0, 0)
+    _, L, nv = _range(plan, shard_begin, shard_end)
     _check_rc(load().zero1_all_gather(ctypes.byref(plan), shard_begin, shard_end,
                                       _dev(master, torch.float32, nv, "master"),
                                       _dev(params, torch.bfloat16, nv, "params"), _stream(stream)))
@@ -334,8 +337,7 @@ def zero1_step_dynamic(plan: Plan, shard_begin: int, shard_end: int, grads, mast
     """One dynamically scaled attempt (S and t from the device scaler);
     sums: fp32 workspace of at least L elements."""
     _replicas(plan, grads, "grads")
-    _, L, nv = plan.shard_range(shard_begin, shard_end) if 0 <= shard_begin < shard_end <= plan.M \
-        else (0, 0, 0)
+    _, L, nv = _range(plan, shard_begin, shard_end)
     _check_rc(load().zero1_step_dynamic(
         ctypes.byref(plan), shard_begin, shard_end, _ptrs(grads, torch.bfloat16, nv, "grads"),
         _dev(master, torch.float32, L, "master"), _dev(m, torch.float32, L, "m"), _dev(v, torch.float32, L, "v"),
@@ -361,8 +363,7 @@ def zero1_step_dynamic_noalloc(plan: Plan, shard_begin: int, shard_end: int, gra
                        ctypes.POINTER(_PolicyStruct), vp]
         fn.restype = ctypes.c_int
     _replicas(plan, grads, "grads")
-    _, L, nv = plan.shard_range(shard_begin, shard_end) if 0 <= shard_begin < shard_end <= plan.M \
-        else (0, 0, 0)
+    _, L, nv = _range(plan, shard_begin, shard_end)
     _check_rc(fn(ctypes.byref(plan), shard_begin, shard_end, _ptrs(grads, torch.bfloat16, nv, "grads"),
                  _dev(master, torch.float32, L, "master"), _dev(m, torch.float32, L, "m"),
                  _dev(v, torch.float32, L, "v"), _dev(params, torch.bfloat16, nv, "params"),

@@ -387,8 +387,7 @@ class FusedStep:
     def __init__(self, plan: Plan, shard_begin: int, shard_end: int, grads, master, m, v, params,
                  overflow_flag=None, skip_if_flag: bool = False, stream=None):
         _replicas(plan, grads, "grads")
-        _, L, nv = plan.shard_range(shard_begin, shard_end) if 0 <= shard_begin < shard_end <= plan.M \
-            else (0, 0, 0)
+        _, L, nv = _range(plan, shard_begin, shard_end)
         self._plan = plan
         self._keep = (grads, master, m, v, params, overflow_flag)
         self._grads = _ptrs(grads, torch.bfloat16, nv, "grads")

@@ -320,3 +320,32 @@ def test_prepared_step_equals_one_shot_calls(cuda_device):
     for x, y, what in zip(a, b, ("master", "m", "v")):
         assert_f32_bits(f32(y), f32(x), what)
     assert_bf16_bits(u16(pb), u16(pa), "params")
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 5, 7, 8])
+def test_pipelined_kernel_above_the_small_range_threshold(cuda_device, M):
+    """Ranges above 2^21 elements run the two-deep pipelined kernel (smaller
+    ones the wide kernel): every M it is compiled for, a ragged tail, a
+    per-element head (a range starting at element 3), every element against
+    the oracle."""
+    dev = cuda_device
+    n = 2 ** 21 + 2 ** 17 + 37
+    plan = z.zero1_plan(n, M, 1)
+    P, s = plan.padded_n, plan.shard
+    master, m, v = make_state(n, P, 500 + M, dev, nonzero_moments=True)
+    params = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+    o = [f32(master), f32(m), f32(v)]
+    for t in (1, 2):
+        hp = z.AdamW(global_batch=max(M, 16), step=t)
+        grads = make_grads(M, n, 1e-2, 510 + M, t, dev)
+        if t == 1:
+            z.zero1_reduce_scatter_adamw_allgather(plan, 0, M, grads, master, m, v, params, hp)
+        else:        # a large range starting at element 3: a per-element head, then vectors
+            z.zero1_step_bucket(plan, 0, 3, grads, master, m, v, params, hp)
+            z.zero1_step_bucket(plan, 3, P, [g[3:] for g in grads], master[3:], m[3:], v[3:], params[3:], hp)
+        torch.cuda.synchronize()
+        want = oracle_step(plan, [u16(g) for g in grads], *o, oracle_hp(hp))
+        assert_f32_bits(f32(master), o[0], f"master t={t}")
+        assert_f32_bits(f32(m), o[1], f"m t={t}")
+        assert_f32_bits(f32(v), o[2], f"v t={t}")
+        assert_bf16_bits(u16(params), want, f"params t={t}")

@@ -500,6 +500,8 @@ def main(argv=None) -> int:
                     choices=["step", "dynamic", "overflow_check", "allreduce", "unfused", "bucketed"],
                     help="what one timed step runs: the fused ZeRO-1 step (default) or one of the other "
                          "entry points, for component measurements")
+    ap.add_argument("--replicas", type=int, default=0, help="override the workload's M (measurement sweeps)")
+    ap.add_argument("--params", type=int, default=0, help="override the workload's n (measurement sweeps)")
     ap.add_argument("--graph", action="store_true",
                     help="with --op dynamic: capture one attempt in a CUDA graph and replay it each step")
     ap.add_argument("--bucket-elems", type=int, default=50_000_000,
@@ -517,6 +519,11 @@ def main(argv=None) -> int:
     if args.workload not in W.BY_NAME:
         ap.error(f"unknown workload {args.workload}; choose from {sorted(W.BY_NAME)}")
     w = W.BY_NAME[args.workload]
+    if args.replicas or args.params:          # size overrides for measurement sweeps
+        import dataclasses
+        w = dataclasses.replace(w, M=args.replicas or w.M, n=args.params or w.n,
+                                B=max(w.B, args.replicas or 0), shard_begin=0, shard_end=None,
+                                name=f"{w.name}[M={args.replicas or w.M},n={args.params or w.n}]")
     if args.impl == "reference":
         run_reference(args, w)
     else:

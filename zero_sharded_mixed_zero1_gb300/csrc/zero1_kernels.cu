@@ -312,7 +312,7 @@ __device__ __forceinline__ void fused_scalar_rest(const GradPtrs &g, int M, floa
 // (launch bounds of one block per SM) beat higher occupancy with one vector
 // in flight.  fp32 state is read with L1::no_allocate and every store is .cs.
 template <int MT>
-__global__ void __launch_bounds__(kBlock, 1)
+__global__ void __launch_bounds__(kBlock, MT <= 2 ? 2 : 1)
 k_fused_step(const __grid_constant__ GradPtrs g, int M, float *__restrict__ master,
              float *__restrict__ mom, float *__restrict__ var, uint16_t *__restrict__ params,
              const Walk w, const Z1Consts c, uint32_t *flag, int skip)

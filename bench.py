@@ -394,7 +394,8 @@ def run_ours(args, w) -> None:
     barrier(world)
     wall1 = time.time()
     ms_local = start.elapsed_time(end)
-    kernel_ms = float(np.mean([evs[2 * i].elapsed_time(evs[2 * i + 1]) for i in range(args.steps)]))
+    launch_ms = np.array([evs[2 * i].elapsed_time(evs[2 * i + 1]) for i in range(args.steps)])
+    kernel_ms = float(launch_ms.mean())
     clocks = sampler.summary(wall0, wall1) if sampler else None
     if sampler:
         sampler.stop()
@@ -474,7 +475,8 @@ def run_ours(args, w) -> None:
                      "frac": achieved / peaks["hbm_gbs"], "peak_source": peaks["source"],
                      "traffic": recorded_traffic(w.name) if op == "step" else None,
                      "kernel": op_kernel,
-                     "bytes_per_launch": bytes_launch, "kernel_ms": kernel_ms},
+                     "bytes_per_launch": bytes_launch, "kernel_ms": kernel_ms,
+                     "kernel_ms_median": float(np.median(launch_ms)), "kernel_ms_min": float(launch_ms.min())},
         "cpu_baseline": cpu_baseline,
         "e2e": e2e,
         "e2e_copy_then_step": e2e_copy,

@@ -346,6 +346,11 @@ def run_ours(args, w) -> None:
         launches_per_step = 3
         op_bytes = nv * (2 * w.M + 4) + (L - nv) * 4 + 28 * L + 6 * nv
         op_kernel = "unfused: k_reduce_scatter (fp32) + k_adamw + k_all_gather"
+    elif op == "tma":
+        def launch(gr, tt, st=None):
+            z.zero1_step_tma(plan, sb, se, gr, master, m, v, params, hp(tt), flag, stream=st)
+        launches_per_step, op_bytes = 1, algorithmic_bytes(nv, L - nv, w.M)
+        op_kernel = "k_fused_step_tma (shared-memory staging by bulk copies)"
     elif op == "bucketed":
         # reduce_bucket_size 5e7 elements, as in the pages' DeepSpeed config
         bucket = args.bucket_elems
@@ -499,7 +504,7 @@ def main(argv=None) -> int:
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--op", default="step",
-                    choices=["step", "dynamic", "overflow_check", "allreduce", "unfused", "bucketed"],
+                    choices=["step", "dynamic", "overflow_check", "allreduce", "unfused", "bucketed", "tma"],
                     help="what one timed step runs: the fused ZeRO-1 step (default) or one of the other "
                          "entry points, for component measurements")
     ap.add_argument("--replicas", type=int, default=0, help="override the workload's M (measurement sweeps)")

@@ -185,6 +185,28 @@ int zero1_step_bucket(const zero1_plan_t *plan, int64_t elem_begin, int64_t elem
                       const void *const *grads, float *master, float *m, float *v, void *params,
                       const zero1_adamw_t *hp, uint32_t *overflow_flag, zero1_stream_t stream);
 
+/* The fused step with its vector body staged through shared memory by the
+ * Tensor Memory Accelerator [Z1], [DP], [MEM]: a producer warp issues 1-D bulk
+ * copies (cp.async.bulk, completion counted on mbarriers) of each tile's M
+ * gradient slices and master/m/v into a ring of shared-memory stages, and
+ * eight consumer warps compute from there.  Same arguments and bit for bit the
+ * same results as zero1_reduce_scatter_adamw_allgather; every buffer must be
+ * device memory (EINVAL otherwise).  On GB300 this staging measured slower
+ * than the direct register-pipelined loads of the fused step (the stream has
+ * no reuse), so the fused step does not use it; it is kept so the comparison
+ * can be reproduced.  Its waits are bounded: a wait that runs out (1 s) sets
+ * bit 0 of the device status (zero1_device_status) and the kernel returns. */
+int zero1_step_tma(const zero1_plan_t *plan, int32_t shard_begin, int32_t shard_end,
+                   const void *const *grads, float *master, float *m, float *v, void *params,
+                   const zero1_adamw_t *hp, uint32_t *overflow_flag, int32_t skip_if_flag,
+                   zero1_stream_t stream);
+
+/* The library's device status word on the current device: bit 0 set if a
+ * bounded wait in a kernel ran out (the kernel then stopped early and its
+ * outputs are incomplete).  Copies it to *status (synchronous with the
+ * device) and clears it if `clear` is nonzero. */
+int zero1_device_status(uint32_t *status, int32_t clear);
+
 /* Overflow check [OPT]: ORs 1 into *flag (device uint32) if the rank order
  * fp32 sum of any real element of shards [shard_begin, shard_end) is inf or
  * NaN.  Reads the same nv elements of grads[r] as the fused step (none, and

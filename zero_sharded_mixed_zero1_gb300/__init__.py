@@ -32,6 +32,8 @@ from ._lib import (  # noqa: F401
     zero1_reduce_scatter_adamw_allgather,
     zero1_scaler_init,
     zero1_step_bucket,
+    zero1_step_tma,
+    zero1_device_status,
     zero1_step_dynamic,
     zero1_step_dynamic_noalloc,
 )

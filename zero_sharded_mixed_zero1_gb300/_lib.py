@@ -138,6 +138,8 @@ def load() -> ctypes.CDLL:
         "zero1_all_gather_shards": [P, vp, vp, vp],
         "zero1_scaler_init": [vp, ctypes.POINTER(_PolicyStruct), A, vp],
         "zero1_step_bucket": [P, i64, i64, vp, vp, vp, vp, vp, A, vp, vp],
+        "zero1_step_tma": [P, i32, i32, vp, vp, vp, vp, vp, A, vp, i32, vp],
+        "zero1_device_status": [vp, i32],
         "zero1_step_dynamic": [P, i32, i32, vp, vp, vp, vp, vp, A, vp, ctypes.POINTER(_PolicyStruct), vp, vp],
     }
     for name, args in sig.items():
@@ -246,6 +248,28 @@ def zero1_reduce_scatter_adamw_allgather(plan: Plan, shard_begin: int, shard_end
         _dev(master, torch.float32, L, "master"), _dev(m, torch.float32, L, "m"),
         _dev(v, torch.float32, L, "v"), _dev(params, torch.bfloat16, nv, "params"),
         ctypes.byref(hp.c_struct()), flag or None, int(bool(skip_if_flag)), _stream(stream)))
+
+
+def zero1_step_tma(plan: Plan, shard_begin: int, shard_end: int, grads, master, m, v, params, hp: AdamW,
+                   overflow_flag=None, skip_if_flag: bool = False, stream=None) -> None:
+    """The fused step with shared-memory staging by bulk copies (same
+    arguments and bits as zero1_reduce_scatter_adamw_allgather; device
+    memory only)."""
+    _replicas(plan, grads, "grads")
+    _, L, nv = _range(plan, shard_begin, shard_end)
+    flag = 0 if overflow_flag is None else _dev(overflow_flag, torch.int32, 1, "overflow_flag")
+    _check_rc(load().zero1_step_tma(
+        ctypes.byref(plan), shard_begin, shard_end, _ptrs(grads, torch.bfloat16, nv, "grads"),
+        _dev(master, torch.float32, L, "master"), _dev(m, torch.float32, L, "m"), _dev(v, torch.float32, L, "v"),
+        _dev(params, torch.bfloat16, nv, "params"), ctypes.byref(hp.c_struct()), flag or None,
+        int(bool(skip_if_flag)), _stream(stream)))
+
+
+def zero1_device_status(clear: bool = True) -> int:
+    """The library's device status word (bit 0: a bounded wait ran out)."""
+    out = ctypes.c_uint32()
+    _check_rc(load().zero1_device_status(ctypes.byref(out), int(bool(clear))))
+    return out.value
 
 
 def zero1_step_bucket(plan: Plan, elem_begin: int, elem_end: int, grads, master, m, v, params, hp: AdamW,

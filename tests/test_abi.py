@@ -156,3 +156,51 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(L._build, "LIB", str(tmp_path / "missing.so"))
     with pytest.raises(ImportError):
         L.load()
+
+
+C_PROGRAM = r"""
+#include <stdio.h>
+#include <string.h>
+#include "zero1.h"
+
+int main(void)
+{
+    zero1_plan_t p;
+    int64_t naive = 0, z1 = 0;
+    int64_t numels[3] = {5, 7, 11};
+    int64_t t[4], toff[4], soff[4], len[4];
+    int32_t count = 0;
+    if (zero1_plan(1300000000LL, 8, 128, &p) != ZERO1_OK) return 1;
+    if (p.padded_n != 1300000768LL || p.shard != 162500096LL) return 2;
+    if (zero1_plan_memory(&p, &naive, &z1) != ZERO1_OK || naive != 16LL * 1300000000LL) return 3;
+    if (zero1_plan(23, 2, 4, &p) != ZERO1_OK) return 4;
+    if (zero1_plan_segments(&p, numels, 3, 1, 4, t, toff, soff, len, &count) != ZERO1_OK) return 5;
+    printf("%lld %lld %d", (long long)p.padded_n, (long long)p.shard, count);
+    for (int i = 0; i < count; ++i) printf(" (%lld,%lld,%lld,%lld)", (long long)t[i], (long long)toff[i],
+                                           (long long)soff[i], (long long)len[i]);
+    if (zero1_plan(10, 65, 1, &p) != ZERO1_ERANGE) return 6;
+    if (strcmp(zero1_strerror(ZERO1_ERANGE), "size or replica count out of the supported range") != 0) return 7;
+    printf(" | %s\n", zero1_last_error());
+    return zero1_abi_version() == 1 ? 0 : 8;
+}
+"""
+
+
+def test_header_is_plain_c_and_links(lib, tmp_path):
+    """include/zero1.h compiles as C99 and a C program links libzero1.so and
+    calls its host-only functions."""
+    import subprocess
+    src = tmp_path / "use_abi.c"
+    src.write_text(C_PROGRAM)
+    exe = tmp_path / "use_abi"
+    libdir = os.path.dirname(zbuild.LIB)
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    str(src), "-o", str(exe), "-L", libdir, "-l:libzero1.so", f"-Wl,-rpath,{libdir}"], check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, (r.returncode, r.stdout, r.stderr)
+    head, _, err = r.stdout.partition(" | ")
+    P, s, count, *segs = head.split(" ")
+    assert (int(P), int(s)) == oracle.plan(23, 2, 4)
+    want = oracle.segments([5, 7, 11], int(s), 1)
+    assert int(count) == len(want) and segs == [f"({a},{b},{c},{d})" for a, b, c, d in want]
+    assert "M = 65" in err

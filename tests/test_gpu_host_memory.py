@@ -76,3 +76,34 @@ def test_pageable_host_tensor_is_rejected(cuda_device):
     grads = [torch.zeros(100, dtype=torch.bfloat16)]       # pageable: not accepted
     with pytest.raises(ValueError):
         z.zero1_reduce_scatter_adamw_allgather(plan, 0, 1, grads, master, m, v, params, z.AdamW())
+
+
+@pytest.mark.parametrize("M,n,align,chunk,shards", [(8, 100_003, 128, 4096, None), (4, 50_000, 1, 1000, (1, 3)),
+                                                    (13, 9_999, 8, 777, None), (2, 20, 128, 8, (1, 2))])
+def test_host_streamed_step_equals_fused_step(cuda_device, M, n, align, chunk, shards):
+    """Gradients in pinned host memory, copied chunk by chunk on a copy stream
+    while the step runs on the previous chunk: the fused step's bits, and the
+    parameters copied back to host memory."""
+    dev = cuda_device
+    plan = z.zero1_plan(n, M, align)
+    sb, se = shards or (0, M)
+    base, L, nv = plan.shard_range(sb, se)
+    a = [t[base:base + L].clone() for t in make_state(n, plan.padded_n, 90 + M, dev, nonzero_moments=True)]
+    b = [t.clone() for t in a]
+    pa = torch.zeros(max(nv, 1), dtype=torch.bfloat16, device=dev)
+    pb = torch.zeros(max(nv, 1), dtype=torch.bfloat16, device=dev)
+    host_g = [torch.zeros(max(nv, 1), dtype=torch.bfloat16).pin_memory() for _ in range(M)]
+    host_p = torch.zeros(max(nv, 1), dtype=torch.bfloat16).pin_memory()
+    step = z.HostStreamedStep(plan, sb, se, host_g, *b, pb, chunk_elems=chunk, params_host=host_p)
+    for t in (1, 2, 3):
+        grads = [g[base:base + nv] for g in make_grads(M, n, 1e-2, 91 + M, t, dev)]
+        for hg, g in zip(host_g, grads):
+            hg[:nv].copy_(g.cpu())
+        hp = z.AdamW(global_batch=max(M, 64), step=t)
+        z.zero1_reduce_scatter_adamw_allgather(plan, sb, se, grads, *a, pa, hp)
+        step(hp)
+        torch.cuda.synchronize()
+        for x, y, what in zip(a, b, ("master", "m", "v")):
+            assert_f32_bits(f32(y), f32(x), f"{what} t={t}")
+        assert_bf16_bits(u16(pb[:nv]), u16(pa[:nv]), f"params t={t}")
+        assert_bf16_bits(u16(host_p[:nv]), u16(pa[:nv]), f"params on host t={t}")

@@ -37,3 +37,4 @@ from ._lib import (  # noqa: F401
     zero1_step_dynamic,
     zero1_step_dynamic_noalloc,
 )
+from .host_stream import HostStreamedStep  # noqa: E402,F401

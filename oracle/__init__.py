@@ -74,6 +74,7 @@ def _L():
                                        f32, f32, f32, f32, f32, f32, i64, i64, vp, i32]
         lib.orc_zero1_step.restype = ctypes.c_int
         lib.orc_allreduce.argtypes = [i32, vp, i64, f32, i32, vp]
+        lib.orc_checksum16.argtypes = [vp, i64, vp]
         lib.orc_scaler_init.argtypes = [vp, f32, i32, i64]
         lib.orc_scaler_update.argtypes = [vp, ctypes.c_uint32, f32, i32, i32, f32]
         lib.orc_zero1_dynamic_attempt.argtypes = [i32, vp, i64, i64, vp, vp, vp, vp, f32, f32, f32, f32, f32,
@@ -293,3 +294,14 @@ def zero1_dynamic_attempt(grads, n_valid: int, master, m, v, params, hp: AdamW, 
     if rc != 0:
         raise MemoryError("oracle step could not allocate its gradient buffer")
     return int(f.value)
+
+
+def checksum16(buf: np.ndarray) -> tuple[int, int]:
+    """(sum of the 16-bit units, sum of (index + 1) * unit), both mod 2^64."""
+    b = np.ascontiguousarray(buf)
+    if b.nbytes % 2:
+        raise ValueError("buffer length must be a whole number of 16-bit units")
+    u = b.view(np.uint16).reshape(-1)
+    out = np.zeros(2, np.uint64)
+    _L().orc_checksum16(_ptr(u), u.size, _ptr(out))
+    return int(out[0]), int(out[1])

@@ -368,3 +368,25 @@ int orc_zero1_dynamic_attempt(int32_t M, const uint16_t *const *grads, int64_t l
     if (flag_out) *flag_out = f;
     return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Consistency checksum of a buffer (the silent-data-corruption guard of    */
+/* the replicated parameters: "CS336 Lecture 7: Parallelism 1" case studies */
+/* report silent data corruption on large runs; after the all-gather every  */
+/* rank must hold the same parameters).  Over the buffer's 16-bit units      */
+/* u_0 .. u_{U-1} (little-endian):                                           */
+/*   out[0] = sum u_i            mod 2^64                                    */
+/*   out[1] = sum (i + 1) * u_i  mod 2^64                                    */
+/* Exact integer sums, so any order of summation gives the same words.       */
+/* ------------------------------------------------------------------------ */
+
+void orc_checksum16(const uint16_t *u, int64_t U, uint64_t *out)
+{
+    uint64_t s1 = 0, s2 = 0;
+    for (int64_t i = 0; i < U; ++i) {
+        s1 += (uint64_t)u[i];
+        s2 += (uint64_t)(i + 1) * (uint64_t)u[i];
+    }
+    out[0] = s1;
+    out[1] = s2;
+}

@@ -33,6 +33,8 @@ MUTANTS = {
     "scaler_ignores_hysteresis": ("        sc->hyst_left -= 1;", "        sc->hyst_left -= 2;"),
     "scaler_window_off_by_one": ("        if (sc->good >= window) {", "        if (sc->good > window) {"),
     "skip_advances_t": ("        sc->skipped += 1;", "        sc->skipped += 1;\n        sc->step += 1;"),
+    "checksum_index_from_zero": ("        s2 += (uint64_t)(i + 1) * (uint64_t)u[i];", "        s2 += (uint64_t)i * (uint64_t)u[i];"),
+    "checksum_drops_units": ("        s1 += (uint64_t)u[i];", "        s1 += (uint64_t)(u[i] & 0xFFFEu);"),
     "scaler_no_floor": ("            sc->scale = down < min_scale ? min_scale : down;", "            sc->scale = down;"),
 }
 
@@ -49,6 +51,7 @@ def test_pins_catch_mutant(name, tmp_path):
     env = dict(os.environ, ZERO1_ORACLE_LIB=str(so))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_oracle_pins.py"),
-                        os.path.join(ROOT, "tests", "test_oracle_loss_scale.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_loss_scale.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_checksum.py")],
                        env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} survived the pins"

@@ -352,6 +352,19 @@ int zero1_step_dynamic_noalloc(const zero1_plan_t *plan, int32_t shard_begin, in
                                const zero1_adamw_t *hp, zero1_scaler_t *scaler,
                                const zero1_loss_scale_policy_t *policy, zero1_stream_t stream);
 
+/* Consistency checksum of a buffer: the silent-data-corruption guard for the
+ * replicated parameters ("CS336 Lecture 7: Parallelism 1" case studies report
+ * silent data corruption on large runs; after the all-gather every rank must
+ * hold the same parameters, so ranks can compare these two words).  Over the
+ * buffer's 16-bit units u_0 .. u_{U-1} (U = nbytes / 2, little-endian):
+ *   out[0] = sum u_i mod 2^64,  out[1] = sum (i + 1) * u_i mod 2^64.
+ * Exact integer sums: the result does not depend on the order of summation.
+ * Any change of one unit changes out[0]; swapping two unequal units changes
+ * out[1].  data: device (or pinned host) memory, 2-byte aligned; nbytes even;
+ * out: device, two uint64, 8-byte aligned, overwritten (cleared on `stream`
+ * first). */
+int zero1_checksum(const void *data, int64_t nbytes, uint64_t *out, zero1_stream_t stream);
+
 /* Text of a status code. */
 const char *zero1_strerror(int code);
 

@@ -169,3 +169,40 @@ def test_a_failed_rank_is_detected_not_waited_for():
         p.join(timeout=60)
     assert rank == 0 and msg.startswith("detected"), msg
     assert procs[1].exitcode == 3
+
+
+def _worker_sdc(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        import oracle
+        rng = np.random.default_rng(0)                       # the same parameters on every rank
+        params = rng.integers(0, 1 << 16, 10_007).astype(np.uint16)
+        if rank == 1:
+            params[4321] ^= np.uint16(1 << 3)                 # one silently corrupted bit
+        mine = torch.tensor([oracle.checksum16(params)[0] & 0x7FFFFFFFFFFFFFFF,
+                             oracle.checksum16(params)[1] & 0x7FFFFFFFFFFFFFFF], dtype=torch.int64)
+        all_sums = [torch.zeros(2, dtype=torch.int64) for _ in range(world)]
+        dist.all_gather(all_sums, mine)
+        q.put((rank, all(torch.equal(all_sums[0], s) for s in all_sums)))
+    except Exception as e:
+        q.put((rank, f"error: {e!r}"))
+        raise
+    finally:
+        dist.destroy_process_group()
+
+
+def test_ranks_compare_parameter_checksums():
+    """After the all-gather every rank holds the same parameters: ranks
+    exchange their checksums (two words each) and all see the one rank whose
+    copy has a flipped bit."""
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker_sdc, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+    assert res == {0: False, 1: False}

@@ -140,6 +140,7 @@ def load() -> ctypes.CDLL:
         "zero1_step_bucket": [P, i64, i64, vp, vp, vp, vp, vp, A, vp, vp],
         "zero1_step_tma": [P, i32, i32, vp, vp, vp, vp, vp, A, vp, i32, vp],
         "zero1_device_status": [vp, i32],
+        "zero1_checksum": [vp, i64, vp, vp],
         "zero1_step_dynamic": [P, i32, i32, vp, vp, vp, vp, vp, A, vp, ctypes.POINTER(_PolicyStruct), vp, vp],
     }
     for name, args in sig.items():
@@ -263,6 +264,23 @@ def zero1_step_tma(plan: Plan, shard_begin: int, shard_end: int, grads, master, 
         _dev(master, torch.float32, L, "master"), _dev(m, torch.float32, L, "m"), _dev(v, torch.float32, L, "v"),
         _dev(params, torch.bfloat16, nv, "params"), ctypes.byref(hp.c_struct()), flag or None,
         int(bool(skip_if_flag)), _stream(stream)))
+
+
+def zero1_checksum(t: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Consistency checksum of a tensor's bytes as 16-bit units: a device
+    int64 tensor of two words (sum of units, sum of (index + 1) * unit, both
+    mod 2^64; read them as unsigned)."""
+    if not isinstance(t, torch.Tensor) or not t.is_contiguous():
+        raise ValueError("checksum: expected a contiguous tensor")
+    if t.device.type != "cuda" and not (t.device.type == "cpu" and t.is_pinned()):
+        raise ValueError("checksum: must be a CUDA tensor or a pinned host tensor")
+    nbytes = t.numel() * t.element_size()
+    if out is None:
+        dev = t.device if t.device.type == "cuda" else torch.device("cuda", torch.cuda.current_device())
+        out = torch.empty(2, dtype=torch.int64, device=dev)
+    _check_rc(load().zero1_checksum(t.data_ptr() if nbytes else None, nbytes,
+                                    _dev(out, torch.int64, 2, "out"), _stream(stream)))
+    return out
 
 
 def zero1_device_status(clear: bool = True) -> int:

@@ -36,7 +36,10 @@ import torch
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 METRIC = "params/s and achieved HBM GB/s (% of GB300 peak) per fused ZeRO-1 step"
-KERNEL_SOURCE = os.path.join(ROOT, "zero_sharded_mixed_zero1_gb300", "csrc", "zero1_kernels.cu")
+# The fused kernel's sources, hashed in this order (concatenated) to tell
+# whether recorded ncu traffic was taken on the kernel as it stands.
+KERNEL_SOURCES = [os.path.join(ROOT, "zero_sharded_mixed_zero1_gb300", "csrc", f)
+                  for f in ("zero1_fused.cu", "zero1_device.cuh", "zero1_internal.h")]
 
 
 # ------------------------------------------------------------ helpers ------
@@ -68,7 +71,7 @@ def recorded_traffic(workload: str):
     tr = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
     if not sha or not tr:
         return None
-    cur = hashlib.sha256(open(KERNEL_SOURCE, "rb").read()).hexdigest()
+    cur = hashlib.sha256(b"".join(open(f, "rb").read() for f in KERNEL_SOURCES)).hexdigest()
     return int(tr.group(1)) if sha.group(1) == cur else None
 
 

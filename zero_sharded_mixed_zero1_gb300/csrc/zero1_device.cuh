@@ -1,0 +1,458 @@
+// zero1_device.cuh - device and launch helpers shared by the library's CUDA
+// sources (library-internal).
+//
+// Everything here sits in an anonymous namespace on purpose: kernels that two
+// sources instantiate (the reduce-scatter) must have internal linkage, or the
+// merged host stubs of one source would launch the other source's module.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+#include <cmath>
+#include <type_traits>
+
+#include "zero1.h"
+#include "zero1_internal.h"
+
+namespace {
+
+constexpr int kVec = 8;      // elements per thread per iteration (16 B of bf16)
+constexpr int kBlock = 256;  // threads per block
+
+struct GradPtrs {
+    const uint16_t *p[ZERO1_MAX_REPLICAS];
+};
+struct OutPtrs {
+    void *p[ZERO1_MAX_REPLICAS];
+};
+
+// How a range of L elements is walked: [0, head) per element, then nvec
+// aligned 8-element vectors [head, head + 8*nvec) that are all real
+// parameters, then [head + 8*nvec, L) per element (real below nv, padding
+// above).
+struct Walk {
+    int64_t L, nv, head, nvec;
+};
+
+// ---------------------------------------------------------------- helpers --
+
+__device__ __forceinline__ uint4 ld_stream_u4(const void *p)
+{
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint16_t ld_stream_u16(const uint16_t *p)
+{
+    uint16_t r;
+    asm("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(r) : "l"(p));
+    return r;
+}
+
+// bf16 -> fp32 is exact: the bf16 code is the upper half of the binary32.
+__device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
+__device__ __forceinline__ float bf_one(uint16_t x) { return __uint_as_float((uint32_t)x << 16); }
+
+__device__ __forceinline__ void unpack8(const uint4 q, float s[kVec])
+{
+    s[0] = bf_lo(q.x); s[1] = bf_hi(q.x); s[2] = bf_lo(q.y); s[3] = bf_hi(q.y);
+    s[4] = bf_lo(q.z); s[5] = bf_hi(q.z); s[6] = bf_lo(q.w); s[7] = bf_hi(q.w);
+}
+
+__device__ __forceinline__ void add8(const uint4 q, float s[kVec])
+{
+    s[0] = __fadd_rn(s[0], bf_lo(q.x)); s[1] = __fadd_rn(s[1], bf_hi(q.x));
+    s[2] = __fadd_rn(s[2], bf_lo(q.y)); s[3] = __fadd_rn(s[3], bf_hi(q.y));
+    s[4] = __fadd_rn(s[4], bf_lo(q.z)); s[5] = __fadd_rn(s[5], bf_hi(q.z));
+    s[6] = __fadd_rn(s[6], bf_lo(q.w)); s[7] = __fadd_rn(s[7], bf_hi(q.w));
+}
+
+// fp32 -> bf16, round to nearest even (cvt.rn.bf16x2.f32).
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+__device__ __forceinline__ uint16_t to_bf16(float x)
+{
+    return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+// Rank-order fp32 sum of 8 consecutive elements starting at j (16-byte
+// aligned in every replica).  MT > 0: M == MT known at compile time, all M
+// loads issued before the first add.  MT == 0: any M >= 8, in groups of 8.
+template <int MT>
+__device__ __forceinline__ void sum8(const GradPtrs &g, int M, int64_t j, float s[kVec])
+{
+    if constexpr (MT > 0) {
+        uint4 q[MT];
+#pragma unroll
+        for (int r = 0; r < MT; ++r) q[r] = ld_stream_u4(g.p[r] + j);
+        unpack8(q[0], s);
+#pragma unroll
+        for (int r = 1; r < MT; ++r) add8(q[r], s);
+    } else {
+        uint4 q[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) q[r] = ld_stream_u4(g.p[r] + j);
+        unpack8(q[0], s);
+#pragma unroll
+        for (int r = 1; r < 8; ++r) add8(q[r], s);
+        for (int r0 = 8; r0 < M; r0 += 8) {
+            const int cnt = M - r0 < 8 ? M - r0 : 8;
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                if (k < cnt) q[k] = ld_stream_u4(g.p[r0 + k] + j);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                if (k < cnt) add8(q[k], s);
+        }
+    }
+}
+
+__device__ __forceinline__ float sum1(const GradPtrs &g, int M, int64_t j)
+{
+    float s = bf_one(ld_stream_u16(g.p[0] + j));
+    for (int r = 1; r < M; ++r) s = __fadd_rn(s, bf_one(ld_stream_u16(g.p[r] + j)));
+    return s;
+}
+
+// One AdamW update in fp32, one rounding per operation
+// ("五维并行实战" 4.2 names the optimizer and its hyperparameters):
+//   m' = beta1*m + (1-beta1)*g ; v' = beta2*v + (1-beta2)*(g*g)
+//   u = (m'/bc1) / (sqrt(v'/bc2) + eps) ; w' = w*(1-lr*wd) - lr*u
+__device__ __forceinline__ void adamw1(float g, const Z1Consts &c, float &w, float &m, float &v)
+{
+    const float m1 = __fadd_rn(__fmul_rn(c.beta1, m), __fmul_rn(c.omb1, g));
+    const float v1 = __fadd_rn(__fmul_rn(c.beta2, v), __fmul_rn(c.omb2, __fmul_rn(g, g)));
+    const float mh = __fdiv_rn(m1, c.bc1);
+    const float vh = __fdiv_rn(v1, c.bc2);
+    const float u = __fdiv_rn(mh, __fadd_rn(__fsqrt_rn(vh), c.eps));
+    w = __fsub_rn(__fmul_rn(w, c.cdec), __fmul_rn(c.lr, u));
+    m = m1;
+    v = v1;
+}
+
+__device__ __forceinline__ bool finite(float x) { return isfinite(x); }
+
+// Set *flag |= 1 if any thread of the warp saw a non-finite sum: one vote and
+// at most one atomic per warp.  Called by all threads of every warp.
+__device__ __forceinline__ void warp_flag(uint32_t *flag, bool bad)
+{
+    const unsigned any = __ballot_sync(0xffffffffu, bad);
+    if (any && (threadIdx.x & 31) == 0) atomicOr(flag, 1u);
+}
+
+__device__ __forceinline__ int64_t scalar_index(const Walk &w, int64_t q)
+{
+    return q < w.head ? q : q + w.nvec * kVec;
+}
+
+// Two-deep software pipeline over the vector body [0, nvec) with a grid
+// stride: the loads of vector i + nthr are issued before vector i is
+// computed, so each thread keeps two vectors of loads in flight.  (Measured
+// on the fused step: this beat higher occupancy with one vector in flight.)
+template <class Loads, class LoadF, class ComputeF>
+__device__ __forceinline__ void pipelined(int64_t nvec, int64_t tid, int64_t nthr, LoadF &&load, ComputeF &&compute)
+{
+    Loads cur, nxt;
+    int64_t i = tid;
+    if (i < nvec) load(cur, i);
+    for (; i < nvec; i += nthr) {
+        const bool more = i + nthr < nvec;
+        if (more) load(nxt, i + nthr);
+        compute(cur, i);
+        if (more) cur = nxt;
+    }
+}
+
+template <int MT>
+struct GradLoads {
+    uint4 q[MT > 0 ? MT : 1];
+};
+
+// Resident blocks per SM requested from the compiler: one for the pipelined
+// M <= 8 paths (room for two vectors of loads per thread), three for the
+// grouped M > 8 paths.
+#define Z1_BOUNDS(MT) __launch_bounds__(kBlock, (MT) > 0 ? 1 : 3)
+
+// fp32 state loads that do not allocate in L1 (each line is read once) and
+// streaming stores (.cs: the written lines are not read again by this kernel).
+__device__ __forceinline__ float4 ld_state(const float *p)
+{
+    float4 r;
+    asm("ld.global.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
+        : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+        : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ void st_stream(float *p, float a, float b, float c, float d)
+{
+    __stcs(reinterpret_cast<float4 *>(p), make_float4(a, b, c, d));
+}
+
+// AdamW on one 8-element vector whose replica sums are in s, then the
+// streaming stores of master/m/v and the bf16 parameters.
+__device__ __forceinline__ void store_vec(const float s[kVec], float4 w0, float4 w1, float4 m0, float4 m1,
+                                          float4 v0, float4 v1, float *pw, float *pm, float *pv, uint16_t *pp,
+                                          const Z1Consts &c, bool &bad)
+{
+    float ww[kVec] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+    float mm[kVec] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+    float vv[kVec] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+    for (int k = 0; k < kVec; ++k) {
+        bad |= !finite(s[k]);
+        adamw1(__fmul_rn(s[k], c.inv), c, ww[k], mm[k], vv[k]);
+    }
+    st_stream(pw, ww[0], ww[1], ww[2], ww[3]);
+    st_stream(pw + 4, ww[4], ww[5], ww[6], ww[7]);
+    st_stream(pm, mm[0], mm[1], mm[2], mm[3]);
+    st_stream(pm + 4, mm[4], mm[5], mm[6], mm[7]);
+    st_stream(pv, vv[0], vv[1], vv[2], vv[3]);
+    st_stream(pv + 4, vv[4], vv[5], vv[6], vv[7]);
+    __stcs(reinterpret_cast<uint4 *>(pp),
+           make_uint4(pack_bf16x2(ww[0], ww[1]), pack_bf16x2(ww[2], ww[3]), pack_bf16x2(ww[4], ww[5]),
+                      pack_bf16x2(ww[6], ww[7])));
+}
+
+// Per-element remainder of the fused step: [0, head) and the tail after the
+// vector body (real elements below nv, padding above).
+__device__ __forceinline__ void fused_scalar_rest(const GradPtrs &g, int M, float *master, float *mom,
+                                                  float *var, uint16_t *params, const Walk &w,
+                                                  const Z1Consts &c, int64_t tid, int64_t nthr, bool &bad)
+{
+    const int64_t ns = w.L - w.nvec * kVec;
+    for (int64_t q = tid; q < ns; q += nthr) {
+        const int64_t j = scalar_index(w, q);
+        float s = 0.0f;
+        if (j < w.nv) {
+            s = sum1(g, M, j);
+            bad |= !finite(s);
+        }
+        float ww = master[j], mm = mom[j], vv = var[j];
+        adamw1(__fmul_rn(s, c.inv), c, ww, mm, vv);
+        master[j] = ww;
+        mom[j] = mm;
+        var[j] = vv;
+        if (j < w.nv) params[j] = to_bf16(ww);
+    }
+}
+
+// AdamW on fp32 state given the scaled fp32 gradient.
+struct StateLoads {
+    float4 g0, g1, w0, w1, m0, m1, v0, v1;
+};
+
+__device__ __forceinline__ void load_state_vec(StateLoads &x, const float *gin, const float *master,
+                                               const float *mom, const float *var, int64_t j)
+{
+    x.g0 = __ldcs(reinterpret_cast<const float4 *>(gin + j));
+    x.g1 = __ldcs(reinterpret_cast<const float4 *>(gin + j + 4));
+    x.w0 = ld_state(master + j);
+    x.w1 = ld_state(master + j + 4);
+    x.m0 = ld_state(mom + j);
+    x.m1 = ld_state(mom + j + 4);
+    x.v0 = ld_state(var + j);
+    x.v1 = ld_state(var + j + 4);
+}
+
+// Reduce-scatter: out[j] = sum * scale (fp32 or bf16), +0 on padding.
+template <bool BF16>
+__device__ __forceinline__ void rs_store(void *out, int64_t j, float s[kVec], float scale)
+{
+#pragma unroll
+    for (int k = 0; k < kVec; ++k) s[k] = __fmul_rn(s[k], scale);
+    if constexpr (BF16) {
+        __stcs(reinterpret_cast<uint4 *>(static_cast<uint16_t *>(out) + j),
+               make_uint4(pack_bf16x2(s[0], s[1]), pack_bf16x2(s[2], s[3]), pack_bf16x2(s[4], s[5]),
+                          pack_bf16x2(s[6], s[7])));
+    } else {
+        st_stream(static_cast<float *>(out) + j, s[0], s[1], s[2], s[3]);
+        st_stream(static_cast<float *>(out) + j + 4, s[4], s[5], s[6], s[7]);
+    }
+}
+
+template <int MT, bool BF16>
+__global__ void Z1_BOUNDS(MT)
+k_reduce_scatter(const __grid_constant__ GradPtrs g, int M, const Walk w, float scale, void *out,
+                 uint32_t *flag)
+{
+    const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
+    const int64_t nthr = (int64_t)gridDim.x * kBlock;
+    bool bad = false;
+    if constexpr (MT > 0) {
+        pipelined<GradLoads<MT>>(
+            w.nvec, tid, nthr,
+            [&](GradLoads<MT> &x, int64_t i) {
+                const int64_t j = w.head + i * kVec;
+#pragma unroll
+                for (int r = 0; r < MT; ++r) x.q[r] = ld_stream_u4(g.p[r] + j);
+            },
+            [&](const GradLoads<MT> &x, int64_t i) {
+                float s[kVec];
+                unpack8(x.q[0], s);
+#pragma unroll
+                for (int r = 1; r < MT; ++r) add8(x.q[r], s);
+#pragma unroll
+                for (int k = 0; k < kVec; ++k) bad |= !finite(s[k]);
+                rs_store<BF16>(out, w.head + i * kVec, s, scale);
+            });
+    } else {
+        for (int64_t i = tid; i < w.nvec; i += nthr) {
+            const int64_t j = w.head + i * kVec;
+            float s[kVec];
+            sum8<0>(g, M, j, s);
+#pragma unroll
+            for (int k = 0; k < kVec; ++k) bad |= !finite(s[k]);
+            rs_store<BF16>(out, j, s, scale);
+        }
+    }
+    const int64_t ns = w.L - w.nvec * kVec;
+    for (int64_t q = tid; q < ns; q += nthr) {
+        const int64_t j = scalar_index(w, q);
+        float s = 0.0f;
+        if (j < w.nv) {
+            s = sum1(g, M, j);
+            bad |= !finite(s);
+        }
+        s = __fmul_rn(s, scale);
+        if constexpr (BF16) static_cast<uint16_t *>(out)[j] = to_bf16(s);
+        else static_cast<float *>(out)[j] = s;
+    }
+    if (flag) warp_flag(flag, bad);
+}
+
+// ------------------------------------------------------------ host side ----
+
+struct ArrayRef {
+    const void *p;
+    int esize;
+};
+
+// Choose the per-element head h in [0, 8) at which every array is 16-byte
+// aligned; if there is none, the whole range runs per element.
+Walk make_walk(int64_t L, int64_t nv, const ArrayRef *a, int count)
+{
+    Walk w{L, nv, 0, 0};
+    for (int h = 0; h < kVec; ++h) {
+        bool ok = true;
+        for (int k = 0; k < count && ok; ++k)
+            ok = (((uintptr_t)a[k].p + (uintptr_t)h * a[k].esize) & 15u) == 0;
+        if (ok) {
+            w.head = h < nv ? h : nv;
+            w.nvec = nv > h ? (nv - h) / kVec : 0;
+            return w;
+        }
+    }
+    return w;
+}
+
+int check_natural(const void *p, int esize, const char *what)
+{
+    if (((uintptr_t)p & (uintptr_t)(esize - 1)) != 0)
+        return z1_fail(ZERO1_EALIGN, "%s is not %d-byte aligned", what, esize);
+    return ZERO1_OK;
+}
+
+int sm_count()
+{
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev < 64) {
+        int c = cache[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev < 64) cache[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+// One resident wave: SMs x resident blocks of this kernel (cached per kernel
+// and device), capped by the work.
+template <class K>
+int grid_for(K kernel, int64_t work_items)
+{
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int per_sm = dev < 64 ? cache[dev].load(std::memory_order_relaxed) : 0;
+    if (per_sm <= 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kBlock, 0) != cudaSuccess ||
+            per_sm <= 0)
+            per_sm = 1;
+        if (dev < 64) cache[dev].store(per_sm, std::memory_order_relaxed);
+    }
+    const int64_t wave = (int64_t)sm_count() * per_sm;
+    int64_t need = (work_items + kBlock - 1) / kBlock;
+    if (need < 1) need = 1;
+    return (int)(need < wave ? need : (wave > 0 ? wave : 1));
+}
+
+// True if p is host memory the device reaches over the host link (pinned,
+// or plain pageable memory on a system where the GPU can address it).
+bool in_host_memory(const void *p)
+{
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();  // clear the sticky-free error of an unknown pointer
+        return false;
+    }
+    return a.type == cudaMemoryTypeHost || a.type == cudaMemoryTypeUnregistered;
+}
+
+int launch_status(const char *what)
+{
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return z1_fail(ZERO1_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+    return ZERO1_OK;
+}
+
+int64_t work_of(const Walk &w)
+{
+    const int64_t ns = w.L - w.nvec * kVec;
+    return w.nvec > ns ? w.nvec : ns;
+}
+
+int load_grads(const zero1_plan_t *plan, const void *const *grads, GradPtrs *g, const char *what)
+{
+    if (!grads) return z1_fail(ZERO1_EINVAL, "%s: grads array is NULL", what);
+    for (int r = 0; r < plan->M; ++r) {
+        if (!grads[r]) return z1_fail(ZERO1_EINVAL, "%s: grads[%d] is NULL", what, r);
+        int rc = check_natural(grads[r], 2, "a gradient pointer");
+        if (rc != ZERO1_OK) return rc;
+        g->p[r] = static_cast<const uint16_t *>(grads[r]);
+    }
+    return ZERO1_OK;
+}
+
+// Call f with std::integral_constant<int, MT>: MT = M for 1..8 (all loads of
+// an 8-element vector issued at once), MT = 0 for M > 8 (groups of 8).
+template <class F>
+void dispatch_m(int M, F &&f)
+{
+    switch (M) {
+    case 1: f(std::integral_constant<int, 1>{}); break;
+    case 2: f(std::integral_constant<int, 2>{}); break;
+    case 3: f(std::integral_constant<int, 3>{}); break;
+    case 4: f(std::integral_constant<int, 4>{}); break;
+    case 5: f(std::integral_constant<int, 5>{}); break;
+    case 6: f(std::integral_constant<int, 6>{}); break;
+    case 7: f(std::integral_constant<int, 7>{}); break;
+    case 8: f(std::integral_constant<int, 8>{}); break;
+    default: f(std::integral_constant<int, 0>{}); break;
+    }
+}
+
+}  // namespace

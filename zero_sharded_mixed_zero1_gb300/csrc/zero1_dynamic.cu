@@ -1,0 +1,273 @@
+// zero1_dynamic.cu - dynamic loss scaling with the step's skip decided on the
+// device ("五维并行实战" 4.2: the fp16 block's loss_scale 0, initial_scale_power,
+// loss_scale_window, hysteresis, min_loss_scale; 3.2 trap 3), and the same
+// step for callers that cannot allocate device memory.
+
+#include "zero1_device.cuh"
+
+namespace {
+
+// ------------------------------------------------ dynamic loss scaling ------
+//
+// "五维并行实战" 4.2 (fp16 block) names the policy's keys; the rule is stated in
+// zero1.h.  S, t and the derived constants live in a zero1_scaler_t in device
+// memory so the host never waits for the overflow flag.
+
+struct ScalePolicy {
+    float factor;
+    int32_t window, hysteresis;
+    float min_scale;
+};
+
+// b^t in double, square-and-multiply over the bits of t (least significant
+// first), the same operation sequence as the host's z1_pow_int.
+__device__ double pow_int_dev(double b, int64_t t)
+{
+    double r = 1.0, x = b;
+    for (; t > 0; t >>= 1) {
+        if (t & 1) r = __dmul_rn(r, x);
+        x = __dmul_rn(x, x);
+    }
+    return r;
+}
+
+// 1/(B*S), 1 - beta1^t, 1 - beta2^t: double arithmetic rounded once to
+// float, as the host evaluates them.
+__device__ void derive_constants(zero1_scaler_t *sc, int64_t B, float beta1, float beta2)
+{
+    sc->inv = __double2float_rn(__ddiv_rn(1.0, __dmul_rn((double)B, (double)sc->scale)));
+    sc->bc1 = __double2float_rn(__dsub_rn(1.0, pow_int_dev((double)beta1, sc->step)));
+    sc->bc2 = __double2float_rn(__dsub_rn(1.0, pow_int_dev((double)beta2, sc->step)));
+}
+
+__global__ void k_scaler_init(zero1_scaler_t *sc, float initial_scale, int32_t hysteresis, int64_t first_step,
+                              int64_t B, float beta1, float beta2)
+{
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    sc->scale = initial_scale;
+    sc->step = first_step;
+    sc->attempts = 0;
+    sc->skipped = 0;
+    sc->good_steps = 0;
+    sc->hysteresis_left = hysteresis;
+    sc->overflow = 0u;
+    sc->reserved = 0u;
+    derive_constants(sc, B, beta1, beta2);
+}
+
+// Advance the scaler after an attempt (reads the attempt's flag, clears it).
+__global__ void k_scaler_update(zero1_scaler_t *sc, const ScalePolicy pol, int64_t B, float beta1, float beta2)
+{
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    sc->attempts += 1;
+    if (*reinterpret_cast<volatile uint32_t *>(&sc->overflow) != 0u) {
+        sc->skipped += 1;
+        sc->good_steps = 0;
+        sc->hysteresis_left -= 1;
+        if (sc->hysteresis_left <= 0) {
+            const float down = __fdiv_rn(sc->scale, pol.factor);
+            sc->scale = down < pol.min_scale ? pol.min_scale : down;
+            sc->hysteresis_left = pol.hysteresis;
+        }
+    } else {
+        sc->step += 1;
+        sc->good_steps += 1;
+        if (sc->good_steps >= pol.window) {
+            const float up = __fmul_rn(sc->scale, pol.factor);
+            if (isfinite(up)) sc->scale = up;
+            sc->good_steps = 0;
+            sc->hysteresis_left = pol.hysteresis;
+        }
+    }
+    sc->overflow = 0u;
+    derive_constants(sc, B, beta1, beta2);
+}
+
+// AdamW + all-gather from fp32 replica sums (written by the reduce-scatter
+// kernel just before on the same stream), with 1/(B*S) and the bias
+// corrections read from the scaler; nothing is written if the attempt's flag
+// is set.  The arithmetic is the fused step's, operation for operation.
+__global__ void __launch_bounds__(kBlock, 1)
+k_apply_sums(const float *__restrict__ sums, float *__restrict__ master, float *__restrict__ mom,
+             float *__restrict__ var, uint16_t *__restrict__ params, const Walk w, Z1Consts c,
+             const zero1_scaler_t *sc)
+{
+    if (*reinterpret_cast<const volatile uint32_t *>(&sc->overflow) != 0u) return;
+    c.inv = sc->inv;
+    c.bc1 = sc->bc1;
+    c.bc2 = sc->bc2;
+    const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
+    const int64_t nthr = (int64_t)gridDim.x * kBlock;
+    bool bad = false;  // the flag was already taken by the reduce-scatter
+    pipelined<StateLoads>(
+        w.nvec, tid, nthr,
+        [&](StateLoads &x, int64_t i) { load_state_vec(x, sums, master, mom, var, w.head + i * kVec); },
+        [&](const StateLoads &x, int64_t i) {
+            const int64_t j = w.head + i * kVec;
+            const float s[kVec] = {x.g0.x, x.g0.y, x.g0.z, x.g0.w, x.g1.x, x.g1.y, x.g1.z, x.g1.w};
+            store_vec(s, x.w0, x.w1, x.m0, x.m1, x.v0, x.v1, master + j, mom + j, var + j, params + j, c, bad);
+        });
+    const int64_t ns = w.L - w.nvec * kVec;
+    for (int64_t q = tid; q < ns; q += nthr) {
+        const int64_t j = scalar_index(w, q);
+        float ww = master[j], mm = mom[j], vv = var[j];
+        adamw1(__fmul_rn(sums[j], c.inv), c, ww, mm, vv);
+        master[j] = ww;
+        mom[j] = mm;
+        var[j] = vv;
+        if (j < w.nv) params[j] = to_bf16(ww);
+    }
+}
+
+}  // namespace
+
+namespace {
+
+int check_policy(const zero1_loss_scale_policy_t *p)
+{
+    if (!p) return z1_fail(ZERO1_EINVAL, "loss-scale policy is NULL");
+    if (!(p->initial_scale > 0.0f) || !std::isfinite(p->initial_scale))
+        return z1_fail(ZERO1_EINVAL, "initial_scale must be finite and > 0");
+    if (!(p->factor > 1.0f) || !std::isfinite(p->factor)) return z1_fail(ZERO1_EINVAL, "factor must be finite and > 1");
+    if (p->window < 1) return z1_fail(ZERO1_EINVAL, "window must be >= 1");
+    if (p->hysteresis < 1) return z1_fail(ZERO1_EINVAL, "hysteresis must be >= 1");
+    if (!(p->min_scale > 0.0f) || !std::isfinite(p->min_scale))
+        return z1_fail(ZERO1_EINVAL, "min_scale must be finite and > 0");
+    return ZERO1_OK;
+}
+
+// Validate the hyperparameters a dynamic step uses (its own S and t come
+// from the scaler) and evaluate the host constants.
+int dynamic_constants(const zero1_adamw_t *hp, int32_t M, Z1Consts *c)
+{
+    if (!hp) return z1_fail(ZERO1_EINVAL, "hyperparameters are NULL");
+    zero1_adamw_t h = *hp;
+    h.loss_scale = 1.0f;
+    h.step = 1;
+    return z1_adamw_constants(&h, M, c);
+}
+
+int check_scaler_ptr(const zero1_scaler_t *sc)
+{
+    if (!sc) return z1_fail(ZERO1_EINVAL, "scaler is NULL");
+    if (((uintptr_t)sc & 7u) != 0) return z1_fail(ZERO1_EALIGN, "scaler is not 8-byte aligned");
+    return ZERO1_OK;
+}
+
+}  // namespace
+
+extern "C" int zero1_scaler_init(zero1_scaler_t *scaler, const zero1_loss_scale_policy_t *policy,
+                                 const zero1_adamw_t *hp, zero1_stream_t stream)
+{
+    int rc;
+    if ((rc = check_scaler_ptr(scaler)) != ZERO1_OK || (rc = check_policy(policy)) != ZERO1_OK) return rc;
+    if (!hp) return z1_fail(ZERO1_EINVAL, "hyperparameters are NULL");
+    if (!(hp->beta1 >= 0.0f && hp->beta1 < 1.0f) || !(hp->beta2 >= 0.0f && hp->beta2 < 1.0f))
+        return z1_fail(ZERO1_EINVAL, "betas must lie in [0, 1)");
+    if (hp->global_batch < 1) return z1_fail(ZERO1_EINVAL, "global batch must be >= 1");
+    if (hp->step < 1) return z1_fail(ZERO1_EINVAL, "step t = %lld < 1", (long long)hp->step);
+    k_scaler_init<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        scaler, policy->initial_scale, policy->hysteresis, hp->step, hp->global_batch, hp->beta1, hp->beta2);
+    return launch_status("scaler init launch");
+}
+
+extern "C" int zero1_step_dynamic(const zero1_plan_t *plan, int32_t shard_begin, int32_t shard_end,
+                                  const void *const *grads, float *master, float *m, float *v, void *params,
+                                  const zero1_adamw_t *hp, zero1_scaler_t *scaler,
+                                  const zero1_loss_scale_policy_t *policy, float *sums, zero1_stream_t stream)
+{
+    Z1Range r;
+    int rc = z1_range(plan, shard_begin, shard_end, &r);
+    if (rc != ZERO1_OK) return rc;
+    Z1Consts c;
+    if ((rc = dynamic_constants(hp, plan->M, &c)) != ZERO1_OK) return rc;
+    if ((rc = check_scaler_ptr(scaler)) != ZERO1_OK || (rc = check_policy(policy)) != ZERO1_OK) return rc;
+    if (!master || !m || !v || !sums)
+        return z1_fail(ZERO1_EINVAL, "dynamic step: master, m, v and sums must be non-NULL");
+    if (r.nv > 0 && !params)
+        return z1_fail(ZERO1_EINVAL, "dynamic step: params must be non-NULL when the range holds parameters");
+    GradPtrs g{};
+    if (r.nv > 0 && (rc = load_grads(plan, grads, &g, "dynamic step")) != ZERO1_OK) return rc;
+    if ((rc = check_natural(master, 4, "master")) || (rc = check_natural(m, 4, "m")) ||
+        (rc = check_natural(v, 4, "v")) || (rc = check_natural(params, 2, "params")) ||
+        (rc = check_natural(sums, 4, "sums")))
+        return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int M = plan->M;
+    // 1. reduce-scatter into the fp32 sums, flag into the scaler
+    ArrayRef ra[ZERO1_MAX_REPLICAS + 1] = {{sums, 4}};
+    for (int k = 0; k < M; ++k) ra[1 + k] = {g.p[k], 2};
+    const Walk wr = make_walk(r.L, r.nv, ra, 1 + M);
+    uint32_t *flag = &scaler->overflow;
+    dispatch_m(M, [&](auto mt) {
+        constexpr int MT = decltype(mt)::value;
+        const int grid = grid_for(k_reduce_scatter<MT, false>, work_of(wr));
+        k_reduce_scatter<MT, false><<<grid, kBlock, 0, st>>>(g, M, wr, 1.0f, sums, flag);
+    });
+    // 2. the update from the sums (skipped on overflow)
+    const ArrayRef ua[5] = {{sums, 4}, {master, 4}, {m, 4}, {v, 4}, {params, 2}};
+    const Walk wu = make_walk(r.L, r.nv, ua, 5);
+    const int grid = grid_for(k_apply_sums, work_of(wu));
+    k_apply_sums<<<grid, kBlock, 0, st>>>(sums, master, m, v, static_cast<uint16_t *>(params), wu, c, scaler);
+    // 3. the scaler advances
+    const ScalePolicy pol{policy->factor, policy->window, policy->hysteresis, policy->min_scale};
+    k_scaler_update<<<1, 32, 0, st>>>(scaler, pol, hp->global_batch, hp->beta1, hp->beta2);
+    return launch_status("dynamic step launch");
+}
+
+// ------------------------------------------- step without caller allocation --
+//
+// For callers that cannot call cudaMalloc (their pool allocator owns the
+// device memory, or allocation would synchronise the device): the sums
+// workspace of zero1_step_dynamic is this file-scope array, which exists on
+// every device that loads the library until the process exits.  Its name is a
+// host-side stand-in in host code; the device address comes from
+// cudaGetSymbolAddress, looked up once per device with that device current.
+static __device__ __align__(256) float g_noalloc_sums[ZERO1_NOALLOC_MAX_ELEMS];
+
+namespace {
+
+std::atomic<float *> g_noalloc_addr[64];
+
+// Device address of g_noalloc_sums on the current device (looked up on the
+// first call on each device).
+int noalloc_sums(float **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return z1_fail(ZERO1_ECUDA, "no-alloc step: cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= 64) return z1_fail(ZERO1_ERANGE, "no-alloc step: device %d beyond 64 devices", dev);
+    float *p = g_noalloc_addr[dev].load(std::memory_order_acquire);
+    if (!p) {
+        void *addr = nullptr;
+        e = cudaGetSymbolAddress(&addr, g_noalloc_sums);
+        if (e != cudaSuccess || !addr)
+            return z1_fail(ZERO1_ECUDA, "no-alloc step: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+        p = static_cast<float *>(addr);
+        g_noalloc_addr[dev].store(p, std::memory_order_release);
+    }
+    *out = p;
+    return ZERO1_OK;
+}
+
+}  // namespace
+
+extern "C" int zero1_step_dynamic_noalloc(const zero1_plan_t *plan, int32_t shard_begin, int32_t shard_end,
+                                          const void *const *grads, float *master, float *m, float *v,
+                                          void *params, const zero1_adamw_t *hp, zero1_scaler_t *scaler,
+                                          const zero1_loss_scale_policy_t *policy, zero1_stream_t stream)
+{
+    Z1Range r;
+    int rc = z1_range(plan, shard_begin, shard_end, &r);
+    if (rc != ZERO1_OK) return rc;
+    if (r.L > (int64_t)ZERO1_NOALLOC_MAX_ELEMS)
+        return z1_fail(ZERO1_ERANGE,
+                       "no-alloc step: range of %lld elements exceeds the built-in workspace of %d elements "
+                       "(64 MiB); split the call by shards",
+                       (long long)r.L, ZERO1_NOALLOC_MAX_ELEMS);
+    float *sums = nullptr;
+    if ((rc = noalloc_sums(&sums)) != ZERO1_OK) return rc;
+    return zero1_step_dynamic(plan, shard_begin, shard_end, grads, master, m, v, params, hp, scaler, policy,
+                              sums, stream);
+}
+

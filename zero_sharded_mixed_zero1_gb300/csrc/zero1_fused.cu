@@ -1,0 +1,300 @@
+// zero1_fused.cu - the fused ZeRO-1 step: reduce-scatter of the M replicas'
+// gradients, AdamW on the shard and all-gather of the bf16 parameters in one
+// pass ("CS336 Lecture 7: Parallelism 1", ZeRO Stage 1; naive-DP equation for
+// the 1/B mean; 16 bytes/parameter table for the dtypes).
+//
+//   M x 2 B bf16 gradient reads  ->  fp32 rank-order sum  ->  x 1/(B*S)
+//   12 B fp32 master/m/v read    ->  AdamW in registers   ->  12 B written
+//                                ->  bf16 parameter, 2 B written once
+//
+// 2M + 26 bytes per parameter, bound by HBM bandwidth.  Four kernels, chosen
+// per call: two vectors of loads in flight per thread for M <= 8 (the
+// measured fastest on large ranges), one vector per thread at four blocks per
+// SM on small ranges, replicas in groups of 8 for M > 8, and four vectors of
+// state loads in flight when master/m/v live in host memory.  Arithmetic uses
+// the explicit round-to-nearest intrinsics (__fadd_rn, __fmul_rn, __fdiv_rn,
+// __fsqrt_rn): no contraction, IEEE division and square root, so the results
+// are reproducible bit for bit.
+
+#include "zero1_device.cuh"
+
+namespace {
+
+// One 8-element vector of the fused step for M = MT <= 8 whose loads are in q
+// and the six state registers.
+template <int MT>
+__device__ __forceinline__ void fused_vec(int64_t j, const uint4 *q, float4 w0, float4 w1, float4 m0, float4 m1,
+                                          float4 v0, float4 v1, float *master, float *mom, float *var,
+                                          uint16_t *params, const Z1Consts &c, bool &bad)
+{
+    float s[kVec];
+    unpack8(q[0], s);
+#pragma unroll
+    for (int r = 1; r < MT; ++r) add8(q[r], s);
+    store_vec(s, w0, w1, m0, m1, v0, v1, master + j, mom + j, var + j, params + j, c, bad);
+}
+
+// The loads of one 8-element vector for M <= 8: every replica's gradient
+// vector, then the fp32 state.
+template <int MT>
+struct VecLoads {
+    uint4 q[MT];
+    float4 w0, w1, m0, m1, v0, v1;
+    __device__ __forceinline__ void load(const GradPtrs &g, const float *master, const float *mom,
+                                         const float *var, int64_t j)
+    {
+#pragma unroll
+        for (int r = 0; r < MT; ++r) q[r] = ld_stream_u4(g.p[r] + j);
+        w0 = ld_state(master + j);
+        w1 = ld_state(master + j + 4);
+        m0 = ld_state(mom + j);
+        m1 = ld_state(mom + j + 4);
+        v0 = ld_state(var + j);
+        v1 = ld_state(var + j + 4);
+    }
+};
+
+// The fused reduce-scatter + AdamW + all-gather for M <= 8 (M = MT known at
+// compile time).
+//
+// Shape chosen by measurement on GB300 (CUDA events through this entry point
+// on the 124M-parameter M = 8 workload): each thread issues all loads of its
+// next vector before computing the current one, so two vectors - 2 x
+// (16M + 96) bytes - are in flight per thread; the register budget this needs
+// (launch bounds of one block per SM) beat higher occupancy with one vector
+// in flight.  fp32 state is read with L1::no_allocate and every store is .cs.
+template <int MT>
+__global__ void __launch_bounds__(kBlock, MT <= 2 ? 2 : 1)
+k_fused_step(const __grid_constant__ GradPtrs g, int M, float *__restrict__ master,
+             float *__restrict__ mom, float *__restrict__ var, uint16_t *__restrict__ params,
+             const Walk w, const Z1Consts c, uint32_t *flag, int skip)
+{
+    if (skip && *reinterpret_cast<volatile uint32_t *>(flag) != 0u) return;
+    const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
+    const int64_t nthr = (int64_t)gridDim.x * kBlock;
+    bool bad = false;
+    VecLoads<MT> cur, nxt;
+    int64_t i = tid;
+    if (i < w.nvec) cur.load(g, master, mom, var, w.head + i * kVec);
+    for (; i < w.nvec; i += nthr) {
+        const int64_t j = w.head + i * kVec;
+        const bool more = i + nthr < w.nvec;
+        if (more) nxt.load(g, master, mom, var, j + nthr * kVec);
+        fused_vec<MT>(j, cur.q, cur.w0, cur.w1, cur.m0, cur.m1, cur.v0, cur.v1, master, mom, var,
+                      params, c, bad);
+        if (more) cur = nxt;
+    }
+    fused_scalar_rest(g, M, master, mom, var, params, w, c, tid, nthr, bad);
+    if (flag && !skip) warp_flag(flag, bad);
+}
+
+// The fused step for M <= 8 on small ranges (at most kWideMaxVec vectors):
+// one vector per thread and iteration at up to four blocks per SM.  Few
+// vectors per thread means the two-deep pipeline has nothing to overlap, and
+// the chain of dependent iterations per thread, not bandwidth, sets the time;
+// four times the threads shortens that chain.
+constexpr int64_t kWideMaxVec = 1 << 18;  // 2M elements
+
+template <int MT>
+__global__ void __launch_bounds__(kBlock, 4)
+k_fused_step_wide(const __grid_constant__ GradPtrs g, int M, float *__restrict__ master,
+                  float *__restrict__ mom, float *__restrict__ var, uint16_t *__restrict__ params,
+                  const Walk w, const Z1Consts c, uint32_t *flag, int skip)
+{
+    if (skip && *reinterpret_cast<volatile uint32_t *>(flag) != 0u) return;
+    const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
+    const int64_t nthr = (int64_t)gridDim.x * kBlock;
+    bool bad = false;
+    for (int64_t i = tid; i < w.nvec; i += nthr) {
+        const int64_t j = w.head + i * kVec;
+        VecLoads<MT> x;
+        x.load(g, master, mom, var, j);
+        fused_vec<MT>(j, x.q, x.w0, x.w1, x.m0, x.m1, x.v0, x.v1, master, mom, var, params, c, bad);
+    }
+    fused_scalar_rest(g, M, master, mom, var, params, w, c, tid, nthr, bad);
+    if (flag && !skip) warp_flag(flag, bad);
+}
+
+// The fused step for M > 8: the state is read first with the default
+// policy, then the replicas in groups of 8 into the same registers; stores
+// are .cs.  Three resident blocks per SM (at most 85 registers).  Measured on
+// the 64-replica shard: this shape beat deeper pipelining, fewer resident
+// blocks and L1::no_allocate state loads.
+__global__ void __launch_bounds__(kBlock, 3)
+k_fused_step_grouped(const __grid_constant__ GradPtrs g, int M, float *__restrict__ master,
+                     float *__restrict__ mom, float *__restrict__ var, uint16_t *__restrict__ params,
+                     const Walk w, const Z1Consts c, uint32_t *flag, int skip)
+{
+    if (skip && *reinterpret_cast<volatile uint32_t *>(flag) != 0u) return;
+    const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
+    const int64_t nthr = (int64_t)gridDim.x * kBlock;
+    bool bad = false;
+    for (int64_t i = tid; i < w.nvec; i += nthr) {
+        const int64_t j = w.head + i * kVec;
+        const float4 *pw = reinterpret_cast<const float4 *>(master + j);
+        const float4 *pm = reinterpret_cast<const float4 *>(mom + j);
+        const float4 *pv = reinterpret_cast<const float4 *>(var + j);
+        const float4 w0 = pw[0], w1 = pw[1], m0 = pm[0], m1 = pm[1], v0 = pv[0], v1 = pv[1];
+        float s[kVec];
+        uint4 q[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) q[r] = ld_stream_u4(g.p[r] + j);
+        unpack8(q[0], s);
+#pragma unroll
+        for (int r = 1; r < 8; ++r) add8(q[r], s);
+        for (int r0 = 8; r0 < M; r0 += 8) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                if (r0 + k < M) q[k] = ld_stream_u4(g.p[r0 + k] + j);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                if (r0 + k < M) add8(q[k], s);
+        }
+        store_vec(s, w0, w1, m0, m1, v0, v1, master + j, mom + j, var + j, params + j, c, bad);
+    }
+    fused_scalar_rest(g, M, master, mom, var, params, w, c, tid, nthr, bad);
+    if (flag && !skip) warp_flag(flag, bad);
+}
+
+// The fused step when master/m/v live in host memory (optimizer-state
+// offload over NVLink-C2C).  The host link needs many bytes in flight: each
+// thread issues the state loads of kOffloadDepth vectors (grid-strided)
+// before computing any of them, and the gradients (in HBM) are loaded per
+// vector.  Measured on GB300: the link sustains about 340 GB/s of combined
+// reads and writes with four vectors in flight per thread and 285 GB/s with
+// one.
+constexpr int kOffloadDepth = 4;
+
+template <int MT>
+__global__ void __launch_bounds__(kBlock, 1)
+k_fused_step_offload(const __grid_constant__ GradPtrs g, int M, float *__restrict__ master,
+                     float *__restrict__ mom, float *__restrict__ var, uint16_t *__restrict__ params,
+                     const Walk w, const Z1Consts c, uint32_t *flag, int skip)
+{
+    if (skip && *reinterpret_cast<volatile uint32_t *>(flag) != 0u) return;
+    const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
+    const int64_t nthr = (int64_t)gridDim.x * kBlock;
+    bool bad = false;
+    for (int64_t i0 = tid; i0 < w.nvec; i0 += kOffloadDepth * nthr) {
+        float4 st[kOffloadDepth][6];
+#pragma unroll
+        for (int u = 0; u < kOffloadDepth; ++u) {
+            const int64_t i = i0 + u * nthr;
+            if (i < w.nvec) {
+                const int64_t j = w.head + i * kVec;
+                st[u][0] = ld_state(master + j);
+                st[u][1] = ld_state(master + j + 4);
+                st[u][2] = ld_state(mom + j);
+                st[u][3] = ld_state(mom + j + 4);
+                st[u][4] = ld_state(var + j);
+                st[u][5] = ld_state(var + j + 4);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kOffloadDepth; ++u) {
+            const int64_t i = i0 + u * nthr;
+            if (i < w.nvec) {
+                const int64_t j = w.head + i * kVec;
+                float s[kVec];
+                sum8<MT>(g, M, j, s);
+                store_vec(s, st[u][0], st[u][1], st[u][2], st[u][3], st[u][4], st[u][5], master + j, mom + j,
+                          var + j, params + j, c, bad);
+            }
+        }
+    }
+    fused_scalar_rest(g, M, master, mom, var, params, w, c, tid, nthr, bad);
+    if (flag && !skip) warp_flag(flag, bad);
+}
+
+}  // namespace
+
+// ------------------------------------------------------------ C ABI -------
+
+namespace {
+
+// Validate and launch the fused step over one range of L elements whose
+// first nv are real parameters (the pointers are at the range's start).
+int launch_fused_range(const zero1_plan_t *plan, int64_t L, int64_t nv, const void *const *grads, float *master,
+                       float *m, float *v, void *params, const zero1_adamw_t *hp, uint32_t *overflow_flag,
+                       int32_t skip_if_flag, zero1_stream_t stream, const char *what)
+{
+    Z1Consts c;
+    int rc;
+    if ((rc = z1_adamw_constants(hp, plan->M, &c)) != ZERO1_OK) return rc;
+    if (!master || !m || !v)
+        return z1_fail(ZERO1_EINVAL, "%s: master, m and v must be non-NULL", what);
+    if (nv > 0 && !params)
+        return z1_fail(ZERO1_EINVAL, "%s: params must be non-NULL when the range holds parameters", what);
+    if (skip_if_flag && !overflow_flag)
+        return z1_fail(ZERO1_EINVAL, "%s: skip_if_flag needs an overflow flag", what);
+    GradPtrs g{};
+    if (nv > 0 && (rc = load_grads(plan, grads, &g, what)) != ZERO1_OK) return rc;
+    if ((rc = check_natural(master, 4, "master")) || (rc = check_natural(m, 4, "m")) ||
+        (rc = check_natural(v, 4, "v")) || (rc = check_natural(params, 2, "params")) ||
+        (overflow_flag && (rc = check_natural(overflow_flag, 4, "overflow_flag"))))
+        return rc;
+    ArrayRef arr[ZERO1_MAX_REPLICAS + 4] = {{master, 4}, {m, 4}, {v, 4}, {params, 2}};
+    for (int k = 0; k < plan->M; ++k) arr[4 + k] = {g.p[k], 2};
+    const Walk w = make_walk(L, nv, arr, 4 + plan->M);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint16_t *pp = static_cast<uint16_t *>(params);
+    const int M = plan->M;
+    const int skip = skip_if_flag ? 1 : 0;
+    if (in_host_memory(master)) {
+        dispatch_m(M, [&](auto mt) {
+            constexpr int MT = decltype(mt)::value;
+            const int grid = grid_for(k_fused_step_offload<MT>, work_of(w));
+            k_fused_step_offload<MT><<<grid, kBlock, 0, st>>>(g, M, master, m, v, pp, w, c, overflow_flag, skip);
+        });
+    } else if (M > 8) {
+        const int grid = grid_for(k_fused_step_grouped, work_of(w));
+        k_fused_step_grouped<<<grid, kBlock, 0, st>>>(g, M, master, m, v, pp, w, c, overflow_flag, skip);
+    } else {
+        dispatch_m(M, [&](auto mt) {
+            constexpr int MT = decltype(mt)::value;
+            if constexpr (MT > 0) {
+                if (w.nvec <= kWideMaxVec) {
+                    const int grid = grid_for(k_fused_step_wide<MT>, work_of(w));
+                    k_fused_step_wide<MT><<<grid, kBlock, 0, st>>>(g, M, master, m, v, pp, w, c, overflow_flag,
+                                                                   skip);
+                } else {
+                    const int grid = grid_for(k_fused_step<MT>, work_of(w));
+                    k_fused_step<MT><<<grid, kBlock, 0, st>>>(g, M, master, m, v, pp, w, c, overflow_flag, skip);
+                }
+            }
+        });
+    }
+    return launch_status(what);
+}
+
+}  // namespace
+
+extern "C" int zero1_reduce_scatter_adamw_allgather(const zero1_plan_t *plan, int32_t shard_begin,
+                                                    int32_t shard_end, const void *const *grads,
+                                                    float *master, float *m, float *v, void *params,
+                                                    const zero1_adamw_t *hp, uint32_t *overflow_flag,
+                                                    int32_t skip_if_flag, zero1_stream_t stream)
+{
+    Z1Range r;
+    int rc = z1_range(plan, shard_begin, shard_end, &r);
+    if (rc != ZERO1_OK) return rc;
+    return launch_fused_range(plan, r.L, r.nv, grads, master, m, v, params, hp, overflow_flag, skip_if_flag,
+                              stream, "fused step");
+}
+
+extern "C" int zero1_step_bucket(const zero1_plan_t *plan, int64_t elem_begin, int64_t elem_end,
+                                 const void *const *grads, float *master, float *m, float *v, void *params,
+                                 const zero1_adamw_t *hp, uint32_t *overflow_flag, zero1_stream_t stream)
+{
+    int rc = z1_check_plan(plan);
+    if (rc != ZERO1_OK) return rc;
+    if (elem_begin < 0 || elem_end > plan->padded_n || elem_begin >= elem_end)
+        return z1_fail(ZERO1_EINVAL, "bucket [%lld, %lld) not inside [0, %lld)", (long long)elem_begin,
+                       (long long)elem_end, (long long)plan->padded_n);
+    const int64_t L = elem_end - elem_begin;
+    int64_t nv = plan->n - elem_begin;
+    nv = nv < 0 ? 0 : (nv > L ? L : nv);
+    return launch_fused_range(plan, L, nv, grads, master, m, v, params, hp, overflow_flag, 0, stream,
+                              "bucketed step");
+}
+

@@ -1,0 +1,352 @@
+// zero1_phases.cu - the step's phases as separate kernels, and the naive
+// data-parallel All-Reduce ("CS336 Lecture 7: Parallelism 1": the five
+// collectives and All-Reduce == Reduce-Scatter + All-Gather): the overflow
+// check, AdamW from a scaled fp32 gradient, the all-gather of the updated
+// shard, the all-gather of bf16 shards into M outputs and the All-Reduce.
+// (The reduce-scatter kernel itself is in zero1_device.cuh: the dynamic step
+// uses it too.)
+
+#include "zero1_device.cuh"
+
+namespace {
+
+// Overflow check: flag |= any non-finite rank-order sum over real elements.
+// A pure read stream: one vector in flight per thread at the compiler's
+// register budget (5 blocks per SM) measured faster here than the two-deep
+// pipeline (7196 vs 6952 GB/s at M = 8); the M > 8 grouped path keeps three
+// blocks per SM (7422 GB/s at M = 64).
+template <int MT>
+__global__ void __launch_bounds__(kBlock, (MT) > 0 ? 5 : 3)
+k_overflow(const __grid_constant__ GradPtrs g, int M, const Walk w, uint32_t *flag)
+{
+    const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
+    const int64_t nthr = (int64_t)gridDim.x * kBlock;
+    bool bad = false;
+    for (int64_t i = tid; i < w.nvec; i += nthr) {
+        float s[kVec];
+        sum8<MT>(g, M, w.head + i * kVec, s);
+#pragma unroll
+        for (int k = 0; k < kVec; ++k) bad |= !finite(s[k]);
+    }
+    const int64_t ns = w.L - w.nvec * kVec;
+    for (int64_t q = tid; q < ns; q += nthr) {
+        const int64_t j = scalar_index(w, q);
+        if (j < w.nv) bad |= !finite(sum1(g, M, j));
+    }
+    warp_flag(flag, bad);
+}
+
+__global__ void __launch_bounds__(kBlock, 1)
+k_adamw(const float *__restrict__ gin, float *__restrict__ master, float *__restrict__ mom,
+        float *__restrict__ var, const Walk w, const Z1Consts c)
+{
+    const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
+    const int64_t nthr = (int64_t)gridDim.x * kBlock;
+    pipelined<StateLoads>(
+        w.nvec, tid, nthr,
+        [&](StateLoads &x, int64_t i) { load_state_vec(x, gin, master, mom, var, w.head + i * kVec); },
+        [&](const StateLoads &x, int64_t i) {
+            const int64_t j = w.head + i * kVec;
+            float gg[kVec] = {x.g0.x, x.g0.y, x.g0.z, x.g0.w, x.g1.x, x.g1.y, x.g1.z, x.g1.w};
+            float ww[kVec] = {x.w0.x, x.w0.y, x.w0.z, x.w0.w, x.w1.x, x.w1.y, x.w1.z, x.w1.w};
+            float mm[kVec] = {x.m0.x, x.m0.y, x.m0.z, x.m0.w, x.m1.x, x.m1.y, x.m1.z, x.m1.w};
+            float vv[kVec] = {x.v0.x, x.v0.y, x.v0.z, x.v0.w, x.v1.x, x.v1.y, x.v1.z, x.v1.w};
+#pragma unroll
+            for (int k = 0; k < kVec; ++k) adamw1(gg[k], c, ww[k], mm[k], vv[k]);
+            st_stream(master + j, ww[0], ww[1], ww[2], ww[3]);
+            st_stream(master + j + 4, ww[4], ww[5], ww[6], ww[7]);
+            st_stream(mom + j, mm[0], mm[1], mm[2], mm[3]);
+            st_stream(mom + j + 4, mm[4], mm[5], mm[6], mm[7]);
+            st_stream(var + j, vv[0], vv[1], vv[2], vv[3]);
+            st_stream(var + j + 4, vv[4], vv[5], vv[6], vv[7]);
+        });
+    const int64_t ns = w.L - w.nvec * kVec;
+    for (int64_t q = tid; q < ns; q += nthr) {
+        const int64_t j = scalar_index(w, q);
+        float ww = master[j], mm = mom[j], vv = var[j];
+        adamw1(gin[j], c, ww, mm, vv);
+        master[j] = ww;
+        mom[j] = mm;
+        var[j] = vv;
+    }
+}
+
+// All-gather of the updated shard: params[j] = bf16(master[j]), real only.
+struct MasterLoads {
+    float4 a, b;
+};
+
+__global__ void __launch_bounds__(kBlock, 1)
+k_all_gather(const float *__restrict__ master, uint16_t *__restrict__ params, const Walk w)
+{
+    const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
+    const int64_t nthr = (int64_t)gridDim.x * kBlock;
+    pipelined<MasterLoads>(
+        w.nvec, tid, nthr,
+        [&](MasterLoads &x, int64_t i) {
+            const float4 *pw = reinterpret_cast<const float4 *>(master + w.head + i * kVec);
+            x.a = __ldcs(pw);
+            x.b = __ldcs(pw + 1);
+        },
+        [&](const MasterLoads &x, int64_t i) {
+            __stcs(reinterpret_cast<uint4 *>(params + w.head + i * kVec),
+                   make_uint4(pack_bf16x2(x.a.x, x.a.y), pack_bf16x2(x.a.z, x.a.w), pack_bf16x2(x.b.x, x.b.y),
+                              pack_bf16x2(x.b.z, x.b.w)));
+        });
+    const int64_t ns = w.L - w.nvec * kVec;
+    for (int64_t q = tid; q < ns; q += nthr) {
+        const int64_t j = scalar_index(w, q);
+        if (j < w.nv) params[j] = to_bf16(master[j]);
+    }
+}
+
+// All-gather of bf16 shards into M outputs (real elements only).
+__global__ void __launch_bounds__(kBlock)
+k_all_gather_shards(const uint16_t *__restrict__ shards, const __grid_constant__ OutPtrs o, int M,
+                    const Walk w)
+{
+    const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
+    const int64_t nthr = (int64_t)gridDim.x * kBlock;
+    for (int64_t i = tid; i < w.nvec; i += nthr) {
+        const int64_t j = w.head + i * kVec;
+        const uint4 q = ld_stream_u4(shards + j);
+        for (int r = 0; r < M; ++r) *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(o.p[r]) + j) = q;
+    }
+    const int64_t ns = w.L - w.nvec * kVec;
+    for (int64_t q = tid; q < ns; q += nthr) {
+        const int64_t j = scalar_index(w, q);
+        if (j < w.nv) {
+            const uint16_t x = shards[j];
+            for (int r = 0; r < M; ++r) static_cast<uint16_t *>(o.p[r])[j] = x;
+        }
+    }
+}
+
+// Naive All-Reduce: every output gets sum * scale.  Element j's inputs are
+// all read before any output of j is written (outputs may alias inputs).
+template <bool BF16>
+__device__ __forceinline__ void ar_store(const OutPtrs &o, int M, int64_t j, float s[kVec], float scale)
+{
+#pragma unroll
+    for (int k = 0; k < kVec; ++k) s[k] = __fmul_rn(s[k], scale);
+    if constexpr (BF16) {
+        const uint4 q = make_uint4(pack_bf16x2(s[0], s[1]), pack_bf16x2(s[2], s[3]), pack_bf16x2(s[4], s[5]),
+                                   pack_bf16x2(s[6], s[7]));
+        for (int r = 0; r < M; ++r) __stcs(reinterpret_cast<uint4 *>(static_cast<uint16_t *>(o.p[r]) + j), q);
+    } else {
+        for (int r = 0; r < M; ++r) {
+            st_stream(static_cast<float *>(o.p[r]) + j, s[0], s[1], s[2], s[3]);
+            st_stream(static_cast<float *>(o.p[r]) + j + 4, s[4], s[5], s[6], s[7]);
+        }
+    }
+}
+
+template <int MT, bool BF16>
+__global__ void Z1_BOUNDS(MT)
+k_allreduce(const __grid_constant__ GradPtrs g, const __grid_constant__ OutPtrs o, int M,
+            const Walk w, float scale)
+{
+    const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
+    const int64_t nthr = (int64_t)gridDim.x * kBlock;
+    if constexpr (MT > 0) {
+        // in place, the next vector's loads touch other elements than the
+        // current vector's stores, so prefetching them stays correct
+        pipelined<GradLoads<MT>>(
+            w.nvec, tid, nthr,
+            [&](GradLoads<MT> &x, int64_t i) {
+                const int64_t j = w.head + i * kVec;
+#pragma unroll
+                for (int r = 0; r < MT; ++r) x.q[r] = ld_stream_u4(g.p[r] + j);
+            },
+            [&](const GradLoads<MT> &x, int64_t i) {
+                float s[kVec];
+                unpack8(x.q[0], s);
+#pragma unroll
+                for (int r = 1; r < MT; ++r) add8(x.q[r], s);
+                ar_store<BF16>(o, MT, w.head + i * kVec, s, scale);
+            });
+    } else {
+        for (int64_t i = tid; i < w.nvec; i += nthr) {
+            const int64_t j = w.head + i * kVec;
+            float s[kVec];
+            sum8<0>(g, M, j, s);
+            ar_store<BF16>(o, M, j, s, scale);
+        }
+    }
+    const int64_t ns = w.L - w.nvec * kVec;
+    for (int64_t q = tid; q < ns; q += nthr) {
+        const int64_t j = scalar_index(w, q);
+        const float s = __fmul_rn(sum1(g, M, j), scale);
+        for (int r = 0; r < M; ++r) {
+            if constexpr (BF16) static_cast<uint16_t *>(o.p[r])[j] = to_bf16(s);
+            else static_cast<float *>(o.p[r])[j] = s;
+        }
+    }
+}
+
+}  // namespace
+
+extern "C" int zero1_overflow_check(const zero1_plan_t *plan, int32_t shard_begin, int32_t shard_end,
+                                    const void *const *grads, uint32_t *flag, zero1_stream_t stream)
+{
+    Z1Range r;
+    int rc = z1_range(plan, shard_begin, shard_end, &r);
+    if (rc != ZERO1_OK) return rc;
+    if (!flag) return z1_fail(ZERO1_EINVAL, "overflow check: flag is NULL");
+    if ((rc = check_natural(flag, 4, "flag")) != ZERO1_OK) return rc;
+    if (r.nv == 0) return ZERO1_OK;
+    GradPtrs g{};
+    if ((rc = load_grads(plan, grads, &g, "overflow check")) != ZERO1_OK) return rc;
+    ArrayRef arr[ZERO1_MAX_REPLICAS];
+    for (int k = 0; k < plan->M; ++k) arr[k] = {grads[k], 2};
+    const Walk w = make_walk(r.nv, r.nv, arr, plan->M);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int M = plan->M;
+    dispatch_m(M, [&](auto mt) {
+        constexpr int MT = decltype(mt)::value;
+        const int grid = grid_for(k_overflow<MT>, work_of(w));
+        k_overflow<MT><<<grid, kBlock, 0, st>>>(g, M, w, flag);
+    });
+    return launch_status("overflow check launch");
+}
+
+extern "C" int dp_allreduce(const zero1_plan_t *plan, const void *const *grads_in, void *const *outs,
+                            float scale, int32_t out_dtype, zero1_stream_t stream)
+{
+    int rc = z1_check_plan(plan);
+    if (rc != ZERO1_OK) return rc;
+    if (out_dtype != ZERO1_DTYPE_BF16 && out_dtype != ZERO1_DTYPE_F32)
+        return z1_fail(ZERO1_EINVAL, "all-reduce: unknown output dtype %d", out_dtype);
+    if (!std::isfinite(scale)) return z1_fail(ZERO1_EINVAL, "all-reduce: scale is not finite");
+    GradPtrs g{};
+    if ((rc = load_grads(plan, grads_in, &g, "all-reduce")) != ZERO1_OK) return rc;
+    if (!outs) return z1_fail(ZERO1_EINVAL, "all-reduce: outs is NULL");
+    const int M = plan->M;
+    const int osz = out_dtype == ZERO1_DTYPE_BF16 ? 2 : 4;
+    OutPtrs o{};
+    ArrayRef arr[2 * ZERO1_MAX_REPLICAS];
+    for (int k = 0; k < M; ++k) {
+        if (!outs[k]) return z1_fail(ZERO1_EINVAL, "all-reduce: outs[%d] is NULL", k);
+        if ((rc = check_natural(outs[k], osz, "an all-reduce output")) != ZERO1_OK) return rc;
+        if (osz == 4) {
+            const uintptr_t a = (uintptr_t)outs[k], b = a + (uintptr_t)plan->n * 4;
+            for (int q = 0; q < M; ++q) {
+                const uintptr_t c0 = (uintptr_t)grads_in[q], c1 = c0 + (uintptr_t)plan->n * 2;
+                if (a < c1 && c0 < b)
+                    return z1_fail(ZERO1_EINVAL, "all-reduce: fp32 output %d overlaps input %d", k, q);
+            }
+        }
+        o.p[k] = outs[k];
+        arr[k] = {grads_in[k], 2};
+        arr[M + k] = {outs[k], osz};
+    }
+    const Walk w = make_walk(plan->n, plan->n, arr, 2 * M);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    dispatch_m(M, [&](auto mt) {
+        constexpr int MT = decltype(mt)::value;
+        if (osz == 2) {
+            const int grid = grid_for(k_allreduce<MT, true>, work_of(w));
+            k_allreduce<MT, true><<<grid, kBlock, 0, st>>>(g, o, M, w, scale);
+        } else {
+            const int grid = grid_for(k_allreduce<MT, false>, work_of(w));
+            k_allreduce<MT, false><<<grid, kBlock, 0, st>>>(g, o, M, w, scale);
+        }
+    });
+    return launch_status("all-reduce launch");
+}
+
+extern "C" int zero1_reduce_scatter(const zero1_plan_t *plan, int32_t shard_begin, int32_t shard_end,
+                                    const void *const *grads, float scale, int32_t out_dtype, void *out,
+                                    uint32_t *flag, zero1_stream_t stream)
+{
+    Z1Range r;
+    int rc = z1_range(plan, shard_begin, shard_end, &r);
+    if (rc != ZERO1_OK) return rc;
+    if (out_dtype != ZERO1_DTYPE_BF16 && out_dtype != ZERO1_DTYPE_F32)
+        return z1_fail(ZERO1_EINVAL, "reduce-scatter: unknown output dtype %d", out_dtype);
+    if (!std::isfinite(scale)) return z1_fail(ZERO1_EINVAL, "reduce-scatter: scale is not finite");
+    if (!out) return z1_fail(ZERO1_EINVAL, "reduce-scatter: out is NULL");
+    const int osz = out_dtype == ZERO1_DTYPE_BF16 ? 2 : 4;
+    if ((rc = check_natural(out, osz, "reduce-scatter output")) != ZERO1_OK) return rc;
+    if (flag && (rc = check_natural(flag, 4, "flag")) != ZERO1_OK) return rc;
+    GradPtrs g{};
+    if (r.nv > 0 && (rc = load_grads(plan, grads, &g, "reduce-scatter")) != ZERO1_OK) return rc;
+    ArrayRef arr[ZERO1_MAX_REPLICAS + 1] = {{out, osz}};
+    for (int k = 0; k < plan->M; ++k) arr[1 + k] = {g.p[k], 2};
+    const Walk w = make_walk(r.L, r.nv, arr, 1 + plan->M);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int M = plan->M;
+    dispatch_m(M, [&](auto mt) {
+        constexpr int MT = decltype(mt)::value;
+        if (osz == 2) {
+            const int grid = grid_for(k_reduce_scatter<MT, true>, work_of(w));
+            k_reduce_scatter<MT, true><<<grid, kBlock, 0, st>>>(g, M, w, scale, out, flag);
+        } else {
+            const int grid = grid_for(k_reduce_scatter<MT, false>, work_of(w));
+            k_reduce_scatter<MT, false><<<grid, kBlock, 0, st>>>(g, M, w, scale, out, flag);
+        }
+    });
+    return launch_status("reduce-scatter launch");
+}
+
+extern "C" int zero1_adamw_update(const zero1_plan_t *plan, int32_t shard_begin, int32_t shard_end,
+                                  const float *gin, float *master, float *m, float *v,
+                                  const zero1_adamw_t *hp, zero1_stream_t stream)
+{
+    Z1Range r;
+    int rc = z1_range(plan, shard_begin, shard_end, &r);
+    if (rc != ZERO1_OK) return rc;
+    Z1Consts c;
+    if ((rc = z1_adamw_constants(hp, plan->M, &c)) != ZERO1_OK) return rc;
+    if (!gin || !master || !m || !v) return z1_fail(ZERO1_EINVAL, "adamw: NULL array");
+    if ((rc = check_natural(gin, 4, "g")) || (rc = check_natural(master, 4, "master")) ||
+        (rc = check_natural(m, 4, "m")) || (rc = check_natural(v, 4, "v")))
+        return rc;
+    const ArrayRef arr[4] = {{gin, 4}, {master, 4}, {m, 4}, {v, 4}};
+    // every element of the range is updated: walk it as if all were real
+    const Walk w = make_walk(r.L, r.L, arr, 4);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int grid = grid_for(k_adamw, work_of(w));
+    k_adamw<<<grid, kBlock, 0, st>>>(gin, master, m, v, w, c);
+    return launch_status("adamw launch");
+}
+
+extern "C" int zero1_all_gather(const zero1_plan_t *plan, int32_t shard_begin, int32_t shard_end,
+                                const float *master, void *params, zero1_stream_t stream)
+{
+    Z1Range r;
+    int rc = z1_range(plan, shard_begin, shard_end, &r);
+    if (rc != ZERO1_OK) return rc;
+    if (r.nv == 0) return ZERO1_OK;
+    if (!master || !params) return z1_fail(ZERO1_EINVAL, "all-gather: NULL array");
+    if ((rc = check_natural(master, 4, "master")) || (rc = check_natural(params, 2, "params"))) return rc;
+    const ArrayRef arr[2] = {{master, 4}, {params, 2}};
+    const Walk w = make_walk(r.nv, r.nv, arr, 2);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int grid = grid_for(k_all_gather, work_of(w));
+    k_all_gather<<<grid, kBlock, 0, st>>>(master, static_cast<uint16_t *>(params), w);
+    return launch_status("all-gather launch");
+}
+
+extern "C" int zero1_all_gather_shards(const zero1_plan_t *plan, const void *shards, void *const *outs,
+                                       zero1_stream_t stream)
+{
+    int rc = z1_check_plan(plan);
+    if (rc != ZERO1_OK) return rc;
+    if (!shards || !outs) return z1_fail(ZERO1_EINVAL, "all-gather shards: NULL argument");
+    if ((rc = check_natural(shards, 2, "shards")) != ZERO1_OK) return rc;
+    OutPtrs o{};
+    ArrayRef arr[ZERO1_MAX_REPLICAS + 1] = {{shards, 2}};
+    for (int k = 0; k < plan->M; ++k) {
+        if (!outs[k]) return z1_fail(ZERO1_EINVAL, "all-gather shards: outs[%d] is NULL", k);
+        if ((rc = check_natural(outs[k], 2, "an all-gather output")) != ZERO1_OK) return rc;
+        o.p[k] = outs[k];
+        arr[1 + k] = {outs[k], 2};
+    }
+    const Walk w = make_walk(plan->n, plan->n, arr, 1 + plan->M);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int grid = grid_for(k_all_gather_shards, work_of(w));
+    k_all_gather_shards<<<grid, kBlock, 0, st>>>(static_cast<const uint16_t *>(shards), o, plan->M, w);
+    return launch_status("all-gather shards launch");
+}
+

@@ -19,6 +19,14 @@ __device__ __forceinline__ void warp_sum_u64(uint64_t &x)
     for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
 }
 
+// Units j and j + 1 packed in one 32-bit word (j in the low half).
+__device__ __forceinline__ void add_pair(uint32_t word, int64_t j, uint64_t &s1, uint64_t &s2)
+{
+    const uint64_t lo = word & 0xffffu, hi = word >> 16;
+    s1 += lo + hi;
+    s2 += (uint64_t)(j + 1) * lo + (uint64_t)(j + 2) * hi;
+}
+
 __global__ void __launch_bounds__(kBlock)
 k_checksum16(const uint16_t *__restrict__ u, const Walk w, unsigned long long *out)
 {
@@ -28,13 +36,10 @@ k_checksum16(const uint16_t *__restrict__ u, const Walk w, unsigned long long *o
     for (int64_t i = tid; i < w.nvec; i += nthr) {
         const int64_t j = w.head + i * kVec;
         const uint4 q = ld_stream_u4(u + j);
-        const uint32_t words[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const uint64_t lo = words[k] & 0xffffu, hi = words[k] >> 16;
-            s1 += lo + hi;
-            s2 += (uint64_t)(j + 2 * k + 1) * lo + (uint64_t)(j + 2 * k + 2) * hi;
-        }
+        add_pair(q.x, j, s1, s2);
+        add_pair(q.y, j + 2, s1, s2);
+        add_pair(q.z, j + 4, s1, s2);
+        add_pair(q.w, j + 6, s1, s2);
     }
     const int64_t ns = w.L - w.nvec * kVec;
     for (int64_t q = tid; q < ns; q += nthr) {

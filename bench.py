@@ -233,12 +233,63 @@ def run_reference(args, w) -> None:
 
 # --------------------------------------------------------- our arm ---------
 
-def config_of(w, state_on_host: bool = False, op: str = "step") -> dict:
+def host_link_rates(dev, nbytes: int = 1 << 30, reps: int = 4) -> dict:
+    """Copy-engine bandwidth of the host link in GB/s, measured with CUDA
+    events: pinned host -> HBM on two streams, HBM -> pinned host, and both
+    directions at once (the sum of the two)."""
+    host_in = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    host_out = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    dev_a = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    dev_b = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    host_in.fill_(1)
+    main = torch.cuda.current_stream(dev)
+    side = [torch.cuda.Stream(device=dev) for _ in range(2)]
+    half = nbytes // 2
+
+    def timed(jobs):
+        """jobs: one list of (dst, src) copies per side stream; returns seconds."""
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for _ in range(2):                       # the first round warms up
+            start.record(main)
+            for st, copies in zip(side, jobs):
+                st.wait_stream(main)
+                with torch.cuda.stream(st):
+                    for _ in range(reps):
+                        for dst, src in copies:
+                            dst.copy_(src, non_blocking=True)
+            for st in side[:len(jobs)]:
+                main.wait_stream(st)
+            end.record(main)
+            torch.cuda.synchronize(dev)
+        return start.elapsed_time(end) * 1e-3
+
+    h2d = nbytes * reps / timed([[(dev_a[:half], host_in[:half])], [(dev_a[half:], host_in[half:])]]) / 1e9
+    d2h = nbytes * reps / timed([[(host_out, dev_b)]]) / 1e9
+    both = 2 * nbytes * reps / timed([[(dev_a, host_in)], [(host_out, dev_b)]]) / 1e9
+    return {"h2d_gbs": h2d, "d2h_gbs": d2h, "both_directions_gbs": both,
+            "method": f"cudaMemcpyAsync of {nbytes >> 20} MiB pinned buffers x {reps}, CUDA events"}
+
+
+def link_roofline(link: dict, h2d_bytes: int, d2h_bytes: int, seconds_per_step: float) -> dict:
+    """The host link's lower bound on an end-to-end step that moves h2d_bytes
+    in and d2h_bytes out: max(in / h2d rate, out / d2h rate, both / rate of
+    both directions at once), and the measured step against it."""
+    bound_s = max(h2d_bytes / (link["h2d_gbs"] * 1e9), d2h_bytes / (link["d2h_gbs"] * 1e9),
+                  (h2d_bytes + d2h_bytes) / (link["both_directions_gbs"] * 1e9))
+    return {"bound": "host_link", "link_bytes_per_step": h2d_bytes + d2h_bytes,
+            "achieved_gbs": (h2d_bytes + d2h_bytes) / seconds_per_step / 1e9,
+            "bound_ms": bound_s * 1e3, "ms_per_step": seconds_per_step * 1e3,
+            "frac": bound_s / seconds_per_step, **link}
+
+
+def config_of(w, state_on_host: bool = False, op: str = "step", transfer: str = "zero_copy") -> dict:
     c = {"workload": w.name, "n": w.n, "M": w.M, "align": w.align, "global_batch": w.B,
          "loss_scale": w.S, "shards": list(w.shards), "io": "bf16 grads and params, fp32 master/m/v",
          "l2": "inputs larger than L2 (no flush)", "parallelism": "replicas only"}
     if state_on_host:
         c["state"] = "fp32 master/m/v in pinned host memory (offload)"
+        c["offload_transfer"] = {"zero_copy": "the kernel reads and writes the host state over the link",
+                                 "copy_engines": "state chunks staged through HBM by the copy engines"}[transfer]
     if op == "dynamic":
         c["loss_scaling"] = "dynamic, device-resident (window 1000, hysteresis 2, factor 2)"
     elif op != "step":
@@ -371,13 +422,23 @@ def run_ours(args, w) -> None:
     else:
         # one prepared step per gradient set: buffers validated once, then each
         # call passes only the hyperparameters (a few microseconds of host time)
-        prepared = {id(gs): z.FusedStep(plan, sb, se, gs, master, m, v, params, flag, stream=stream)
-                    for gs in gsets}
+        launches_per_step, op_bytes = 1, algorithmic_bytes(nv, L - nv, w.M)
+        if args.state_on_host and args.offload_transfer == "copy_engines":
+            prepared = {id(gs): z.HostStreamedStep(plan, sb, se, gs, master, m, v, params,
+                                                   chunk_elems=args.chunk_elems, overflow_flag=flag, stream=stream)
+                        for gs in gsets}
+            launches_per_step = len(prepared[id(gsets[0])].pieces)
+            op_kernel = (f"k_fused_step per {args.chunk_elems}-element chunk, state chunks staged through HBM "
+                         "by the copy engines")
+        else:
+            prepared = {id(gs): z.FusedStep(plan, sb, se, gs, master, m, v, params, flag, stream=stream)
+                        for gs in gsets}
+            op_kernel = f"k_fused_step<M={w.M}>" if w.M <= 8 else "k_fused_step_grouped"
+            if args.state_on_host:
+                op_kernel = f"k_fused_step_offload<{w.M if w.M <= 8 else 0}>"
 
         def launch(gr, tt, st=None):
             prepared[id(gr)](hp(tt))
-        launches_per_step, op_bytes = 1, algorithmic_bytes(nv, L - nv, w.M)
-        op_kernel = f"k_fused_step<M={w.M}>" if w.M <= 8 else "k_fused_step_grouped"
 
     t = 1
     for _ in range(args.warmup):
@@ -452,15 +513,20 @@ def run_ours(args, w) -> None:
 
         copy_s = timed(copy_step)
         zero_s = timed(zero_copy_step)
+        del streamed
+        link = host_link_rates(dev)
+        bi, bo = w.M * nv * 2, nv * 2 + 4
         e2e = {"value": world * nv * e2e_steps / copy_s, "unit": "params/s",
-               "h2d_bytes_per_step": w.M * nv * 2, "d2h_bytes_per_step": nv * 2 + 4, "steps": e2e_steps,
+               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": e2e_steps,
                "transfer": "cudaMemcpyAsync of the gradients to HBM in 16M-element chunks on a copy stream, "
-                           "overlapping the step on the previous chunk; params and flag copied back"}
+                           "overlapping the step on the previous chunk; params and flag copied back",
+               "roofline": link_roofline(link, bi, bo, copy_s / e2e_steps)}
         e2e_zero = {"value": world * nv * e2e_steps / zero_s, "unit": "params/s",
-                    "h2d_bytes_per_step": w.M * nv * 2, "d2h_bytes_per_step": nv * 2 + 4,
+                    "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
                     "transfer": "the kernel reads the pinned gradients and writes the pinned params "
-                                "over the host link (no staging copy)"}
-        del streamed, host_g
+                                "over the host link (no staging copy)",
+                    "roofline": link_roofline(link, bi, bo, zero_s / e2e_steps)}
+        del host_g
 
     if rank != 0:
         return
@@ -480,7 +546,7 @@ def run_ours(args, w) -> None:
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
-        "config": config_of(w, args.state_on_host, op),
+        "config": config_of(w, args.state_on_host, op, args.offload_transfer),
         "hbm_gbs": bytes_launch * args.steps / (ms_total * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "peak_source": peaks["source"],
@@ -524,6 +590,11 @@ def main(argv=None) -> int:
                          "with the fp16 block's policy instead of the fused step")
     ap.add_argument("--state-on-host", action="store_true",
                     help="keep fp32 master/m/v in pinned host memory (optimizer-state offload)")
+    ap.add_argument("--offload-transfer", choices=["zero_copy", "copy_engines"], default="zero_copy",
+                    help="with --state-on-host: the kernel reads and writes the host state over the link "
+                         "(zero_copy), or chunks are staged through HBM by the copy engines (copy_engines)")
+    ap.add_argument("--chunk-elems", type=int, default=1 << 24,
+                    help="chunk size of the staged (copy-engine) paths")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

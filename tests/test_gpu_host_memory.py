@@ -80,30 +80,78 @@ def test_pageable_host_tensor_is_rejected(cuda_device):
 
 @pytest.mark.parametrize("M,n,align,chunk,shards", [(8, 100_003, 128, 4096, None), (4, 50_000, 1, 1000, (1, 3)),
                                                     (13, 9_999, 8, 777, None), (2, 20, 128, 8, (1, 2))])
-def test_host_streamed_step_equals_fused_step(cuda_device, M, n, align, chunk, shards):
-    """Gradients in pinned host memory, copied chunk by chunk on a copy stream
-    while the step runs on the previous chunk: the fused step's bits, and the
+@pytest.mark.parametrize("where", ["grads", "state", "grads_state", "params"])
+def test_host_streamed_step_equals_fused_step(cuda_device, M, n, align, chunk, shards, where):
+    """Buffers in pinned host memory, staged chunk by chunk through HBM by
+    copy streams while the step runs on another chunk (three slots: copy in,
+    step, copy back): the fused step's bits on device buffers, and the
     parameters copied back to host memory."""
     dev = cuda_device
     plan = z.zero1_plan(n, M, align)
     sb, se = shards or (0, M)
     base, L, nv = plan.shard_range(sb, se)
     a = [t[base:base + L].clone() for t in make_state(n, plan.padded_n, 90 + M, dev, nonzero_moments=True)]
-    b = [t.clone() for t in a]
+    b = [pinned(t) for t in a] if where in ("state", "grads_state") else [t.clone() for t in a]
     pa = torch.zeros(max(nv, 1), dtype=torch.bfloat16, device=dev)
     pb = torch.zeros(max(nv, 1), dtype=torch.bfloat16, device=dev)
-    host_g = [torch.zeros(max(nv, 1), dtype=torch.bfloat16).pin_memory() for _ in range(M)]
+    grads_on_host = where in ("grads", "grads_state")
+    gb = [torch.zeros(max(nv, 1), dtype=torch.bfloat16, device=dev) for _ in range(M)]
+    if grads_on_host:
+        gb = [pinned(g) for g in gb]
     host_p = torch.zeros(max(nv, 1), dtype=torch.bfloat16).pin_memory()
-    step = z.HostStreamedStep(plan, sb, se, host_g, *b, pb, chunk_elems=chunk, params_host=host_p)
-    for t in (1, 2, 3):
+    step = z.HostStreamedStep(plan, sb, se, gb, *b, pb, chunk_elems=chunk, params_host=host_p)
+    for t in (1, 2, 3, 4):
         grads = [g[base:base + nv] for g in make_grads(M, n, 1e-2, 91 + M, t, dev)]
-        for hg, g in zip(host_g, grads):
-            hg[:nv].copy_(g.cpu())
+        for x, g in zip(gb, grads):
+            x[:nv].copy_(g)
+        torch.cuda.synchronize()
         hp = z.AdamW(global_batch=max(M, 64), step=t)
         z.zero1_reduce_scatter_adamw_allgather(plan, sb, se, grads, *a, pa, hp)
         step(hp)
         torch.cuda.synchronize()
         for x, y, what in zip(a, b, ("master", "m", "v")):
-            assert_f32_bits(f32(y), f32(x), f"{what} t={t}")
-        assert_bf16_bits(u16(pb[:nv]), u16(pa[:nv]), f"params t={t}")
-        assert_bf16_bits(u16(host_p[:nv]), u16(pa[:nv]), f"params on host t={t}")
+            assert_f32_bits(f32(y), f32(x), f"{where}: {what} t={t}")
+        assert_bf16_bits(u16(pb[:nv]), u16(pa[:nv]), f"{where}: params t={t}")
+        assert_bf16_bits(u16(host_p[:nv]), u16(pa[:nv]), f"{where}: params on host t={t}")
+
+
+def test_host_streamed_step_is_ordered_on_its_stream(cuda_device):
+    """Work enqueued on the step's stream after a call sees the host state the
+    call copied back, and the next call sees work enqueued before it."""
+    dev = cuda_device
+    M, n = 4, 40_000
+    plan = z.zero1_plan(n, M, 8)
+    L = plan.padded_n
+    dev_state = make_state(n, L, 5, dev, nonzero_moments=True)
+    ref = [t.clone() for t in dev_state]
+    host_state = [pinned(t) for t in dev_state]
+    grads = make_grads(M, n, 1e-2, 6, 1, dev)
+    pa = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+    pb = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+    st = torch.cuda.Stream(device=dev)
+    step = z.HostStreamedStep(plan, 0, M, grads, *host_state, pb, chunk_elems=4096, stream=st)
+    snap = torch.empty(L, dtype=torch.float32, device=dev)
+    for t in (1, 2):
+        hp = z.AdamW(global_batch=64, step=t)
+        z.zero1_reduce_scatter_adamw_allgather(plan, 0, M, grads, *ref, pa, hp)
+        with torch.cuda.stream(st):
+            step(hp)
+            snap.copy_(host_state[0], non_blocking=True)     # ordered after the copies back
+        st.synchronize()
+        torch.cuda.synchronize()
+        assert_f32_bits(f32(snap), f32(ref[0]), f"master seen on the stream t={t}")
+
+
+def test_host_streamed_step_rejects_mixed_placement(cuda_device):
+    dev = cuda_device
+    M, n = 2, 1000
+    plan = z.zero1_plan(n, M, 1)
+    state = make_state(n, plan.padded_n, 1, dev)
+    params = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+    grads = [torch.zeros(n, dtype=torch.bfloat16, device=dev) for _ in range(M)]
+    with pytest.raises(ValueError):      # nothing in host memory
+        z.HostStreamedStep(plan, 0, M, grads, *state, params)
+    with pytest.raises(ValueError):      # master on the host, m and v on the device
+        z.HostStreamedStep(plan, 0, M, grads, pinned(state[0]), state[1], state[2], params)
+    with pytest.raises(ValueError):      # one replica's gradients on the host
+        z.HostStreamedStep(plan, 0, M, [grads[0], pinned(grads[1])], *state, params)

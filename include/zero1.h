@@ -16,7 +16,9 @@
  *    memory (optimizer-state offload).  Such accesses run at the host link's
  *    speed instead of HBM's.  Arrays of pointers (grads, outs) are HOST arrays
  *    of M such pointers.  The caller owns all memory; the library allocates
- *    nothing and keeps no state between calls.
+ *    nothing and keeps no state between calls, except a staged-step handle
+ *    (zero1_staged_create), which owns its staging memory, streams and
+ *    events until zero1_staged_destroy.
  *  - Sizes are in elements.  bf16 buffers hold IEEE binary32 values'
  *    upper 16 bits (bfloat16); fp32 buffers hold IEEE binary32.
  *  - Device pointers must be naturally aligned (2 bytes for bf16, 4 for fp32,
@@ -184,6 +186,64 @@ int zero1_reduce_scatter_adamw_allgather(const zero1_plan_t *plan, int32_t shard
 int zero1_step_bucket(const zero1_plan_t *plan, int64_t elem_begin, int64_t elem_end,
                       const void *const *grads, float *master, float *m, float *v, void *params,
                       const zero1_adamw_t *hp, uint32_t *overflow_flag, zero1_stream_t stream);
+
+/* Staged step: the fused step over buffers in pinned host memory, staged
+ * through device memory by the copy engines [Z1], [OPT] (offload_optimizer:
+ * the fp32 optimizer state kept in host memory; the update itself runs on
+ * the GPU).  The handle's range (shards [shard_begin, shard_end)) is cut into
+ * chunks of chunk_elems elements (rounded up to a multiple of 8).  For each
+ * chunk an inbound stream copies the staged inputs into one of three device
+ * slots, `stream` runs zero1_step_bucket on the slot, and an outbound stream
+ * copies the staged outputs back; with three slots the inbound copy of one
+ * chunk, the step on the next older one and the outbound copy of the one
+ * before overlap.  Results are bit for bit those of
+ * zero1_reduce_scatter_adamw_allgather on device buffers (the step is
+ * element-wise).
+ *
+ * `what` selects what is staged (at least one bit):
+ *  ZERO1_STAGE_GRADS:  grads[r] are pinned host memory, copied in;
+ *  ZERO1_STAGE_STATE:  master, m, v are pinned host memory, copied in and
+ *                      the updated values copied back;
+ *  ZERO1_STAGE_PARAMS: the updated bf16 parameters are also copied to
+ *                      params_host (pinned host memory).
+ * Buffers not staged must be device memory; params is always device memory
+ * (the kernels write it).  Layouts as zero1_reduce_scatter_adamw_allgather:
+ * grads[r] and params hold the range's nv real elements, master/m/v its L
+ * elements, params_host nv elements.
+ *
+ * zero1_staged_create allocates, on the current device, 3 x chunk x (2M
+ * bytes if gradients are staged + 12 bytes if state is) of device memory,
+ * two non-blocking streams and the events that order them.
+ * zero1_staged_step enqueues one step; when `stream` reaches the work
+ * enqueued after it, the step's copies back to host memory are complete.
+ * Successive calls on one handle may use different streams (each waits for
+ * the previous call); calls must not be made concurrently from several host
+ * threads, and the call cannot be captured in a CUDA graph (EINVAL while
+ * `stream` is capturing).  overflow_flag is ORed as in the fused step; a
+ * chunk cannot wait for later chunks' flags, so there is no skip: when steps
+ * must be skipped on overflow, check the gradients first
+ * (zero1_overflow_check) and do not call the step.
+ * zero1_staged_destroy waits for the handle's queued work, then frees it
+ * (NULL is accepted).
+ * EINVAL: bad range, `what` or chunk size, a NULL or misplaced buffer (host
+ * where device memory is required or the reverse), the wrong current device,
+ * a capturing stream.  All arguments are checked before anything is
+ * enqueued; on ZERO1_ECUDA part of the step may have been enqueued. */
+#define ZERO1_STAGE_GRADS 1
+#define ZERO1_STAGE_STATE 2
+#define ZERO1_STAGE_PARAMS 4
+typedef struct zero1_staged zero1_staged_t;
+int zero1_staged_create(const zero1_plan_t *plan, int32_t shard_begin, int32_t shard_end, int32_t what,
+                        int64_t chunk_elems, zero1_staged_t **out);
+int zero1_staged_step(zero1_staged_t *handle, const void *const *grads, float *master, float *m, float *v,
+                      void *params, void *params_host, const zero1_adamw_t *hp, uint32_t *overflow_flag,
+                      zero1_stream_t stream);
+int zero1_staged_destroy(zero1_staged_t *handle);
+/* The handle's chunk boundaries: *count = chunks + 1 values 0 = cuts[0] <
+ * ... < cuts[chunks] = L, written to cuts (if not NULL; ERANGE if cap is
+ * smaller): chunks of chunk_elems (rounded up to a multiple of 8) elements,
+ * the last one shorter. */
+int zero1_staged_chunks(const zero1_staged_t *handle, int64_t *cuts, int32_t cap, int32_t *count);
 
 /* The fused step with its vector body staged through shared memory by the
  * Tensor Memory Accelerator [Z1], [DP], [MEM]: a producer warp issues 1-D bulk

@@ -150,6 +150,24 @@ def test_other_entry_points_reject_bad_arguments(lib):
     assert lib.zero1_strerror(-2) == b"misaligned device pointer"
 
 
+def test_staged_handle_rejects_bad_arguments(lib):
+    """The staged-step handle validates the plan, range, stage bits and chunk
+    size before any CUDA call; a NULL handle is rejected and destroying NULL
+    is a no-op."""
+    plan = z.zero1_plan(1000, 4, 8)
+    P = ctypes.byref(plan)
+    h = ctypes.c_void_p()
+    assert lib.zero1_staged_create(P, 0, 4, 0, 1024, ctypes.byref(h)) == -1        # nothing staged
+    assert lib.zero1_staged_create(P, 0, 4, 8, 1024, ctypes.byref(h)) == -1        # unknown bit
+    assert lib.zero1_staged_create(P, 0, 4, z.ZERO1_STAGE_STATE, 0, ctypes.byref(h)) == -1
+    assert lib.zero1_staged_create(P, 2, 2, z.ZERO1_STAGE_STATE, 64, ctypes.byref(h)) == -1   # empty range
+    assert lib.zero1_staged_create(P, 0, 5, z.ZERO1_STAGE_STATE, 64, ctypes.byref(h)) == -1
+    assert lib.zero1_staged_create(P, 0, 4, z.ZERO1_STAGE_STATE, 64, None) == -1
+    assert h.value is None
+    assert lib.zero1_staged_step(None, None, None, None, None, None, None, ctypes.byref(_hp()), None, None) == -1
+    assert lib.zero1_staged_destroy(None) == 0
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     import zero_sharded_mixed_zero1_gb300._lib as L
     monkeypatch.setattr(L, "_lib", None)

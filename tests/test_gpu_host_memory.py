@@ -79,7 +79,8 @@ def test_pageable_host_tensor_is_rejected(cuda_device):
 
 
 @pytest.mark.parametrize("M,n,align,chunk,shards", [(8, 100_003, 128, 4096, None), (4, 50_000, 1, 1000, (1, 3)),
-                                                    (13, 9_999, 8, 777, None), (2, 20, 128, 8, (1, 2))])
+                                                    (13, 9_999, 8, 777, None), (2, 20, 128, 8, (1, 2)),
+                                                    (13, 9_999, 8, 1024, None), (3, 70_001, 1, 8192, (0, 2))])
 @pytest.mark.parametrize("where", ["grads", "state", "grads_state", "params"])
 def test_host_streamed_step_equals_fused_step(cuda_device, M, n, align, chunk, shards, where):
     """Buffers in pinned host memory, staged chunk by chunk through HBM by
@@ -155,3 +156,58 @@ def test_host_streamed_step_rejects_mixed_placement(cuda_device):
         z.HostStreamedStep(plan, 0, M, grads, pinned(state[0]), state[1], state[2], params)
     with pytest.raises(ValueError):      # one replica's gradients on the host
         z.HostStreamedStep(plan, 0, M, [grads[0], pinned(grads[1])], *state, params)
+
+
+def test_staged_step_rejects_misplaced_buffers(cuda_device):
+    """Through the C ABI: a handle that stages the state refuses device-memory
+    state and a params_host it was not created for, and a capturing stream is
+    refused before anything is enqueued."""
+    import ctypes
+    dev = cuda_device
+    M, n = 2, 4096
+    plan = z.zero1_plan(n, M, 8)
+    lib = z.load()
+    h = ctypes.c_void_p()
+    assert lib.zero1_staged_create(ctypes.byref(plan), 0, M, z.ZERO1_STAGE_STATE, 1000, ctypes.byref(h)) == 0
+    try:
+        dev_state = make_state(n, plan.padded_n, 3, dev)
+        host_state = [pinned(t) for t in dev_state]
+        grads = make_grads(M, n, 1e-2, 4, 1, dev)
+        g = (ctypes.c_void_p * M)(*[x.data_ptr() for x in grads])
+        params = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+        hp = ctypes.byref(z.AdamW(global_batch=64).c_struct())
+        st = torch.cuda.current_stream().cuda_stream
+        rc = lib.zero1_staged_step(h, g, *[t.data_ptr() for t in dev_state], params.data_ptr(), None, hp, None, st)
+        assert rc == -1 and b"pinned host memory" in lib.zero1_last_error()
+        host_p = torch.zeros(n, dtype=torch.bfloat16).pin_memory()
+        rc = lib.zero1_staged_step(h, g, *[t.data_ptr() for t in host_state], params.data_ptr(), host_p.data_ptr(),
+                                   hp, None, st)
+        assert rc == -1 and b"ZERO1_STAGE_PARAMS" in lib.zero1_last_error()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            rc = lib.zero1_staged_step(h, g, *[t.data_ptr() for t in host_state], params.data_ptr(), None, hp,
+                                       None, torch.cuda.current_stream().cuda_stream)
+        assert rc == -1 and b"capturing" in lib.zero1_last_error()
+        rc = lib.zero1_staged_step(h, g, *[t.data_ptr() for t in host_state], params.data_ptr(), None, hp, None, st)
+        assert rc == 0
+        torch.cuda.synchronize()
+        assert torch.count_nonzero(params).item() > 0
+    finally:
+        assert lib.zero1_staged_destroy(h) == 0
+
+
+@pytest.mark.parametrize("L_n,M,chunk", [(100_003, 8, 4096), (9_999, 13, 1024), (1 << 20, 2, 1 << 16),
+                                         (5000, 1, 1000), (20, 2, 8), (3 * 1024 + 5, 1, 1021)])
+def test_staged_chunk_boundaries(cuda_device, L_n, M, chunk):
+    """The handle's chunks cover [0, L) in order with chunk_elems (rounded up
+    to a multiple of 8) elements each, the last one shorter."""
+    plan = z.zero1_plan(L_n, M, 8)
+    base, L, nv = plan.shard_range(0, M)
+    master, m, v = (pinned(t) for t in make_state(L_n, plan.padded_n, 1, cuda_device))
+    params = torch.zeros(L_n, dtype=torch.bfloat16, device=cuda_device)
+    grads = [torch.zeros(L_n, dtype=torch.bfloat16, device=cuda_device) for _ in range(M)]
+    step = z.HostStreamedStep(plan, 0, M, grads, master, m, v, params, chunk_elems=chunk)
+    cuts = [a for a, _ in step.pieces] + [step.pieces[-1][1]]
+    step.close()
+    c = (chunk + 7) // 8 * 8
+    assert cuts == list(range(0, L, c)) + [L]

@@ -9,6 +9,9 @@ include/zero1.h; this package is its thin Python binding.
 from ._lib import (  # noqa: F401
     ZERO1_DTYPE_BF16,
     ZERO1_DTYPE_F32,
+    ZERO1_STAGE_GRADS,
+    ZERO1_STAGE_PARAMS,
+    ZERO1_STAGE_STATE,
     ZERO1_MAX_REPLICAS,
     SCALER_BYTES,
     AdamW,

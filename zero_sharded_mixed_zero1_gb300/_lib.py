@@ -21,6 +21,7 @@ from . import build as _build
 ZERO1_OK, ZERO1_EINVAL, ZERO1_EALIGN, ZERO1_ERANGE, ZERO1_ECUDA = 0, -1, -2, -3, -4
 ZERO1_MAX_REPLICAS = 64
 ZERO1_DTYPE_BF16, ZERO1_DTYPE_F32 = 0, 1
+ZERO1_STAGE_GRADS, ZERO1_STAGE_STATE, ZERO1_STAGE_PARAMS = 1, 2, 4
 
 _lib = None
 
@@ -142,6 +143,10 @@ def load() -> ctypes.CDLL:
         "zero1_device_status": [vp, i32],
         "zero1_checksum": [vp, i64, vp, vp],
         "zero1_step_dynamic": [P, i32, i32, vp, vp, vp, vp, vp, A, vp, ctypes.POINTER(_PolicyStruct), vp, vp],
+        "zero1_staged_create": [P, i32, i32, i32, i64, ctypes.POINTER(vp)],
+        "zero1_staged_step": [vp, vp, vp, vp, vp, vp, vp, A, vp, vp],
+        "zero1_staged_destroy": [vp],
+        "zero1_staged_chunks": [vp, vp, i32, vp],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)

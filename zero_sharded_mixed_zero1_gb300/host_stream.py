@@ -1,27 +1,23 @@
 """The fused step over buffers in pinned host memory, staged through HBM by
-the copy engines while the computation runs.
+the copy engines while the computation runs: the binding of the staged-step
+handle (zero1_staged_create / zero1_staged_step / zero1_staged_destroy).
 
-The range is cut into chunks.  For each chunk, the inputs that live in host
-memory (the M gradient slices, the fp32 master/m/v) are copied into a device
-staging slot on an inbound copy stream (one cudaMemcpyAsync per slice); the
-step runs on the slot (zero1_step_bucket, the fused step on an element
-range); the outputs that live in host memory (master/m/v, and the bf16
-parameters if a host copy is wanted) are copied back on an outbound copy
-stream.  Three slots rotate, so the inbound copy of chunk k + 1, the step on
-chunk k and the outbound copy of chunk k - 1 run at the same time: with
-optimizer state in host memory both directions of the host link are busy
-(the ZeRO-Offload placement of the fp32 state in CPU memory, with the update
-itself on the GPU).  The step is element-wise, so the result is bit for bit
-that of one fused step on device buffers.  The streams and events are
-PyTorch's; every step of the arithmetic runs in the library's kernels.
+The library cuts the range into chunks; for each chunk an inbound copy
+stream moves the host-resident inputs (gradients, fp32 master/m/v) into one
+of three device slots, the fused step runs on the slot on the caller's
+stream, and an outbound copy stream moves the host-resident outputs back
+(master/m/v, and the bf16 parameters when a host copy is wanted).  This is
+the ZeRO-Offload placement of the fp32 state in host memory with the update
+itself on the GPU.  The results are bit for bit those of one fused step on
+device buffers.
 """
 from __future__ import annotations
+
+import ctypes
 
 import torch
 
 from . import _lib
-
-_SLOTS = 3
 
 
 def _pinned(t: torch.Tensor) -> bool:
@@ -38,14 +34,14 @@ class HostStreamedStep:
     place).  params: a CUDA bf16 tensor of nv elements, written by the step;
     if params_host (pinned, nv elements) is given, the updated parameters are
     also copied into it.  At least one of grads, master/m/v and params_host
-    must be in host memory, or there is nothing to stream.
+    must be in host memory, or there is nothing to stage.
 
     chunk_elems sets the copy granularity (rounded up to a multiple of 8);
-    the staging memory is 3 x chunk_elems x (2M bytes if the gradients are
-    staged + 12 bytes if the state is).  Launches go to `stream` (default:
-    the current stream at construction); the copies go to two more streams.
-    When a call returns, work enqueued later on `stream` sees the whole
-    step, including the copies back to host memory."""
+    the library allocates 3 x chunk_elems x (2M bytes if the gradients are
+    staged + 12 bytes if the state is) of device memory for the slots, and
+    two copy streams.  Launches go to `stream` (default: the current stream
+    at each call); when the stream reaches work enqueued after a call, the
+    step and its copies back to host memory are complete."""
 
     def __init__(self, plan: _lib.Plan, shard_begin: int, shard_end: int, grads, master, m, v, params,
                  chunk_elems: int = 1 << 24, params_host=None, overflow_flag=None, stream=None):
@@ -53,79 +49,64 @@ class HostStreamedStep:
         base, L, nv = _lib._range(plan, shard_begin, shard_end)
         if L == 0:
             raise ValueError("empty or invalid shard range")
-        self.grads_on_host = _pinned(grads[0])
+        grads_on_host = _pinned(grads[0])
         for i, g in enumerate(grads):
-            if g.dtype != torch.bfloat16 or g.numel() < nv or _pinned(g) != self.grads_on_host or \
-                    not (_pinned(g) or g.device.type == "cuda"):
-                raise ValueError(f"grads[{i}] must be a bf16 tensor of at least {nv} elements, all of them "
-                                 "pinned host tensors or all CUDA tensors")
-        self.state_on_host = _pinned(master)
-        for name, x in (("master", master), ("m", m), ("v", v)):
-            if x.dtype != torch.float32 or x.numel() < L or _pinned(x) != self.state_on_host or \
-                    not (_pinned(x) or x.device.type == "cuda"):
-                raise ValueError(f"{name} must be an fp32 tensor of at least {L} elements; master, m and v "
-                                 "all pinned host tensors or all CUDA tensors")
+            if _pinned(g) != grads_on_host:
+                raise ValueError("grads: all pinned host tensors or all CUDA tensors")
+        state_on_host = _pinned(master)
+        if _pinned(m) != state_on_host or _pinned(v) != state_on_host:
+            raise ValueError("master, m and v: all pinned host tensors or all CUDA tensors")
         if params.device.type != "cuda":
             raise ValueError("params must be a CUDA tensor")
-        if params_host is not None and (not _pinned(params_host) or params_host.numel() < nv):
-            raise ValueError("params_host must be a pinned host tensor of at least nv elements")
-        if not (self.grads_on_host or self.state_on_host or params_host is not None):
+        if params_host is not None and not _pinned(params_host):
+            raise ValueError("params_host must be a pinned host tensor")
+        what = ((_lib.ZERO1_STAGE_GRADS if grads_on_host else 0) |
+                (_lib.ZERO1_STAGE_STATE if state_on_host else 0) |
+                (_lib.ZERO1_STAGE_PARAMS if params_host is not None else 0))
+        if what == 0:
             raise ValueError("no buffer in host memory: call the fused step directly")
-        self.plan, self.base, self.L, self.nv = plan, base, L, nv
-        self.grads, self.master, self.m, self.v, self.params = grads, master, m, v, params
-        self.params_host, self.flag = params_host, overflow_flag
-        dev = params.device
+        self.plan, self.nv, self.L = plan, nv, L
         self.chunk = max(8, (int(chunk_elems) + 7) // 8 * 8)
-        self.stream = stream if stream is not None else torch.cuda.current_stream(dev)
-        self.in_stream = torch.cuda.Stream(device=dev)
-        self.out_stream = torch.cuda.Stream(device=dev)
-        gsize = min(self.chunk, max(nv, 8))
-        ssize = min(self.chunk, L)
-        self.gslots = [[torch.empty(gsize, dtype=torch.bfloat16, device=dev) for _ in range(plan.M)]
-                       for _ in range(_SLOTS)] if self.grads_on_host else None
-        self.sslots = [[torch.empty(ssize, dtype=torch.float32, device=dev) for _ in range(3)]
-                       for _ in range(_SLOTS)] if self.state_on_host else None
-        self.copied_in = [torch.cuda.Event() for _ in range(_SLOTS)]
-        self.computed = [torch.cuda.Event() for _ in range(_SLOTS)]
-        self.copied_out = [torch.cuda.Event() for _ in range(_SLOTS)]
-        cuts = list(range(0, L, self.chunk)) + [L]
-        self.pieces = list(zip(cuts[:-1], cuts[1:]))
+        # keep the tensors alive for as long as the handle holds their addresses
+        self._tensors = (list(grads), master, m, v, params, params_host, overflow_flag)
+        self._grads = _lib._ptrs(grads, torch.bfloat16, nv, "grads")
+        self._state = [_lib._dev(x, torch.float32, L, name) for x, name in ((master, "master"), (m, "m"), (v, "v"))]
+        self._params = _lib._dev(params, torch.bfloat16, nv, "params")
+        self._params_host = _lib._dev(params_host, torch.bfloat16, nv, "params_host") if params_host is not None \
+            else None
+        self._flag = _lib._dev(overflow_flag, torch.int32, 1, "overflow_flag") if overflow_flag is not None \
+            else None
+        self._stream = stream
+        self._device = params.device
+        self._lib = _lib.load()
+        handle = ctypes.c_void_p()
+        with torch.cuda.device(self._device):
+            _lib._check_rc(self._lib.zero1_staged_create(ctypes.byref(plan), shard_begin, shard_end, what,
+                                                         self.chunk, ctypes.byref(handle)))
+        self._handle = handle
+        count = ctypes.c_int32()
+        _lib._check_rc(self._lib.zero1_staged_chunks(handle, None, 0, ctypes.byref(count)))
+        cuts = (ctypes.c_int64 * count.value)()
+        _lib._check_rc(self._lib.zero1_staged_chunks(handle, cuts, count.value, ctypes.byref(count)))
+        self.pieces = list(zip(cuts[:-1], cuts[1:]))   # the library's chunk boundaries
 
     def __call__(self, hp: _lib.AdamW) -> None:
-        st, cin, cout = self.stream, self.in_stream, self.out_stream
-        has_out = self.state_on_host or self.params_host is not None
-        cin.wait_stream(st)                     # earlier work on the buffers is done
-        for k, (e0, e1) in enumerate(self.pieces):
-            slot = k % _SLOTS
-            real = max(0, min(self.nv, e1) - e0)
-            if k >= _SLOTS:                     # the slot's previous chunk is out of it
-                cin.wait_event(self.copied_out[slot] if has_out else self.computed[slot])
-            with torch.cuda.stream(cin):
-                if self.grads_on_host and real:
-                    for s, g in zip(self.gslots[slot], self.grads):
-                        s[:real].copy_(g[e0:e0 + real], non_blocking=True)
-                if self.state_on_host:
-                    for s, x in zip(self.sslots[slot], (self.master, self.m, self.v)):
-                        s[:e1 - e0].copy_(x[e0:e1], non_blocking=True)
-                self.copied_in[slot].record(cin)
-            st.wait_event(self.copied_in[slot])
-            if self.grads_on_host:
-                grads = [s[:max(real, 1)] for s in self.gslots[slot]]
-            else:
-                grads = [g[e0:e0 + real] for g in self.grads]
-            state = self.sslots[slot] if self.state_on_host else [x[e0:] for x in (self.master, self.m, self.v)]
-            params = self.params[e0:] if e0 < self.nv else self.params[:0]
-            _lib.zero1_step_bucket(self.plan, self.base + e0, self.base + e1, grads, *state, params, hp,
-                                   self.flag, stream=st)
-            self.computed[slot].record(st)
-            if has_out:
-                cout.wait_event(self.computed[slot])
-                with torch.cuda.stream(cout):
-                    if self.state_on_host:
-                        for s, x in zip(self.sslots[slot], (self.master, self.m, self.v)):
-                            x[e0:e1].copy_(s[:e1 - e0], non_blocking=True)
-                    if self.params_host is not None and real:
-                        self.params_host[e0:e0 + real].copy_(self.params[e0:e0 + real], non_blocking=True)
-                    self.copied_out[slot].record(cout)
-        if has_out:
-            st.wait_stream(cout)                # the copies back are part of the step
+        if self._handle is None:
+            raise ValueError("the staged step has been closed")
+        with torch.cuda.device(self._device):
+            _lib._check_rc(self._lib.zero1_staged_step(
+                self._handle, self._grads, *self._state, self._params, self._params_host,
+                ctypes.byref(hp.c_struct()), self._flag, _lib._stream(self._stream)))
+
+    def close(self) -> None:
+        """Wait for the handle's queued work and free its staging memory."""
+        if getattr(self, "_handle", None) is not None:
+            with torch.cuda.device(self._device):
+                self._lib.zero1_staged_destroy(self._handle)
+            self._handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -263,11 +263,17 @@ def host_link_rates(dev, nbytes: int = 1 << 30, reps: int = 4) -> dict:
             torch.cuda.synchronize(dev)
         return start.elapsed_time(end) * 1e-3
 
-    h2d = nbytes * reps / timed([[(dev_a[:half], host_in[:half])], [(dev_a[half:], host_in[half:])]]) / 1e9
-    d2h = nbytes * reps / timed([[(host_out, dev_b)]]) / 1e9
-    both = 2 * nbytes * reps / timed([[(dev_a, host_in)], [(host_out, dev_b)]]) / 1e9
+    # other work on a shared host only ever lowers these rates: keep the best
+    # of three measurements as the link's capacity
+    h2d = d2h = both = 0.0
+    for _ in range(3):
+        h2d = max(h2d, nbytes * reps / timed([[(dev_a[:half], host_in[:half])],
+                                               [(dev_a[half:], host_in[half:])]]) / 1e9)
+        d2h = max(d2h, nbytes * reps / timed([[(host_out, dev_b)]]) / 1e9)
+        both = max(both, 2 * nbytes * reps / timed([[(dev_a, host_in)], [(host_out, dev_b)]]) / 1e9)
     return {"h2d_gbs": h2d, "d2h_gbs": d2h, "both_directions_gbs": both,
-            "method": f"cudaMemcpyAsync of {nbytes >> 20} MiB pinned buffers x {reps}, CUDA events"}
+            "method": f"cudaMemcpyAsync of {nbytes >> 20} MiB pinned buffers x {reps}, CUDA events, "
+                      "best of 3"}
 
 
 def link_roofline(link: dict, h2d_bytes: int, d2h_bytes: int, seconds_per_step: float) -> dict:
@@ -474,11 +480,11 @@ def run_ours(args, w) -> None:
 
     # end to end through the public API with host buffers: each step's
     # gradients start in pinned host memory and the step's parameters and
-    # flag end in pinned host memory.  `e2e`: explicit copies of the gradients
-    # to HBM chunk by chunk on a copy stream, overlapping the step on the
-    # previous chunk (HostStreamedStep).  `e2e_zero_copy`: the kernel reads the
+    # flag end in pinned host memory.  `e2e`: the fused kernel reads the
     # pinned gradients and writes the pinned parameters over the host link.
-    e2e = e2e_zero = None
+    # `e2e_staged`: the copy engines stage the gradients to HBM chunk by chunk,
+    # overlapping the step on the previous chunk (zero1_staged_step).
+    e2e = e2e_staged = None
     if not args.no_e2e and op == "step":
         e2e_steps = max(3, min(args.steps, args.e2e_steps))
         host_g = [synth.normal_bf16(nv, w.grad_std * w.S, synth.seed_of(w.seed, 7, r, rank)).pin_memory()
@@ -516,17 +522,18 @@ def run_ours(args, w) -> None:
         del streamed
         link = host_link_rates(dev)
         bi, bo = w.M * nv * 2, nv * 2 + 4
-        e2e = {"value": world * nv * e2e_steps / copy_s, "unit": "params/s",
+        e2e_staged = {"value": world * nv * e2e_steps / copy_s, "unit": "params/s",
+                      "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": e2e_steps,
+                      "transfer": f"the gradients staged to HBM in {args.chunk_elems}-element chunks by the copy "
+                                  "engines (zero1_staged_step), overlapping the step on the previous chunk; params "
+                                  "and flag copied back",
+                      "roofline": link_roofline(link, bi, bo, copy_s / e2e_steps)}
+        e2e = {"value": world * nv * e2e_steps / zero_s, "unit": "params/s",
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": e2e_steps,
-               "transfer": f"the gradients staged to HBM in {args.chunk_elems}-element chunks by the copy engines "
-                           "(zero1_staged_step), overlapping the step on the previous chunk; params and flag "
-                           "copied back",
-               "roofline": link_roofline(link, bi, bo, copy_s / e2e_steps)}
-        e2e_zero = {"value": world * nv * e2e_steps / zero_s, "unit": "params/s",
-                    "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
-                    "transfer": "the kernel reads the pinned gradients and writes the pinned params "
-                                "over the host link (no staging copy)",
-                    "roofline": link_roofline(link, bi, bo, zero_s / e2e_steps)}
+               "transfer": "every step the fused kernel reads the M gradient buffers from pinned host memory and "
+                           "writes the bf16 params to pinned host memory over NVLink-C2C (no staging copy); "
+                           "the flag is copied back and the stream synchronised",
+               "roofline": link_roofline(link, bi, bo, zero_s / e2e_steps)}
         del host_g
 
     # with the state in host memory the step is bound by the host link: 12 B
@@ -567,7 +574,7 @@ def run_ours(args, w) -> None:
         "cpu_baseline": cpu_baseline,
         "offload_link_roofline": offload_link,
         "e2e": e2e,
-        "e2e_zero_copy": e2e_zero,
+        "e2e_staged": e2e_staged,
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks,
         "overflow_flag": overflow,

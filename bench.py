@@ -298,6 +298,9 @@ def config_of(w, state_on_host: bool = False, op: str = "step", transfer: str = 
                                  "copy_engines": "state chunks staged through HBM by the copy engines"}[transfer]
     if op == "dynamic":
         c["loss_scaling"] = "dynamic, device-resident (window 1000, hysteresis 2, factor 2)"
+    elif op == "dynamic_pingpong":
+        c["loss_scaling"] = ("dynamic, device-resident (window 1000, hysteresis 2, factor 2), ping-pong state "
+                             "(two copies of master/m/v)")
     elif op != "step":
         c["op"] = op + " (component measurement, not the step)"
     return c
@@ -351,17 +354,28 @@ def run_ours(args, w) -> None:
         return z.AdamW(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay,
                        loss_scale=w.S, global_batch=w.B, step=t)
 
-    op = "dynamic" if args.dynamic_loss_scale else args.op
-    if op == "dynamic":
+    op = args.op if args.op == "dynamic_pingpong" else ("dynamic" if args.dynamic_loss_scale else args.op)
+    if op in ("dynamic", "dynamic_pingpong"):
         policy = z.LossScalePolicy(initial_scale=w.S if w.S > 1 else 2.0 ** 12, factor=2.0, window=1000,
                                    hysteresis=2, min_scale=1.0)
         scaler = z.new_scaler(dev)
         z.zero1_scaler_init(scaler, policy, hp(1))
-        sums = torch.empty(L, dtype=torch.float32, device=dev)
+        if op == "dynamic":
+            sums = torch.empty(L, dtype=torch.float32, device=dev)
 
-        def launch(gr, tt, st=None):
-            z.zero1_step_dynamic(plan, sb, se, gr, master, m, v, params, hp(tt), scaler, policy, sums, stream=st)
-        op_kernel = "dynamic step: k_reduce_scatter + k_apply_sums + k_scaler_update"
+            def launch(gr, tt, st=None):
+                z.zero1_step_dynamic(plan, sb, se, gr, master, m, v, params, hp(tt), scaler, policy, sums,
+                                     stream=st)
+            op_kernel = "dynamic step: k_reduce_scatter + k_apply_sums + k_scaler_update"
+            launches_per_step, op_bytes = 3, algorithmic_bytes(nv, L - nv, w.M) + 8 * L
+        else:
+            pairs = [[x, torch.empty_like(x)] for x in (master, m, v)]
+
+            def launch(gr, tt, st=None):
+                z.zero1_step_dynamic_pingpong(plan, sb, se, gr, *pairs, params, hp(tt), scaler, policy, stream=st)
+            op_kernel = ("dynamic step, ping-pong state: k_fused_step_pingpong + k_restore_params (returns at "
+                         "once without overflow) + k_scaler_update")
+            launches_per_step, op_bytes = 3, algorithmic_bytes(nv, L - nv, w.M)
         if args.graph:
             # S and t live on the device: one attempt per gradient set is
             # captured once and replayed every step
@@ -381,7 +395,6 @@ def run_ours(args, w) -> None:
             def launch(gr, tt, st=None):      # noqa: F811 - replay instead of the eager call
                 graphs[id(gr)].replay()
             op_kernel += " (replayed from a CUDA graph)"
-        launches_per_step, op_bytes = 3, algorithmic_bytes(nv, L - nv, w.M) + 8 * L
     elif op == "overflow_check":
         def launch(gr, tt, st=None):
             z.zero1_overflow_check(plan, sb, se, gr, flag, stream=st)
@@ -594,7 +607,8 @@ def main(argv=None) -> int:
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--op", default="step",
-                    choices=["step", "dynamic", "overflow_check", "allreduce", "unfused", "bucketed", "tma"],
+                    choices=["step", "dynamic", "dynamic_pingpong", "overflow_check", "allreduce", "unfused",
+                             "bucketed", "tma"],
                     help="what one timed step runs: the fused ZeRO-1 step (default) or one of the other "
                          "entry points, for component measurements")
     ap.add_argument("--replicas", type=int, default=0, help="override the workload's M (measurement sweeps)")

@@ -350,7 +350,7 @@ typedef struct zero1_scaler {
     int32_t good_steps;      /* clean attempts in a row since S last changed */
     int32_t hysteresis_left; /* overflowing attempts still tolerated */
     uint32_t overflow;       /* flag of the attempt in progress; 0 between attempts */
-    uint32_t reserved;
+    uint32_t current;        /* ping-pong step: copy (0 or 1) of master/m/v holding the current state */
 } zero1_scaler_t;
 
 /* Start a scaler (one tiny kernel on `stream`): S = policy->initial_scale,
@@ -380,6 +380,32 @@ int zero1_step_dynamic(const zero1_plan_t *plan, int32_t shard_begin, int32_t sh
                        const void *const *grads, float *master, float *m, float *v, void *params,
                        const zero1_adamw_t *hp, zero1_scaler_t *scaler,
                        const zero1_loss_scale_policy_t *policy, float *sums, zero1_stream_t stream);
+
+/* One attempt of the dynamically scaled step with ping-pong state [Z1], [OPT]:
+ * the same rule and bit for bit the same results as zero1_step_dynamic, in a
+ * single pass over the data (2M + 26 bytes per parameter, the fused step's
+ * traffic) at the cost of a second copy of master/m/v.  master[k], m[k],
+ * v[k] (k = 0, 1; host arrays of two device pointers, L fp32 elements each,
+ * distinct buffers) are two copies of the state; scaler->current (0 after
+ * zero1_scaler_init) names the copy that holds the current state.  Three
+ * kernels on `stream`:
+ *  1. the fused step reading copy `current` and writing the updated master,
+ *     m, v into the other copy and the bf16 parameters into params, ORing the
+ *     overflow flag into scaler->overflow;
+ *  2. if the flag is set, params is rewritten as bf16(master[current]) - so
+ *     a skipped attempt leaves params unchanged provided they held
+ *     bf16(master[current]) on entry, as they do after any applied step;
+ *  3. the scaler advances by the rule above; a clean attempt also switches
+ *     scaler->current to the copy just written.
+ * The other copy's contents on entry do not matter.  Both copies must start
+ * at the same 16-byte phase for the 128-bit path (else the whole range runs
+ * per element).  No workspace is needed; the call can be captured in a CUDA
+ * graph (the copy to read is decided on the device).  EINVAL: as
+ * zero1_step_dynamic, or the two copies of an array are the same buffer. */
+int zero1_step_dynamic_pingpong(const zero1_plan_t *plan, int32_t shard_begin, int32_t shard_end,
+                                const void *const *grads, float *const *master, float *const *m,
+                                float *const *v, void *params, const zero1_adamw_t *hp, zero1_scaler_t *scaler,
+                                const zero1_loss_scale_policy_t *policy, zero1_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * The dynamically scaled step without any device allocation by the caller.

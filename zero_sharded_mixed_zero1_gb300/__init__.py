@@ -40,5 +40,7 @@ from ._lib import (  # noqa: F401
     zero1_checksum,
     zero1_step_dynamic,
     zero1_step_dynamic_noalloc,
+    zero1_step_dynamic_pingpong,
+    current_state,
 )
 from .host_stream import HostStreamedStep  # noqa: E402,F401

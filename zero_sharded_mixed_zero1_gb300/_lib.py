@@ -106,7 +106,7 @@ def scaler_state(scaler: torch.Tensor) -> dict:
     """Read a zero1_scaler_t back to the host (synchronises with its stream)."""
     raw = bytes(scaler.cpu().numpy().tobytes())
     k = ["scale", "inv", "bc1", "bc2", "step", "attempts", "skipped", "good_steps", "hysteresis_left",
-         "overflow", "reserved"]
+         "overflow", "current"]
     return dict(zip(k, struct.unpack(_SCALER_FMT, raw)))
 
 
@@ -143,6 +143,7 @@ def load() -> ctypes.CDLL:
         "zero1_device_status": [vp, i32],
         "zero1_checksum": [vp, i64, vp, vp],
         "zero1_step_dynamic": [P, i32, i32, vp, vp, vp, vp, vp, A, vp, ctypes.POINTER(_PolicyStruct), vp, vp],
+        "zero1_step_dynamic_pingpong": [P, i32, i32, vp, vp, vp, vp, vp, A, vp, ctypes.POINTER(_PolicyStruct), vp],
         "zero1_staged_create": [P, i32, i32, i32, i64, ctypes.POINTER(vp)],
         "zero1_staged_step": [vp, vp, vp, vp, vp, vp, vp, A, vp, vp],
         "zero1_staged_destroy": [vp],
@@ -390,6 +391,31 @@ def zero1_step_dynamic(plan: Plan, shard_begin: int, shard_end: int, grads, mast
         _dev(master, torch.float32, L, "master"), _dev(m, torch.float32, L, "m"), _dev(v, torch.float32, L, "v"),
         _dev(params, torch.bfloat16, nv, "params"), ctypes.byref(hp.c_struct()), _scaler_ptr(scaler),
         ctypes.byref(policy.c_struct()), _dev(sums, torch.float32, L, "sums"), _stream(stream)))
+
+
+def zero1_step_dynamic_pingpong(plan: Plan, shard_begin: int, shard_end: int, grads, master, m, v, params,
+                                hp: AdamW, scaler: torch.Tensor, policy: LossScalePolicy, stream=None) -> None:
+    """One dynamically scaled attempt with ping-pong state: master, m, v are
+    pairs of fp32 tensors (two copies of the state; the scaler's `current`
+    field names the one holding the current state, see current_state)."""
+    _replicas(plan, grads, "grads")
+    _, L, nv = _range(plan, shard_begin, shard_end)
+    pairs = []
+    for name, pair in (("master", master), ("m", m), ("v", v)):
+        if len(pair) != 2:
+            raise ValueError(f"{name}: expected two tensors (the two copies of the state)")
+        pairs.append((ctypes.c_void_p * 2)(*[_dev(t, torch.float32, L, f"{name}[{k}]") for k, t in enumerate(pair)]))
+    _check_rc(load().zero1_step_dynamic_pingpong(
+        ctypes.byref(plan), shard_begin, shard_end, _ptrs(grads, torch.bfloat16, nv, "grads"), *pairs,
+        _dev(params, torch.bfloat16, nv, "params"), ctypes.byref(hp.c_struct()), _scaler_ptr(scaler),
+        ctypes.byref(policy.c_struct()), _stream(stream)))
+
+
+def current_state(scaler: torch.Tensor, master, m, v):
+    """(master, m, v) of the copy holding the current state after ping-pong
+    attempts (reads the scaler back: synchronises with its stream)."""
+    k = scaler_state(scaler)["current"] & 1
+    return master[k], m[k], v[k]
 
 
 # -- the dynamically scaled step with the library's own workspace --------------

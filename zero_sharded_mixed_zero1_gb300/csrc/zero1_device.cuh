@@ -225,6 +225,26 @@ __device__ __forceinline__ void store_vec(const float s[kVec], float4 w0, float4
                       pack_bf16x2(ww[6], ww[7])));
 }
 
+// The loads of one 8-element vector for M <= 8: every replica's gradient
+// vector, then the fp32 state.
+template <int MT>
+struct VecLoads {
+    uint4 q[MT];
+    float4 w0, w1, m0, m1, v0, v1;
+    __device__ __forceinline__ void load(const GradPtrs &g, const float *master, const float *mom,
+                                         const float *var, int64_t j)
+    {
+#pragma unroll
+        for (int r = 0; r < MT; ++r) q[r] = ld_stream_u4(g.p[r] + j);
+        w0 = ld_state(master + j);
+        w1 = ld_state(master + j + 4);
+        m0 = ld_state(mom + j);
+        m1 = ld_state(mom + j + 4);
+        v0 = ld_state(var + j);
+        v1 = ld_state(var + j + 4);
+    }
+};
+
 // Per-element remainder of the fused step: [0, head) and the tail after the
 // vector body (real elements below nv, padding above).
 __device__ __forceinline__ void fused_scalar_rest(const GradPtrs &g, int M, float *master, float *mom,

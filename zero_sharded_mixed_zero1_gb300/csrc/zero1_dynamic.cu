@@ -51,16 +51,21 @@ __global__ void k_scaler_init(zero1_scaler_t *sc, float initial_scale, int32_t h
     sc->good_steps = 0;
     sc->hysteresis_left = hysteresis;
     sc->overflow = 0u;
-    sc->reserved = 0u;
+    sc->current = 0u;
     derive_constants(sc, B, beta1, beta2);
 }
 
 // Advance the scaler after an attempt (reads the attempt's flag, clears it).
-__global__ void k_scaler_update(zero1_scaler_t *sc, const ScalePolicy pol, int64_t B, float beta1, float beta2)
+// With ping-pong state a clean attempt also makes the buffer it wrote the
+// current one.
+__global__ void k_scaler_update(zero1_scaler_t *sc, const ScalePolicy pol, int64_t B, float beta1, float beta2,
+                                int pingpong)
 {
     if (threadIdx.x != 0 || blockIdx.x != 0) return;
     sc->attempts += 1;
-    if (*reinterpret_cast<volatile uint32_t *>(&sc->overflow) != 0u) {
+    const bool overflow = *reinterpret_cast<volatile uint32_t *>(&sc->overflow) != 0u;
+    if (pingpong && !overflow) sc->current ^= 1u;
+    if (overflow) {
         sc->skipped += 1;
         sc->good_steps = 0;
         sc->hysteresis_left -= 1;
@@ -116,6 +121,111 @@ k_apply_sums(const float *__restrict__ sums, float *__restrict__ master, float *
         mom[j] = mm;
         var[j] = vv;
         if (j < w.nv) params[j] = to_bf16(ww);
+    }
+}
+
+// --------------------------------------------------- ping-pong state ------
+//
+// The dynamic step in one pass over the data: master/m/v exist twice, and
+// scaler->current says which copy holds the current state.  An attempt reads
+// the current copy and writes the updated state into the other one, so an
+// attempt whose gradients overflow has changed nothing that is current: the
+// scaler update simply does not switch copies.  The bf16 parameters (one
+// copy) are written by the attempt and, if it overflowed, rewritten from the
+// current master by k_restore_params.  Traffic per element is the fused
+// step's 2M + 26 bytes instead of the two-pass 2M + 34.
+
+struct PingPong {
+    float *master[2], *mom[2], *var[2];
+};
+
+// One attempt for M <= 8 (MT = M, two vectors of loads in flight per thread)
+// or M > 8 (MT = 0, replicas in groups of 8).  For M > 8, measured on the
+// 64-replica shard: state read with the default policy at two blocks per SM
+// (107 registers) beat three blocks per SM, whose 85-register cap spilled
+// (2.64 against 2.75-2.85 ms).
+template <int MT>
+__global__ void __launch_bounds__(kBlock, MT == 0 ? 2 : (MT <= 2 ? 2 : 1))
+k_fused_step_pingpong(const __grid_constant__ GradPtrs g, int M, const PingPong s, uint16_t *__restrict__ params,
+                      const Walk w, Z1Consts c, zero1_scaler_t *sc)
+{
+    const int cur = (int)(*reinterpret_cast<const volatile uint32_t *>(&sc->current) & 1u);
+    c.inv = sc->inv;
+    c.bc1 = sc->bc1;
+    c.bc2 = sc->bc2;
+    // selects, not s.x[cur]: indexing the parameter struct by a runtime value
+    // would copy it to local memory
+    const float *__restrict__ sw = cur ? s.master[1] : s.master[0];
+    const float *__restrict__ sm = cur ? s.mom[1] : s.mom[0];
+    const float *__restrict__ sv = cur ? s.var[1] : s.var[0];
+    float *__restrict__ dw = cur ? s.master[0] : s.master[1];
+    float *__restrict__ dm = cur ? s.mom[0] : s.mom[1];
+    float *__restrict__ dv = cur ? s.var[0] : s.var[1];
+    const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
+    const int64_t nthr = (int64_t)gridDim.x * kBlock;
+    bool bad = false;
+    if constexpr (MT > 0) {
+        pipelined<VecLoads<MT>>(
+            w.nvec, tid, nthr, [&](VecLoads<MT> &x, int64_t i) { x.load(g, sw, sm, sv, w.head + i * kVec); },
+            [&](const VecLoads<MT> &x, int64_t i) {
+                const int64_t j = w.head + i * kVec;
+                float sum[kVec];
+                unpack8(x.q[0], sum);
+#pragma unroll
+                for (int r = 1; r < MT; ++r) add8(x.q[r], sum);
+                store_vec(sum, x.w0, x.w1, x.m0, x.m1, x.v0, x.v1, dw + j, dm + j, dv + j, params + j, c, bad);
+            });
+    } else {
+        for (int64_t i = tid; i < w.nvec; i += nthr) {
+            const int64_t j = w.head + i * kVec;
+            const float4 *pw = reinterpret_cast<const float4 *>(sw + j);
+            const float4 *pm = reinterpret_cast<const float4 *>(sm + j);
+            const float4 *pv = reinterpret_cast<const float4 *>(sv + j);
+            const float4 w0 = pw[0], w1 = pw[1], m0 = pm[0], m1 = pm[1], v0 = pv[0], v1 = pv[1];
+            float sum[kVec];
+            sum8<0>(g, M, j, sum);
+            store_vec(sum, w0, w1, m0, m1, v0, v1, dw + j, dm + j, dv + j, params + j, c, bad);
+        }
+    }
+    const int64_t ns = w.L - w.nvec * kVec;
+    for (int64_t q = tid; q < ns; q += nthr) {
+        const int64_t j = scalar_index(w, q);
+        float gs = 0.0f;
+        if (j < w.nv) {
+            gs = sum1(g, M, j);
+            bad |= !finite(gs);
+        }
+        float ww = sw[j], mm = sm[j], vv = sv[j];
+        adamw1(__fmul_rn(gs, c.inv), c, ww, mm, vv);
+        dw[j] = ww;
+        dm[j] = mm;
+        dv[j] = vv;
+        if (j < w.nv) params[j] = to_bf16(ww);
+    }
+    warp_flag(&sc->overflow, bad);
+}
+
+// After an attempt that overflowed, put back params = bf16(current master);
+// after a clean attempt, return at once.
+__global__ void __launch_bounds__(kBlock)
+k_restore_params(const PingPong s, uint16_t *__restrict__ params, const Walk w, const zero1_scaler_t *sc)
+{
+    if (*reinterpret_cast<const volatile uint32_t *>(&sc->overflow) == 0u) return;
+    const float *__restrict__ master =
+        (*reinterpret_cast<const volatile uint32_t *>(&sc->current) & 1u) ? s.master[1] : s.master[0];
+    const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
+    const int64_t nthr = (int64_t)gridDim.x * kBlock;
+    for (int64_t i = tid; i < w.nvec; i += nthr) {
+        const int64_t j = w.head + i * kVec;
+        const float4 a = ld_state(master + j), b = ld_state(master + j + 4);
+        __stcs(reinterpret_cast<uint4 *>(params + j),
+               make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y),
+                          pack_bf16x2(b.z, b.w)));
+    }
+    const int64_t ns = w.L - w.nvec * kVec;
+    for (int64_t q = tid; q < ns; q += nthr) {
+        const int64_t j = scalar_index(w, q);
+        if (j < w.nv) params[j] = to_bf16(master[j]);
     }
 }
 
@@ -211,8 +321,59 @@ extern "C" int zero1_step_dynamic(const zero1_plan_t *plan, int32_t shard_begin,
     k_apply_sums<<<grid, kBlock, 0, st>>>(sums, master, m, v, static_cast<uint16_t *>(params), wu, c, scaler);
     // 3. the scaler advances
     const ScalePolicy pol{policy->factor, policy->window, policy->hysteresis, policy->min_scale};
-    k_scaler_update<<<1, 32, 0, st>>>(scaler, pol, hp->global_batch, hp->beta1, hp->beta2);
+    k_scaler_update<<<1, 32, 0, st>>>(scaler, pol, hp->global_batch, hp->beta1, hp->beta2, 0);
     return launch_status("dynamic step launch");
+}
+
+extern "C" int zero1_step_dynamic_pingpong(const zero1_plan_t *plan, int32_t shard_begin, int32_t shard_end,
+                                           const void *const *grads, float *const *master, float *const *m,
+                                           float *const *v, void *params, const zero1_adamw_t *hp,
+                                           zero1_scaler_t *scaler, const zero1_loss_scale_policy_t *policy,
+                                           zero1_stream_t stream)
+{
+    Z1Range r;
+    int rc = z1_range(plan, shard_begin, shard_end, &r);
+    if (rc != ZERO1_OK) return rc;
+    Z1Consts c;
+    if ((rc = dynamic_constants(hp, plan->M, &c)) != ZERO1_OK) return rc;
+    if ((rc = check_scaler_ptr(scaler)) != ZERO1_OK || (rc = check_policy(policy)) != ZERO1_OK) return rc;
+    if (!master || !m || !v) return z1_fail(ZERO1_EINVAL, "ping-pong step: master, m and v arrays are NULL");
+    PingPong s{};
+    for (int k = 0; k < 2; ++k) {
+        if (!master[k] || !m[k] || !v[k])
+            return z1_fail(ZERO1_EINVAL, "ping-pong step: copy %d of master, m or v is NULL", k);
+        if ((rc = check_natural(master[k], 4, "master")) || (rc = check_natural(m[k], 4, "m")) ||
+            (rc = check_natural(v[k], 4, "v")))
+            return rc;
+        s.master[k] = master[k];
+        s.mom[k] = m[k];
+        s.var[k] = v[k];
+    }
+    if (s.master[0] == s.master[1] || s.mom[0] == s.mom[1] || s.var[0] == s.var[1])
+        return z1_fail(ZERO1_EINVAL, "ping-pong step: the two copies of master, m or v are the same buffer");
+    if (r.nv > 0 && !params)
+        return z1_fail(ZERO1_EINVAL, "ping-pong step: params must be non-NULL when the range holds parameters");
+    if ((rc = check_natural(params, 2, "params")) != ZERO1_OK) return rc;
+    GradPtrs g{};
+    if (r.nv > 0 && (rc = load_grads(plan, grads, &g, "ping-pong step")) != ZERO1_OK) return rc;
+    // one walk serves both copies: they must share the 16-byte phase
+    ArrayRef arr[ZERO1_MAX_REPLICAS + 7] = {{s.master[0], 4}, {s.mom[0], 4}, {s.var[0], 4}, {s.master[1], 4},
+                                            {s.mom[1], 4},    {s.var[1], 4}, {params, 2}};
+    const int M = plan->M;
+    for (int k = 0; k < M; ++k) arr[7 + k] = {g.p[k], 2};
+    const Walk w = make_walk(r.L, r.nv, arr, 7 + M);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint16_t *pp = static_cast<uint16_t *>(params);
+    dispatch_m(M, [&](auto mt) {
+        constexpr int MT = decltype(mt)::value;
+        const int grid = grid_for(k_fused_step_pingpong<MT>, work_of(w));
+        k_fused_step_pingpong<MT><<<grid, kBlock, 0, st>>>(g, M, s, pp, w, c, scaler);
+    });
+    const int rgrid = grid_for(k_restore_params, work_of(w));
+    k_restore_params<<<rgrid, kBlock, 0, st>>>(s, pp, w, scaler);
+    const ScalePolicy pol{policy->factor, policy->window, policy->hysteresis, policy->min_scale};
+    k_scaler_update<<<1, 32, 0, st>>>(scaler, pol, hp->global_batch, hp->beta1, hp->beta2, 1);
+    return launch_status("ping-pong step launch");
 }
 
 // ------------------------------------------- step without caller allocation --

@@ -298,9 +298,11 @@ def config_of(w, state_on_host: bool = False, op: str = "step", transfer: str = 
                                  "copy_engines": "state chunks staged through HBM by the copy engines"}[transfer]
     if op == "dynamic":
         c["loss_scaling"] = "dynamic, device-resident (window 1000, hysteresis 2, factor 2)"
-    elif op == "dynamic_pingpong":
+    elif op in ("dynamic_pingpong", "bucketed_pingpong"):
         c["loss_scaling"] = ("dynamic, device-resident (window 1000, hysteresis 2, factor 2), ping-pong state "
                              "(two copies of master/m/v)")
+        if op == "bucketed_pingpong":
+            c["op"] = "gradient buckets updated as they arrive, skip decided after the last bucket"
     elif op != "step":
         c["op"] = op + " (component measurement, not the step)"
     return c
@@ -354,8 +356,8 @@ def run_ours(args, w) -> None:
         return z.AdamW(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay,
                        loss_scale=w.S, global_batch=w.B, step=t)
 
-    op = args.op if args.op == "dynamic_pingpong" else ("dynamic" if args.dynamic_loss_scale else args.op)
-    if op in ("dynamic", "dynamic_pingpong"):
+    op = args.op if "pingpong" in args.op else ("dynamic" if args.dynamic_loss_scale else args.op)
+    if op in ("dynamic", "dynamic_pingpong", "bucketed_pingpong"):
         policy = z.LossScalePolicy(initial_scale=w.S if w.S > 1 else 2.0 ** 12, factor=2.0, window=1000,
                                    hysteresis=2, min_scale=1.0)
         scaler = z.new_scaler(dev)
@@ -368,7 +370,7 @@ def run_ours(args, w) -> None:
                                      stream=st)
             op_kernel = "dynamic step: k_reduce_scatter + k_apply_sums + k_scaler_update"
             launches_per_step, op_bytes = 3, algorithmic_bytes(nv, L - nv, w.M) + 8 * L
-        else:
+        elif op == "dynamic_pingpong":
             pairs = [[x, torch.empty_like(x)] for x in (master, m, v)]
 
             def launch(gr, tt, st=None):
@@ -376,6 +378,23 @@ def run_ours(args, w) -> None:
             op_kernel = ("dynamic step, ping-pong state: k_fused_step_pingpong + k_restore_params (returns at "
                          "once without overflow) + k_scaler_update")
             launches_per_step, op_bytes = 3, algorithmic_bytes(nv, L - nv, w.M)
+        else:
+            # gradient buckets of reduce_bucket_size elements updated as they
+            # arrive, the skip decided once all have run
+            pairs = [[x, torch.empty_like(x)] for x in (master, m, v)]
+            buckets = z.PingPongBuckets(plan, sb, se, *pairs, params, scaler, policy, stream=stream)
+            bucket = args.bucket_elems
+            cuts = list(range(0, L, bucket)) + [L]
+
+            def launch(gr, tt, st=None):
+                h = hp(tt)
+                for e0, e1 in zip(cuts[:-1], cuts[1:]):
+                    k = max(0, min(nv, e1) - e0)
+                    buckets.bucket(e0, e1, [g[e0:e0 + k] for g in gr], h)
+                buckets.finish(h)
+            op_kernel = (f"dynamic step, ping-pong state, buckets of {bucket} elements: k_fused_step_pingpong "
+                         "per bucket + k_restore_params + k_scaler_update")
+            launches_per_step, op_bytes = len(cuts) + 1, algorithmic_bytes(nv, L - nv, w.M)
         if args.graph:
             # S and t live on the device: one attempt per gradient set is
             # captured once and replayed every step
@@ -607,8 +626,8 @@ def main(argv=None) -> int:
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--op", default="step",
-                    choices=["step", "dynamic", "dynamic_pingpong", "overflow_check", "allreduce", "unfused",
-                             "bucketed", "tma"],
+                    choices=["step", "dynamic", "dynamic_pingpong", "bucketed_pingpong", "overflow_check",
+                             "allreduce", "unfused", "bucketed", "tma"],
                     help="what one timed step runs: the fused ZeRO-1 step (default) or one of the other "
                          "entry points, for component measurements")
     ap.add_argument("--replicas", type=int, default=0, help="override the workload's M (measurement sweeps)")

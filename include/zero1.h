@@ -407,6 +407,30 @@ int zero1_step_dynamic_pingpong(const zero1_plan_t *plan, int32_t shard_begin, i
                                 float *const *v, void *params, const zero1_adamw_t *hp, zero1_scaler_t *scaler,
                                 const zero1_loss_scale_policy_t *policy, zero1_stream_t stream);
 
+/* The ping-pong attempt in buckets, for gradients that arrive bucket by
+ * bucket during the backward pass [Z1], [OPT] (reduce_bucket_size,
+ * overlap_comm; "CS336 Lecture 7: Parallelism 1", ZeRO Stage 2).  Because an
+ * attempt only writes the non-current copy, each bucket can be updated as
+ * soon as its gradients exist, before the attempt's overflow flag is known:
+ *  zero1_pingpong_bucket: kernel 1 of zero1_step_dynamic_pingpong on the
+ *      element range [elem_begin, elem_end) of the padded flat buffer
+ *      (grads[r]: the bucket's gradients; master[k], m[k], v[k], params:
+ *      pointers to element elem_begin of each copy and of the parameters, as
+ *      zero1_step_bucket); the flag is ORed into scaler->overflow;
+ *  zero1_pingpong_finish: kernels 2 and 3 over shards [shard_begin,
+ *      shard_end) (master[k] and params at the range's first element).
+ * The buckets of one attempt must cover the finish's whole range, each
+ * element once, before the finish; then the attempt is bit for bit
+ * zero1_step_dynamic_pingpong over that range (the step is element-wise and
+ * the copy to read does not change before the finish).  A bucket's gradient
+ * buffers can be reused once its launch has run. */
+int zero1_pingpong_bucket(const zero1_plan_t *plan, int64_t elem_begin, int64_t elem_end,
+                          const void *const *grads, float *const *master, float *const *m, float *const *v,
+                          void *params, const zero1_adamw_t *hp, zero1_scaler_t *scaler, zero1_stream_t stream);
+int zero1_pingpong_finish(const zero1_plan_t *plan, int32_t shard_begin, int32_t shard_end,
+                          float *const *master, void *params, const zero1_adamw_t *hp, zero1_scaler_t *scaler,
+                          const zero1_loss_scale_policy_t *policy, zero1_stream_t stream);
+
 /* ---------------------------------------------------------------------------
  * The dynamically scaled step without any device allocation by the caller.
  *

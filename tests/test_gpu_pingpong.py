@@ -221,3 +221,78 @@ def test_pingpong_rejects_bad_arguments(cuda_device):
         pair(st[2].data_ptr(), v1.data_ptr()), params.data_ptr(), ctypes.byref(hp.c_struct()),
         scaler.data_ptr(), ctypes.byref(policy.c_struct()), torch.cuda.current_stream().cuda_stream)
     assert rc == -2
+
+
+def random_cover(L, rng, max_bucket):
+    """Random bucket boundaries over [0, L), multiples of 8 but the last."""
+    cuts = [0]
+    while cuts[-1] < L:
+        step = int(rng.integers(1, max_bucket // 8 + 1)) * 8
+        cuts.append(min(L, cuts[-1] + step))
+    return list(zip(cuts[:-1], cuts[1:]))
+
+
+@pytest.mark.parametrize("M,n,align,shards,max_bucket", [(8, 200_003, 128, None, 50_000),
+                                                         (13, 30_011, 8, (2, 11), 4096),
+                                                         (3, 9_999, 1, (1, 2), 800)])
+def test_bucketed_pingpong_equals_whole_attempt(cuda_device, M, n, align, shards, max_bucket):
+    """Buckets in random order and sizes, their gradient buffers recycled,
+    then the finish: bit for bit the whole-range ping-pong attempt, including
+    attempts skipped because one bucket overflowed."""
+    dev = cuda_device
+    rng = np.random.default_rng(M)
+    plan = z.zero1_plan(n, M, align)
+    sb, se = shards or (0, M)
+    base, L, nv = plan.shard_range(sb, se)
+    policy = z.LossScalePolicy(initial_scale=1024.0, factor=2.0, window=2, hysteresis=1, min_scale=1.0)
+    hp = z.AdamW(global_batch=1024, step=1)
+    start = [t[base:base + L].clone() for t in make_state(n, plan.padded_n, 51, dev, nonzero_moments=True)]
+    whole = [[t.clone(), torch.zeros_like(t)] for t in start]
+    bucketed = [[t.clone(), torch.full_like(t, float("nan"))] for t in start]
+    pw = bf16_of(start[0], nv) if nv else torch.zeros(1, dtype=torch.bfloat16, device=dev)
+    pb = pw.clone()
+    s_w, s_b = z.new_scaler(dev), z.new_scaler(dev)
+    z.zero1_scaler_init(s_w, policy, hp)
+    z.zero1_scaler_init(s_b, policy, hp)
+    attempt = z.PingPongBuckets(plan, sb, se, *bucketed, pb, s_b, policy)
+    recycled = [torch.empty(max_bucket, dtype=torch.bfloat16, device=dev) for _ in range(M)]
+    for k in range(5):
+        grads = [synth.normal_bf16(max(nv, 1), 1e-3 * 1024, synth.seed_of(52, k, r), dev)[:nv] for r in range(M)]
+        if k in (1, 3) and nv:
+            grads[k % M][nv - 1 - k] = float("inf")          # in the range's last bucket
+        z.zero1_step_dynamic_pingpong(plan, sb, se, grads, *whole, pw, hp, s_w, policy)
+        cover = random_cover(L, rng, max_bucket)
+        for i in rng.permutation(len(cover)):
+            b, e = cover[i]
+            real = max(0, min(nv, e) - b)
+            for buf, g in zip(recycled, grads):
+                buf[:real].copy_(g[b:b + real])
+            attempt.bucket(b, e, [buf[:real] for buf in recycled], hp)
+        attempt.finish(hp)
+        torch.cuda.synchronize()
+        for x, y, what in zip(z.current_state(s_w, *whole), z.current_state(s_b, *bucketed), ("master", "m", "v")):
+            assert_f32_bits(f32(y), f32(x), f"{what} attempt {k}")
+        assert_bf16_bits(u16(pb[:nv]), u16(pw[:nv]), f"params attempt {k}")
+        assert z.scaler_state(s_b) == z.scaler_state(s_w)
+    assert z.scaler_state(s_b)["skipped"] == 2
+
+
+def test_bucketed_pingpong_checks_coverage(cuda_device):
+    dev = cuda_device
+    M, n = 2, 4096
+    plan = z.zero1_plan(n, M, 8)
+    policy = z.LossScalePolicy()
+    hp = z.AdamW(global_batch=64)
+    sc = z.new_scaler(dev)
+    z.zero1_scaler_init(sc, policy, hp)
+    st = make_state(n, plan.padded_n, 1, dev)
+    pairs = [[t, torch.zeros_like(t)] for t in st]
+    params = bf16_of(st[0], n)
+    grads = [torch.zeros(n, dtype=torch.bfloat16, device=dev) for _ in range(M)]
+    attempt = z.PingPongBuckets(plan, 0, M, *pairs, params, sc, policy)
+    attempt.bucket(0, 1024, [g[:1024] for g in grads], hp)
+    attempt.bucket(2048, 4096, [g[2048:] for g in grads], hp)
+    with pytest.raises(ValueError):          # [1024, 2048) missing
+        attempt.finish(hp)
+    with pytest.raises(ValueError):
+        attempt.bucket(4000, 4100, [g[4000:] for g in grads], hp)

@@ -41,6 +41,9 @@ from ._lib import (  # noqa: F401
     zero1_step_dynamic,
     zero1_step_dynamic_noalloc,
     zero1_step_dynamic_pingpong,
+    zero1_pingpong_bucket,
+    zero1_pingpong_finish,
+    PingPongBuckets,
     current_state,
 )
 from .host_stream import HostStreamedStep  # noqa: E402,F401

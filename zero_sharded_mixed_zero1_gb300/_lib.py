@@ -144,6 +144,8 @@ def load() -> ctypes.CDLL:
         "zero1_checksum": [vp, i64, vp, vp],
         "zero1_step_dynamic": [P, i32, i32, vp, vp, vp, vp, vp, A, vp, ctypes.POINTER(_PolicyStruct), vp, vp],
         "zero1_step_dynamic_pingpong": [P, i32, i32, vp, vp, vp, vp, vp, A, vp, ctypes.POINTER(_PolicyStruct), vp],
+        "zero1_pingpong_bucket": [P, i64, i64, vp, vp, vp, vp, vp, A, vp, vp],
+        "zero1_pingpong_finish": [P, i32, i32, vp, vp, A, vp, ctypes.POINTER(_PolicyStruct), vp],
         "zero1_staged_create": [P, i32, i32, i32, i64, ctypes.POINTER(vp)],
         "zero1_staged_step": [vp, vp, vp, vp, vp, vp, vp, A, vp, vp],
         "zero1_staged_destroy": [vp],
@@ -400,15 +402,82 @@ def zero1_step_dynamic_pingpong(plan: Plan, shard_begin: int, shard_end: int, gr
     field names the one holding the current state, see current_state)."""
     _replicas(plan, grads, "grads")
     _, L, nv = _range(plan, shard_begin, shard_end)
-    pairs = []
-    for name, pair in (("master", master), ("m", m), ("v", v)):
-        if len(pair) != 2:
-            raise ValueError(f"{name}: expected two tensors (the two copies of the state)")
-        pairs.append((ctypes.c_void_p * 2)(*[_dev(t, torch.float32, L, f"{name}[{k}]") for k, t in enumerate(pair)]))
+    pairs = [_pair(name, pair, L) for name, pair in (("master", master), ("m", m), ("v", v))]
     _check_rc(load().zero1_step_dynamic_pingpong(
         ctypes.byref(plan), shard_begin, shard_end, _ptrs(grads, torch.bfloat16, nv, "grads"), *pairs,
         _dev(params, torch.bfloat16, nv, "params"), ctypes.byref(hp.c_struct()), _scaler_ptr(scaler),
         ctypes.byref(policy.c_struct()), _stream(stream)))
+
+
+def _pair(name, pair, numel):
+    if len(pair) != 2:
+        raise ValueError(f"{name}: expected two tensors (the two copies of the state)")
+    return (ctypes.c_void_p * 2)(*[_dev(t, torch.float32, numel, f"{name}[{k}]") for k, t in enumerate(pair)])
+
+
+def zero1_pingpong_bucket(plan: Plan, elem_begin: int, elem_end: int, grads, master, m, v, params, hp: AdamW,
+                          scaler: torch.Tensor, stream=None) -> None:
+    """The ping-pong kernel on one bucket [elem_begin, elem_end): master, m,
+    v are pairs of tensors and params a tensor, all starting at element
+    elem_begin; grads[r] the bucket's gradients."""
+    _replicas(plan, grads, "grads")
+    L = max(0, elem_end - elem_begin)
+    nv = max(0, min(plan.n - elem_begin, L))
+    _check_rc(load().zero1_pingpong_bucket(
+        ctypes.byref(plan), elem_begin, elem_end, _ptrs(grads, torch.bfloat16, nv, "grads"),
+        _pair("master", master, L), _pair("m", m, L), _pair("v", v, L), _dev(params, torch.bfloat16, nv, "params"),
+        ctypes.byref(hp.c_struct()), _scaler_ptr(scaler), _stream(stream)))
+
+
+def zero1_pingpong_finish(plan: Plan, shard_begin: int, shard_end: int, master, params, hp: AdamW,
+                          scaler: torch.Tensor, policy: LossScalePolicy, stream=None) -> None:
+    """End of a bucketed ping-pong attempt over shards [shard_begin,
+    shard_end): params restored if any bucket overflowed, scaler advanced."""
+    _, L, nv = _range(plan, shard_begin, shard_end)
+    _check_rc(load().zero1_pingpong_finish(
+        ctypes.byref(plan), shard_begin, shard_end, _pair("master", master, L),
+        _dev(params, torch.bfloat16, nv, "params"), ctypes.byref(hp.c_struct()), _scaler_ptr(scaler),
+        ctypes.byref(policy.c_struct()), _stream(stream)))
+
+
+class PingPongBuckets:
+    """One ping-pong attempt fed bucket by bucket over shards [shard_begin,
+    shard_end), with the copies (pairs of L-element fp32 tensors) and params
+    (nv elements) of the whole range.  bucket() takes offsets relative to the
+    range; finish() checks on the host that the attempt's buckets covered the
+    range once, then ends the attempt."""
+
+    def __init__(self, plan: Plan, shard_begin: int, shard_end: int, master, m, v, params, scaler: torch.Tensor,
+                 policy: LossScalePolicy, stream=None):
+        self.plan, self.sb, self.se = plan, shard_begin, shard_end
+        self.base, self.L, self.nv = _range(plan, shard_begin, shard_end)
+        if self.L == 0:
+            raise ValueError("empty or invalid shard range")
+        self.master, self.m, self.v, self.params = master, m, v, params
+        self.scaler, self.policy, self.stream = scaler, policy, stream
+        self._done = []
+
+    def bucket(self, begin: int, end: int, grads, hp: AdamW) -> None:
+        if not 0 <= begin < end <= self.L:
+            raise ValueError(f"bucket [{begin}, {end}) not inside the range [0, {self.L})")
+        params = self.params[begin:] if begin < self.nv else self.params[:0]
+        zero1_pingpong_bucket(self.plan, self.base + begin, self.base + end, grads,
+                              [x[begin:] for x in self.master], [x[begin:] for x in self.m],
+                              [x[begin:] for x in self.v], params, hp, self.scaler, self.stream)
+        self._done.append((begin, end))
+
+    def finish(self, hp: AdamW) -> None:
+        cover = sorted(self._done)
+        edge = 0
+        for b, e in cover:
+            if b != edge:
+                raise ValueError(f"the attempt's buckets do not cover the range once (at element {edge})")
+            edge = e
+        if edge != self.L:
+            raise ValueError(f"the attempt's buckets end at element {edge}, not {self.L}")
+        zero1_pingpong_finish(self.plan, self.sb, self.se, self.master, self.params, hp, self.scaler, self.policy,
+                              self.stream)
+        self._done = []
 
 
 def current_state(scaler: torch.Tensor, master, m, v):

@@ -325,6 +325,91 @@ extern "C" int zero1_step_dynamic(const zero1_plan_t *plan, int32_t shard_begin,
     return launch_status("dynamic step launch");
 }
 
+namespace {
+
+// The two copies of master/m/v (host arrays of two device pointers each).
+int load_pingpong(float *const *master, float *const *m, float *const *v, PingPong *s, const char *what)
+{
+    if (!master || !m || !v) return z1_fail(ZERO1_EINVAL, "%s: master, m and v arrays are NULL", what);
+    int rc;
+    for (int k = 0; k < 2; ++k) {
+        if (!master[k] || !m[k] || !v[k])
+            return z1_fail(ZERO1_EINVAL, "%s: copy %d of master, m or v is NULL", what, k);
+        if ((rc = check_natural(master[k], 4, "master")) || (rc = check_natural(m[k], 4, "m")) ||
+            (rc = check_natural(v[k], 4, "v")))
+            return rc;
+        s->master[k] = master[k];
+        s->mom[k] = m[k];
+        s->var[k] = v[k];
+    }
+    if (s->master[0] == s->master[1] || s->mom[0] == s->mom[1] || s->var[0] == s->var[1])
+        return z1_fail(ZERO1_EINVAL, "%s: the two copies of master, m or v are the same buffer", what);
+    return ZERO1_OK;
+}
+
+// Validate and launch the ping-pong kernel over L elements (nv real) whose
+// pointers all start at the range's first element.
+int launch_pingpong_range(const zero1_plan_t *plan, int64_t L, int64_t nv, const void *const *grads,
+                          float *const *master, float *const *m, float *const *v, void *params,
+                          const zero1_adamw_t *hp, zero1_scaler_t *scaler, cudaStream_t st, const char *what)
+{
+    int rc;
+    Z1Consts c;
+    if ((rc = dynamic_constants(hp, plan->M, &c)) != ZERO1_OK) return rc;
+    if ((rc = check_scaler_ptr(scaler)) != ZERO1_OK) return rc;
+    PingPong s{};
+    if ((rc = load_pingpong(master, m, v, &s, what)) != ZERO1_OK) return rc;
+    if (nv > 0 && !params)
+        return z1_fail(ZERO1_EINVAL, "%s: params must be non-NULL when the range holds parameters", what);
+    if ((rc = check_natural(params, 2, "params")) != ZERO1_OK) return rc;
+    GradPtrs g{};
+    if (nv > 0 && (rc = load_grads(plan, grads, &g, what)) != ZERO1_OK) return rc;
+    // one walk serves both copies: they must share the 16-byte phase
+    ArrayRef arr[ZERO1_MAX_REPLICAS + 7] = {{s.master[0], 4}, {s.mom[0], 4}, {s.var[0], 4}, {s.master[1], 4},
+                                            {s.mom[1], 4},    {s.var[1], 4}, {params, 2}};
+    const int M = plan->M;
+    for (int k = 0; k < M; ++k) arr[7 + k] = {g.p[k], 2};
+    const Walk w = make_walk(L, nv, arr, 7 + M);
+    uint16_t *pp = static_cast<uint16_t *>(params);
+    dispatch_m(M, [&](auto mt) {
+        constexpr int MT = decltype(mt)::value;
+        const int grid = grid_for(k_fused_step_pingpong<MT>, work_of(w));
+        k_fused_step_pingpong<MT><<<grid, kBlock, 0, st>>>(g, M, s, pp, w, c, scaler);
+    });
+    return launch_status(what);
+}
+
+// Validate and launch the end of a ping-pong attempt over L elements (nv
+// real): params restored after an overflow, then the scaler update.
+int launch_pingpong_finish(int64_t L, int64_t nv, float *const *master, void *params, const zero1_adamw_t *hp,
+                           zero1_scaler_t *scaler, const zero1_loss_scale_policy_t *policy, cudaStream_t st,
+                           const char *what)
+{
+    int rc;
+    if ((rc = check_scaler_ptr(scaler)) != ZERO1_OK || (rc = check_policy(policy)) != ZERO1_OK) return rc;
+    if (!hp) return z1_fail(ZERO1_EINVAL, "hyperparameters are NULL");
+    if (!master || !master[0] || !master[1])
+        return z1_fail(ZERO1_EINVAL, "%s: the master copies are NULL", what);
+    if (master[0] == master[1]) return z1_fail(ZERO1_EINVAL, "%s: the two master copies are the same buffer", what);
+    if ((rc = check_natural(master[0], 4, "master")) || (rc = check_natural(master[1], 4, "master")))
+        return rc;
+    if (nv > 0 && !params)
+        return z1_fail(ZERO1_EINVAL, "%s: params must be non-NULL when the range holds parameters", what);
+    if ((rc = check_natural(params, 2, "params")) != ZERO1_OK) return rc;
+    PingPong s{};
+    s.master[0] = master[0];
+    s.master[1] = master[1];
+    const ArrayRef arr[3] = {{master[0], 4}, {master[1], 4}, {params, 2}};
+    const Walk w = make_walk(L, nv, arr, 3);
+    const int grid = grid_for(k_restore_params, work_of(w));
+    k_restore_params<<<grid, kBlock, 0, st>>>(s, static_cast<uint16_t *>(params), w, scaler);
+    const ScalePolicy pol{policy->factor, policy->window, policy->hysteresis, policy->min_scale};
+    k_scaler_update<<<1, 32, 0, st>>>(scaler, pol, hp->global_batch, hp->beta1, hp->beta2, 1);
+    return launch_status(what);
+}
+
+}  // namespace
+
 extern "C" int zero1_step_dynamic_pingpong(const zero1_plan_t *plan, int32_t shard_begin, int32_t shard_end,
                                            const void *const *grads, float *const *master, float *const *m,
                                            float *const *v, void *params, const zero1_adamw_t *hp,
@@ -334,46 +419,41 @@ extern "C" int zero1_step_dynamic_pingpong(const zero1_plan_t *plan, int32_t sha
     Z1Range r;
     int rc = z1_range(plan, shard_begin, shard_end, &r);
     if (rc != ZERO1_OK) return rc;
-    Z1Consts c;
-    if ((rc = dynamic_constants(hp, plan->M, &c)) != ZERO1_OK) return rc;
-    if ((rc = check_scaler_ptr(scaler)) != ZERO1_OK || (rc = check_policy(policy)) != ZERO1_OK) return rc;
-    if (!master || !m || !v) return z1_fail(ZERO1_EINVAL, "ping-pong step: master, m and v arrays are NULL");
-    PingPong s{};
-    for (int k = 0; k < 2; ++k) {
-        if (!master[k] || !m[k] || !v[k])
-            return z1_fail(ZERO1_EINVAL, "ping-pong step: copy %d of master, m or v is NULL", k);
-        if ((rc = check_natural(master[k], 4, "master")) || (rc = check_natural(m[k], 4, "m")) ||
-            (rc = check_natural(v[k], 4, "v")))
-            return rc;
-        s.master[k] = master[k];
-        s.mom[k] = m[k];
-        s.var[k] = v[k];
-    }
-    if (s.master[0] == s.master[1] || s.mom[0] == s.mom[1] || s.var[0] == s.var[1])
-        return z1_fail(ZERO1_EINVAL, "ping-pong step: the two copies of master, m or v are the same buffer");
-    if (r.nv > 0 && !params)
-        return z1_fail(ZERO1_EINVAL, "ping-pong step: params must be non-NULL when the range holds parameters");
-    if ((rc = check_natural(params, 2, "params")) != ZERO1_OK) return rc;
-    GradPtrs g{};
-    if (r.nv > 0 && (rc = load_grads(plan, grads, &g, "ping-pong step")) != ZERO1_OK) return rc;
-    // one walk serves both copies: they must share the 16-byte phase
-    ArrayRef arr[ZERO1_MAX_REPLICAS + 7] = {{s.master[0], 4}, {s.mom[0], 4}, {s.var[0], 4}, {s.master[1], 4},
-                                            {s.mom[1], 4},    {s.var[1], 4}, {params, 2}};
-    const int M = plan->M;
-    for (int k = 0; k < M; ++k) arr[7 + k] = {g.p[k], 2};
-    const Walk w = make_walk(r.L, r.nv, arr, 7 + M);
+    if ((rc = check_policy(policy)) != ZERO1_OK) return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    uint16_t *pp = static_cast<uint16_t *>(params);
-    dispatch_m(M, [&](auto mt) {
-        constexpr int MT = decltype(mt)::value;
-        const int grid = grid_for(k_fused_step_pingpong<MT>, work_of(w));
-        k_fused_step_pingpong<MT><<<grid, kBlock, 0, st>>>(g, M, s, pp, w, c, scaler);
-    });
-    const int rgrid = grid_for(k_restore_params, work_of(w));
-    k_restore_params<<<rgrid, kBlock, 0, st>>>(s, pp, w, scaler);
-    const ScalePolicy pol{policy->factor, policy->window, policy->hysteresis, policy->min_scale};
-    k_scaler_update<<<1, 32, 0, st>>>(scaler, pol, hp->global_batch, hp->beta1, hp->beta2, 1);
-    return launch_status("ping-pong step launch");
+    if ((rc = launch_pingpong_range(plan, r.L, r.nv, grads, master, m, v, params, hp, scaler, st,
+                                    "ping-pong step")) != ZERO1_OK)
+        return rc;
+    return launch_pingpong_finish(r.L, r.nv, master, params, hp, scaler, policy, st, "ping-pong step");
+}
+
+extern "C" int zero1_pingpong_bucket(const zero1_plan_t *plan, int64_t elem_begin, int64_t elem_end,
+                                     const void *const *grads, float *const *master, float *const *m,
+                                     float *const *v, void *params, const zero1_adamw_t *hp,
+                                     zero1_scaler_t *scaler, zero1_stream_t stream)
+{
+    int rc = z1_check_plan(plan);
+    if (rc != ZERO1_OK) return rc;
+    if (elem_begin < 0 || elem_end > plan->padded_n || elem_begin >= elem_end)
+        return z1_fail(ZERO1_EINVAL, "bucket [%lld, %lld) not inside [0, %lld)", (long long)elem_begin,
+                       (long long)elem_end, (long long)plan->padded_n);
+    const int64_t L = elem_end - elem_begin;
+    int64_t nv = plan->n - elem_begin;
+    nv = nv < 0 ? 0 : (nv > L ? L : nv);
+    return launch_pingpong_range(plan, L, nv, grads, master, m, v, params, hp, scaler,
+                                 reinterpret_cast<cudaStream_t>(stream), "ping-pong bucket");
+}
+
+extern "C" int zero1_pingpong_finish(const zero1_plan_t *plan, int32_t shard_begin, int32_t shard_end,
+                                     float *const *master, void *params, const zero1_adamw_t *hp,
+                                     zero1_scaler_t *scaler, const zero1_loss_scale_policy_t *policy,
+                                     zero1_stream_t stream)
+{
+    Z1Range r;
+    int rc = z1_range(plan, shard_begin, shard_end, &r);
+    if (rc != ZERO1_OK) return rc;
+    return launch_pingpong_finish(r.L, r.nv, master, params, hp, scaler, policy,
+                                  reinterpret_cast<cudaStream_t>(stream), "ping-pong finish");
 }
 
 // ------------------------------------------- step without caller allocation --

@@ -2,7 +2,9 @@
 count, size, alignment unit, shard sub-range, the element phase of every
 buffer (so the vector head, the per-element fallback and the ragged tail all
 occur), hyperparameters and step, and every entry point that computes the
-step (one-shot, prepared, bucketed, shared-memory staged, dynamic)."""
+step (one-shot, prepared, bucketed, shared-memory staged, dynamic, ping-pong
+whole and in buckets, and the copy-engine staged step with state or
+gradients in pinned host memory)."""
 import numpy as np
 import pytest
 import torch
@@ -13,7 +15,8 @@ from gpu_helpers import assert_bf16_bits, assert_f32_bits, f32, oracle_hp, u16
 
 pytestmark = pytest.mark.gpu
 
-ENTRIES = ["fused", "prepared", "bucket", "tma", "dynamic"]
+ENTRIES = ["fused", "prepared", "bucket", "tma", "dynamic", "pingpong", "pingpong_buckets", "staged_state",
+           "staged_grads"]
 
 
 def _buf(numel, dtype, phase, dev):
@@ -22,7 +25,18 @@ def _buf(numel, dtype, phase, dev):
     return torch.zeros(numel + 8, dtype=dtype, device=dev)[phase:phase + numel]
 
 
-@pytest.mark.parametrize("case", range(80))
+def _pinned_like(t, phase):
+    """A pinned host copy of t starting `phase` elements into its allocation."""
+    h = torch.zeros(t.numel() + 8, dtype=t.dtype).pin_memory()[phase:phase + t.numel()]
+    h.copy_(t.cpu())
+    return h
+
+
+def _cuts(rng, L):
+    return sorted({0, L, *[int(x) for x in rng.integers(0, L + 1, int(rng.integers(1, 6)))]})
+
+
+@pytest.mark.parametrize("case", range(126))
 def test_random_configuration(cuda_device, case):
     dev = cuda_device
     rng = np.random.default_rng(20_000 + case)
@@ -72,8 +86,34 @@ def test_random_configuration(cuda_device, case):
         z.zero1_scaler_init(scaler, policy, hp)
         sums = _buf(L, torch.float32, ph(), dev)
         z.zero1_step_dynamic(plan, sb, se, grads, *state, params, hp, scaler, policy, sums)
+    elif entry in ("pingpong", "pingpong_buckets"):
+        policy = z.LossScalePolicy(initial_scale=S, window=1000, hysteresis=2)
+        scaler = z.new_scaler(dev)
+        z.zero1_scaler_init(scaler, policy, hp)
+        pairs = [[t, _buf(L, torch.float32, ph(), dev).fill_(float("nan"))] for t in state]
+        if entry == "pingpong":
+            z.zero1_step_dynamic_pingpong(plan, sb, se, grads, *pairs, params, hp, scaler, policy)
+        else:
+            attempt = z.PingPongBuckets(plan, sb, se, *pairs, params, scaler, policy)
+            cuts = _cuts(rng, L)
+            for i in rng.permutation(len(cuts) - 1):
+                e0, e1 = cuts[i], cuts[i + 1]
+                k = max(0, min(nv, e1) - e0)
+                attempt.bucket(e0, e1, [g[e0:e0 + k] for g in grads], hp)
+            attempt.finish(hp)
+        state = list(z.current_state(scaler, *pairs))
+    elif entry == "staged_state":
+        state = [_pinned_like(t, ph()) for t in state]
+        z.HostStreamedStep(plan, sb, se, grads, *state, params, chunk_elems=int(rng.integers(1, 6000)))(hp)
+    elif entry == "staged_grads":
+        grads = [_pinned_like(g, ph()) for g in grads]
+        host_p = _pinned_like(params, ph())
+        z.HostStreamedStep(plan, sb, se, grads, *state, params, chunk_elems=int(rng.integers(1, 6000)),
+                           params_host=host_p)(hp)
+        torch.cuda.synchronize()
+        assert_bf16_bits(u16(host_p), u16(params), f"case {case}: params copied to host")
     else:  # buckets over [base, base + L) in global element coordinates
-        cuts = sorted({0, L, *[int(x) for x in rng.integers(0, L + 1, int(rng.integers(1, 6)))]})
+        cuts = _cuts(rng, L)
         for e0, e1 in zip(cuts[:-1], cuts[1:]):
             k = max(0, min(nv, e1) - e0)
             z.zero1_step_bucket(plan, base + e0, base + e1, [g[e0:e0 + k] for g in grads],

@@ -60,6 +60,7 @@ k_checksum16(const uint16_t *__restrict__ u, const Walk w, unsigned long long *o
 
 extern "C" int zero1_checksum(const void *data, int64_t nbytes, uint64_t *out, zero1_stream_t stream)
 {
+    Z1Trace trace("zero1_checksum");
     if (!out) return z1_fail(ZERO1_EINVAL, "checksum: out is NULL");
     if (((uintptr_t)out & 7u) != 0) return z1_fail(ZERO1_EALIGN, "checksum: out is not 8-byte aligned");
     if (nbytes < 0 || (nbytes & 1)) return z1_fail(ZERO1_EINVAL, "checksum: %lld bytes is not a whole number of "

@@ -269,6 +269,7 @@ int check_scaler_ptr(const zero1_scaler_t *sc)
 extern "C" int zero1_scaler_init(zero1_scaler_t *scaler, const zero1_loss_scale_policy_t *policy,
                                  const zero1_adamw_t *hp, zero1_stream_t stream)
 {
+    Z1Trace trace("zero1_scaler_init");
     int rc;
     if ((rc = check_scaler_ptr(scaler)) != ZERO1_OK || (rc = check_policy(policy)) != ZERO1_OK) return rc;
     if (!hp) return z1_fail(ZERO1_EINVAL, "hyperparameters are NULL");
@@ -286,6 +287,7 @@ extern "C" int zero1_step_dynamic(const zero1_plan_t *plan, int32_t shard_begin,
                                   const zero1_adamw_t *hp, zero1_scaler_t *scaler,
                                   const zero1_loss_scale_policy_t *policy, float *sums, zero1_stream_t stream)
 {
+    Z1Trace trace("zero1_step_dynamic");
     Z1Range r;
     int rc = z1_range(plan, shard_begin, shard_end, &r);
     if (rc != ZERO1_OK) return rc;
@@ -416,6 +418,7 @@ extern "C" int zero1_step_dynamic_pingpong(const zero1_plan_t *plan, int32_t sha
                                            zero1_scaler_t *scaler, const zero1_loss_scale_policy_t *policy,
                                            zero1_stream_t stream)
 {
+    Z1Trace trace("zero1_step_dynamic_pingpong");
     Z1Range r;
     int rc = z1_range(plan, shard_begin, shard_end, &r);
     if (rc != ZERO1_OK) return rc;
@@ -432,6 +435,7 @@ extern "C" int zero1_pingpong_bucket(const zero1_plan_t *plan, int64_t elem_begi
                                      float *const *v, void *params, const zero1_adamw_t *hp,
                                      zero1_scaler_t *scaler, zero1_stream_t stream)
 {
+    Z1Trace trace("zero1_pingpong_bucket");
     int rc = z1_check_plan(plan);
     if (rc != ZERO1_OK) return rc;
     if (elem_begin < 0 || elem_end > plan->padded_n || elem_begin >= elem_end)
@@ -449,6 +453,7 @@ extern "C" int zero1_pingpong_finish(const zero1_plan_t *plan, int32_t shard_beg
                                      zero1_scaler_t *scaler, const zero1_loss_scale_policy_t *policy,
                                      zero1_stream_t stream)
 {
+    Z1Trace trace("zero1_pingpong_finish");
     Z1Range r;
     int rc = z1_range(plan, shard_begin, shard_end, &r);
     if (rc != ZERO1_OK) return rc;
@@ -498,6 +503,7 @@ extern "C" int zero1_step_dynamic_noalloc(const zero1_plan_t *plan, int32_t shar
                                           void *params, const zero1_adamw_t *hp, zero1_scaler_t *scaler,
                                           const zero1_loss_scale_policy_t *policy, zero1_stream_t stream)
 {
+    Z1Trace trace("zero1_step_dynamic_noalloc");
     Z1Range r;
     int rc = z1_range(plan, shard_begin, shard_end, &r);
     if (rc != ZERO1_OK) return rc;

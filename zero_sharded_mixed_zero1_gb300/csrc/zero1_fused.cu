@@ -255,6 +255,7 @@ extern "C" int zero1_reduce_scatter_adamw_allgather(const zero1_plan_t *plan, in
                                                     const zero1_adamw_t *hp, uint32_t *overflow_flag,
                                                     int32_t skip_if_flag, zero1_stream_t stream)
 {
+    Z1Trace trace("zero1_reduce_scatter_adamw_allgather");
     Z1Range r;
     int rc = z1_range(plan, shard_begin, shard_end, &r);
     if (rc != ZERO1_OK) return rc;
@@ -266,6 +267,7 @@ extern "C" int zero1_step_bucket(const zero1_plan_t *plan, int64_t elem_begin, i
                                  const void *const *grads, float *master, float *m, float *v, void *params,
                                  const zero1_adamw_t *hp, uint32_t *overflow_flag, zero1_stream_t stream)
 {
+    Z1Trace trace("zero1_step_bucket");
     int rc = z1_check_plan(plan);
     if (rc != ZERO1_OK) return rc;
     if (elem_begin < 0 || elem_end > plan->padded_n || elem_begin >= elem_end)

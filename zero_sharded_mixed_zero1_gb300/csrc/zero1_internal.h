@@ -2,9 +2,20 @@
 // (library-internal; not part of the C ABI).
 #pragma once
 
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 #include "zero1.h"
+
+// An NVTX range over one C-ABI call, named after the entry point, so that
+// Nsight tools can select a call's kernels and copies (ncu --nvtx-include
+// "<name>/").  With no tool attached the range calls do nothing.
+struct Z1Trace {
+    explicit Z1Trace(const char *name) { nvtxRangePushA(name); }
+    ~Z1Trace() { nvtxRangePop(); }
+    Z1Trace(const Z1Trace &) = delete;
+    Z1Trace &operator=(const Z1Trace &) = delete;
+};
 
 // The per-step constants of the AdamW update, evaluated once on the host
 // ("CS336 Lecture 7: Parallelism 1" naive DP equation for inv = 1/(B*S);

@@ -189,6 +189,7 @@ k_allreduce(const __grid_constant__ GradPtrs g, const __grid_constant__ OutPtrs 
 extern "C" int zero1_overflow_check(const zero1_plan_t *plan, int32_t shard_begin, int32_t shard_end,
                                     const void *const *grads, uint32_t *flag, zero1_stream_t stream)
 {
+    Z1Trace trace("zero1_overflow_check");
     Z1Range r;
     int rc = z1_range(plan, shard_begin, shard_end, &r);
     if (rc != ZERO1_OK) return rc;
@@ -213,6 +214,7 @@ extern "C" int zero1_overflow_check(const zero1_plan_t *plan, int32_t shard_begi
 extern "C" int dp_allreduce(const zero1_plan_t *plan, const void *const *grads_in, void *const *outs,
                             float scale, int32_t out_dtype, zero1_stream_t stream)
 {
+    Z1Trace trace("dp_allreduce");
     int rc = z1_check_plan(plan);
     if (rc != ZERO1_OK) return rc;
     if (out_dtype != ZERO1_DTYPE_BF16 && out_dtype != ZERO1_DTYPE_F32)
@@ -259,6 +261,7 @@ extern "C" int zero1_reduce_scatter(const zero1_plan_t *plan, int32_t shard_begi
                                     const void *const *grads, float scale, int32_t out_dtype, void *out,
                                     uint32_t *flag, zero1_stream_t stream)
 {
+    Z1Trace trace("zero1_reduce_scatter");
     Z1Range r;
     int rc = z1_range(plan, shard_begin, shard_end, &r);
     if (rc != ZERO1_OK) return rc;
@@ -293,6 +296,7 @@ extern "C" int zero1_adamw_update(const zero1_plan_t *plan, int32_t shard_begin,
                                   const float *gin, float *master, float *m, float *v,
                                   const zero1_adamw_t *hp, zero1_stream_t stream)
 {
+    Z1Trace trace("zero1_adamw_update");
     Z1Range r;
     int rc = z1_range(plan, shard_begin, shard_end, &r);
     if (rc != ZERO1_OK) return rc;
@@ -314,6 +318,7 @@ extern "C" int zero1_adamw_update(const zero1_plan_t *plan, int32_t shard_begin,
 extern "C" int zero1_all_gather(const zero1_plan_t *plan, int32_t shard_begin, int32_t shard_end,
                                 const float *master, void *params, zero1_stream_t stream)
 {
+    Z1Trace trace("zero1_all_gather");
     Z1Range r;
     int rc = z1_range(plan, shard_begin, shard_end, &r);
     if (rc != ZERO1_OK) return rc;
@@ -331,6 +336,7 @@ extern "C" int zero1_all_gather(const zero1_plan_t *plan, int32_t shard_begin, i
 extern "C" int zero1_all_gather_shards(const zero1_plan_t *plan, const void *shards, void *const *outs,
                                        zero1_stream_t stream)
 {
+    Z1Trace trace("zero1_all_gather_shards");
     int rc = z1_check_plan(plan);
     if (rc != ZERO1_OK) return rc;
     if (!shards || !outs) return z1_fail(ZERO1_EINVAL, "all-gather shards: NULL argument");

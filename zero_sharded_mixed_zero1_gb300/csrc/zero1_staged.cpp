@@ -126,6 +126,7 @@ void release(zero1_staged_t *h)
 extern "C" int zero1_staged_create(const zero1_plan_t *plan, int32_t shard_begin, int32_t shard_end,
                                    int32_t what, int64_t chunk_elems, zero1_staged_t **out)
 {
+    Z1Trace trace("zero1_staged_create");
     if (!out) return z1_fail(ZERO1_EINVAL, "staged create: out is NULL");
     *out = nullptr;
     int rc;
@@ -198,6 +199,7 @@ extern "C" int zero1_staged_step(zero1_staged_t *h, const void *const *grads, fl
                                  float *v, void *params, void *params_host, const zero1_adamw_t *hp,
                                  uint32_t *overflow_flag, zero1_stream_t stream)
 {
+    Z1Trace trace("zero1_staged_step");
     if (!h) return z1_fail(ZERO1_EINVAL, "staged step: handle is NULL");
     int rc;
     int dev = -1;

@@ -257,6 +257,7 @@ extern "C" int zero1_step_tma(const zero1_plan_t *plan, int32_t shard_begin, int
                               const zero1_adamw_t *hp, uint32_t *overflow_flag, int32_t skip_if_flag,
                               zero1_stream_t stream)
 {
+    Z1Trace trace("zero1_step_tma");
     Z1Range r;
     int rc = z1_range(plan, shard_begin, shard_end, &r);
     if (rc != ZERO1_OK) return rc;

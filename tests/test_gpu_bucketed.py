@@ -112,3 +112,51 @@ def test_llama_layers_in_pages_sized_buckets(cuda_device):
     assert_bf16_bits(u16(pb[idx]), op, "params samples vs oracle")
     del grads, a, b
     torch.cuda.empty_cache()
+
+
+def test_per_tensor_weight_decay_through_buckets(cuda_device):
+    """Weight decay chosen per tensor (none on the norm vectors), done as one
+    bucket per tensor with that tensor's hyperparameters: each tensor's
+    elements equal the oracle's step over that tensor's range with its own
+    weight decay; the padding after the last tensor takes the last call's."""
+    dev = cuda_device
+    d, f = 64, 224          # a small Llama-style layer: norms, attention and MLP matrices
+    numels = [d, d * d, d * d // 4, d * d // 4, d * d, d, d * f, d * f, f * d, d]
+    norms = {0, 5, 9}
+    n = sum(numels)
+    M = 4
+    plan = z.zero1_plan(n, M, 8)
+    P = plan.padded_n
+    state = make_state(n, P, 401, dev, nonzero_moments=True)
+    o = [f32(t) for t in state]
+    params = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+    want_p = np.zeros(n, np.uint16)
+    offsets = np.concatenate([[0], np.cumsum(numels)])
+    start = [x.copy() for x in o]
+    for t in (1, 2, 3):
+        grads = make_grads(M, n, 1e-2, 402, t, dev)
+        g_np = [u16(g) for g in grads]
+        ranges = [(int(offsets[i]), int(offsets[i + 1]), i in norms) for i in range(len(numels))]
+        ranges[-1] = (ranges[-1][0], P, ranges[-1][2])          # the last call also covers the padding
+        for b, e, is_norm in ranges:
+            hp = z.AdamW(global_batch=64, step=t, weight_decay=0.0 if is_norm else 0.1)
+            k = max(0, min(n, e) - b)
+            z.zero1_step_bucket(plan, b, e, [g[b:b + k] for g in grads], *[s[b:] for s in state], params[b:], hp)
+            seg = [x[b:b + k] for x in g_np]
+            o_seg = [x[b:e].copy() for x in o]
+            p_seg = np.zeros(k, np.uint16)
+            oracle.zero1_step(seg, k, *o_seg, p_seg, oracle_hp(hp))
+            for x, y in zip(o, o_seg):
+                x[b:e] = y
+            want_p[b:b + k] = p_seg
+        torch.cuda.synchronize()
+        for x, y, what in zip(state, o, ("master", "m", "v")):
+            assert_f32_bits(f32(x), y, f"{what} t={t}")
+        assert_bf16_bits(u16(params), want_p, f"params t={t}")
+        if t == 1:
+            # the choice mattered: the first norm under the uniform decay differs
+            b, e = int(offsets[0]), int(offsets[1])
+            uni = [x[b:e].copy() for x in start]
+            oracle.zero1_step([x[b:e] for x in g_np], e - b, *uni, np.zeros(e - b, np.uint16),
+                              oracle_hp(z.AdamW(global_batch=64, step=1, weight_decay=0.1)))
+            assert not np.array_equal(uni[0], o[0][b:e])

@@ -349,3 +349,26 @@ def test_pipelined_kernel_above_the_small_range_threshold(cuda_device, M):
         assert_f32_bits(f32(m), o[1], f"m t={t}")
         assert_f32_bits(f32(v), o[2], f"v t={t}")
         assert_bf16_bits(u16(params), want, f"params t={t}")
+
+
+@pytest.mark.parametrize("M,n,align,S", [(8, 2048 * 11 + 5, 128, 65536.0), (4, 30_001, 1, 1.0)])
+def test_pages_deepspeed_optimizer_block(cuda_device, M, n, align, S):
+    """The AdamW block of the pages' DeepSpeed configuration ("五维并行实战" 4.2:
+    lr 0.001, betas (0.9, 0.999), eps 1e-8, weight_decay 0.01), over ten
+    steps with and without the fp16 block's loss scale: bit for bit the
+    oracle at every step."""
+    dev = cuda_device
+    plan = z.zero1_plan(n, M, align)
+    state = make_state(n, plan.padded_n, 600 + M, dev)
+    o = [f32(t) for t in state]
+    params = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+    for t in range(1, 11):
+        hp = z.AdamW(lr=0.001, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, loss_scale=S,
+                     global_batch=1024, step=t)
+        grads = make_grads(M, n, 1e-3 * S, 601 + M, t, dev)
+        z.zero1_reduce_scatter_adamw_allgather(plan, 0, M, grads, *state, params, hp)
+        torch.cuda.synchronize()
+        want_p = oracle_step(plan, [u16(g) for g in grads], *o, oracle_hp(hp))
+        for x, y, what in zip(state, o, ("master", "m", "v")):
+            assert_f32_bits(f32(x), y, f"{what} t={t}")
+        assert_bf16_bits(u16(params), want_p, f"params t={t}")

@@ -168,6 +168,33 @@ def test_staged_handle_rejects_bad_arguments(lib):
     assert lib.zero1_staged_destroy(None) == 0
 
 
+@no_gpu
+def test_pingpong_entries_reject_bad_arguments(lib):
+    """The ping-pong step, bucket and finish validate the two state copies,
+    the policy, the range and the hyperparameters before any CUDA call."""
+    plan = z.zero1_plan(1000, 2, 8)
+    P = ctypes.byref(plan)
+    g = _ptr_array([A + 65536, A + 131072])
+    two = lambda a, b: _ptr_array([a, b])
+    pol = ctypes.byref(z.LossScalePolicy().c_struct())
+    hp = ctypes.byref(_hp(global_batch=64))
+    sc = A + (1 << 22)
+    w, m, v = two(A, A + 8192), two(A + 16384, A + 24576), two(A + 32768, A + 40960)
+    step = lambda *a: lib.zero1_step_dynamic_pingpong(P, 0, 2, g, *a)
+    assert step(two(A, A), m, v, A + 49152, hp, sc, pol, None) == -1             # one buffer for both copies
+    assert step(two(A, A + 8194), m, v, A + 49152, hp, sc, pol, None) == -2      # copy 1 misaligned
+    assert step(None, m, v, A + 49152, hp, sc, pol, None) == -1
+    assert step(w, m, v, A + 49152, hp, sc + 4, pol, None) == -2                # scaler not 8-byte aligned
+    bad_pol = ctypes.byref(z.LossScalePolicy(factor=1.0).c_struct())
+    assert step(w, m, v, A + 49152, hp, sc, bad_pol, None) == -1
+    assert lib.zero1_pingpong_bucket(P, 500, 2000, g, w, m, v, A + 49152, hp, sc, None) == -1   # past P
+    assert lib.zero1_pingpong_bucket(P, 10, 10, g, w, m, v, A + 49152, hp, sc, None) == -1     # empty
+    bad_hp = ctypes.byref(_hp(beta1=1.0, global_batch=64))
+    assert lib.zero1_pingpong_finish(P, 0, 2, w, A + 49152, bad_hp, sc, pol, None) == -1
+    assert lib.zero1_pingpong_finish(P, 0, 2, two(A, A), A + 49152, hp, sc, pol, None) == -1
+    assert lib.zero1_pingpong_finish(P, 0, 3, w, A + 49152, hp, sc, pol, None) == -1         # bad range
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     import zero_sharded_mixed_zero1_gb300._lib as L
     monkeypatch.setattr(L, "_lib", None)

@@ -383,13 +383,14 @@ int launch_pingpong_range(const zero1_plan_t *plan, int64_t L, int64_t nv, const
 
 // Validate and launch the end of a ping-pong attempt over L elements (nv
 // real): params restored after an overflow, then the scaler update.
-int launch_pingpong_finish(int64_t L, int64_t nv, float *const *master, void *params, const zero1_adamw_t *hp,
-                           zero1_scaler_t *scaler, const zero1_loss_scale_policy_t *policy, cudaStream_t st,
-                           const char *what)
+int launch_pingpong_finish(const zero1_plan_t *plan, int64_t L, int64_t nv, float *const *master, void *params,
+                           const zero1_adamw_t *hp, zero1_scaler_t *scaler, const zero1_loss_scale_policy_t *policy,
+                           cudaStream_t st, const char *what)
 {
     int rc;
+    Z1Consts c;  // validates the betas and the global batch the scaler update uses
+    if ((rc = dynamic_constants(hp, plan->M, &c)) != ZERO1_OK) return rc;
     if ((rc = check_scaler_ptr(scaler)) != ZERO1_OK || (rc = check_policy(policy)) != ZERO1_OK) return rc;
-    if (!hp) return z1_fail(ZERO1_EINVAL, "hyperparameters are NULL");
     if (!master || !master[0] || !master[1])
         return z1_fail(ZERO1_EINVAL, "%s: the master copies are NULL", what);
     if (master[0] == master[1]) return z1_fail(ZERO1_EINVAL, "%s: the two master copies are the same buffer", what);
@@ -427,7 +428,7 @@ extern "C" int zero1_step_dynamic_pingpong(const zero1_plan_t *plan, int32_t sha
     if ((rc = launch_pingpong_range(plan, r.L, r.nv, grads, master, m, v, params, hp, scaler, st,
                                     "ping-pong step")) != ZERO1_OK)
         return rc;
-    return launch_pingpong_finish(r.L, r.nv, master, params, hp, scaler, policy, st, "ping-pong step");
+    return launch_pingpong_finish(plan, r.L, r.nv, master, params, hp, scaler, policy, st, "ping-pong step");
 }
 
 extern "C" int zero1_pingpong_bucket(const zero1_plan_t *plan, int64_t elem_begin, int64_t elem_end,
@@ -457,7 +458,7 @@ extern "C" int zero1_pingpong_finish(const zero1_plan_t *plan, int32_t shard_beg
     Z1Range r;
     int rc = z1_range(plan, shard_begin, shard_end, &r);
     if (rc != ZERO1_OK) return rc;
-    return launch_pingpong_finish(r.L, r.nv, master, params, hp, scaler, policy,
+    return launch_pingpong_finish(plan, r.L, r.nv, master, params, hp, scaler, policy,
                                   reinterpret_cast<cudaStream_t>(stream), "ping-pong finish");
 }
 

@@ -143,6 +143,7 @@ def load() -> ctypes.CDLL:
         "zero1_device_status": [vp, i32],
         "zero1_checksum": [vp, i64, vp, vp],
         "zero1_step_dynamic": [P, i32, i32, vp, vp, vp, vp, vp, A, vp, ctypes.POINTER(_PolicyStruct), vp, vp],
+        "zero1_step_dynamic_noalloc": [P, i32, i32, vp, vp, vp, vp, vp, A, vp, ctypes.POINTER(_PolicyStruct), vp],
         "zero1_step_dynamic_pingpong": [P, i32, i32, vp, vp, vp, vp, vp, A, vp, ctypes.POINTER(_PolicyStruct), vp],
         "zero1_pingpong_bucket": [P, i64, i64, vp, vp, vp, vp, vp, A, vp, vp],
         "zero1_pingpong_finish": [P, i32, i32, vp, vp, A, vp, ctypes.POINTER(_PolicyStruct), vp],
@@ -497,13 +498,7 @@ def zero1_step_dynamic_noalloc(plan: Plan, shard_begin: int, shard_end: int, gra
     """zero1_step_dynamic without a caller-provided workspace (the library's
     built-in 64 MiB array; ranges of at most ZERO1_NOALLOC_MAX_ELEMS
     elements).  For callers that cannot allocate device memory."""
-    lib = load()
-    fn = lib.zero1_step_dynamic_noalloc
-    if fn.argtypes is None:
-        vp, i32 = ctypes.c_void_p, ctypes.c_int32
-        fn.argtypes = [ctypes.POINTER(Plan), i32, i32, vp, vp, vp, vp, vp, ctypes.POINTER(_AdamWStruct), vp,
-                       ctypes.POINTER(_PolicyStruct), vp]
-        fn.restype = ctypes.c_int
+    fn = load().zero1_step_dynamic_noalloc
     _replicas(plan, grads, "grads")
     _, L, nv = _range(plan, shard_begin, shard_end)
     _check_rc(fn(ctypes.byref(plan), shard_begin, shard_end, _ptrs(grads, torch.bfloat16, nv, "grads"),

@@ -78,3 +78,50 @@ def test_dynamic_scaler_resumes(cuda_device, tmp_path):
     assert torch.equal(p.view(torch.int16), pref.view(torch.int16))
     assert z.scaler_state(sc) == z.scaler_state(sref)
     assert z.scaler_state(sc)["skipped"] == 2
+
+
+def test_pingpong_resumes_from_the_current_copy(cuda_device, tmp_path):
+    """A ping-pong checkpoint is the scaler (its `current` field included) and
+    the copy it names; the other copy is not saved.  On load the state goes
+    into the copy the saved scaler names, and the run continues bit for bit
+    as if never interrupted, skipped attempts included."""
+    dev = cuda_device
+    M, n = 8, 70_001
+    plan = z.zero1_plan(n, M, 8)
+    P = plan.padded_n
+    policy = z.LossScalePolicy(initial_scale=512.0, window=2, hysteresis=1)
+    hp = z.AdamW(global_batch=64, step=1)
+    grads = [make_grads(M, n, 1e-3 * 512, 61, t, dev) for t in range(9)]
+    grads[3][2][11] = float("inf")
+    grads[7][5][13] = float("nan")
+
+    def fresh():
+        st = make_state(n, P, 60, dev, nonzero_moments=True)
+        pairs = [[x, torch.zeros_like(x)] for x in st]
+        sc = z.new_scaler(dev)
+        z.zero1_scaler_init(sc, policy, hp)
+        return pairs, sc, st[0][:n].to(torch.bfloat16)
+
+    ref, sref, pref = fresh()
+    for k in range(9):
+        z.zero1_step_dynamic_pingpong(plan, 0, M, grads[k], *ref, pref, hp, sref, policy)
+    run, srun, prun = fresh()
+    for k in range(5):
+        z.zero1_step_dynamic_pingpong(plan, 0, M, grads[k], *run, prun, hp, srun, policy)
+    cur = z.current_state(srun, *run)
+    torch.save({"state": [x.cpu() for x in cur], "scaler": srun.cpu(), "params": prun.cpu()}, tmp_path / "pp.pt")
+    ck = torch.load(tmp_path / "pp.pt")
+    sc = ck["scaler"].to(dev)
+    k_cur = z.scaler_state(sc)["current"]
+    pairs = [[torch.full((P,), float("nan"), device=dev) for _ in range(2)] for _ in range(3)]
+    for pair, saved in zip(pairs, ck["state"]):
+        pair[k_cur].copy_(saved)
+    p = ck["params"].to(dev)
+    for k in range(5, 9):
+        z.zero1_step_dynamic_pingpong(plan, 0, M, grads[k], *pairs, p, hp, sc, policy)
+    torch.cuda.synchronize()
+    for a, b in zip(z.current_state(sc, *pairs), z.current_state(sref, *ref)):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    assert torch.equal(p.view(torch.int16), pref.view(torch.int16))
+    assert z.scaler_state(sc) == z.scaler_state(sref)
+    assert z.scaler_state(sc)["skipped"] == 2

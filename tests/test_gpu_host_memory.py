@@ -215,3 +215,22 @@ def test_staged_chunk_boundaries(cuda_device, L_n, M, chunk):
     step.close()
     c = (chunk + 7) // 8 * 8
     assert cuts == list(range(0, L, c)) + [L]
+
+
+def test_staged_step_close(cuda_device):
+    """close() waits for the queued work and frees the handle; a second close
+    is a no-op and a call after it raises."""
+    dev = cuda_device
+    M, n = 2, 10_000
+    plan = z.zero1_plan(n, M, 8)
+    state = [pinned(t) for t in make_state(n, plan.padded_n, 3, dev)]
+    params = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+    grads = make_grads(M, n, 1e-2, 4, 1, dev)
+    step = z.HostStreamedStep(plan, 0, M, grads, *state, params, chunk_elems=1024)
+    step(z.AdamW(global_batch=64))
+    step.close()
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(params).item() > 0
+    step.close()
+    with pytest.raises(ValueError):
+        step(z.AdamW(global_batch=64, step=2))

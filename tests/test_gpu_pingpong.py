@@ -296,3 +296,58 @@ def test_bucketed_pingpong_checks_coverage(cuda_device):
         attempt.finish(hp)
     with pytest.raises(ValueError):
         attempt.bucket(4000, 4100, [g[4000:] for g in grads], hp)
+
+
+def test_llama_layers_pingpong_with_pages_policy(cuda_device):
+    """Full size: the four Llama-style layers (872,448,000 parameters, M = 8,
+    S = 65536), the pages' fp16 block (hysteresis 2), +inf injected on the
+    third attempt: the ping-pong step skips it on the device, keeps S, does
+    not advance t, restores params; sampled elements of the current copy and
+    of params equal the oracle after every attempt."""
+    from zero_sharded_mixed_zero1_gb300 import workloads as W
+    w = W.LLAMA4
+    dev = cuda_device
+    plan = z.zero1_plan(w.n, w.M, w.align)
+    n, P = plan.n, plan.padded_n
+    policy = z.LossScalePolicy(initial_scale=w.S, factor=2.0, window=1000, hysteresis=2, min_scale=1.0)
+    hp = z.AdamW(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay, global_batch=w.B)
+    scaler = z.new_scaler(dev)
+    z.zero1_scaler_init(scaler, policy, hp)
+    sc = oracle.Scaler.start(oracle_policy(policy), 1)
+    master = torch.zeros(P, dtype=torch.float32, device=dev)
+    master[:n] = synth.normal_f32(n, w.master_std, synth.seed_of(w.seed, 1), dev)
+    pairs = [[master, torch.empty_like(master)], [torch.zeros_like(master), torch.empty_like(master)],
+             [torch.zeros_like(master), torch.empty_like(master)]]
+    params = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+    grads = [torch.empty(n, dtype=torch.bfloat16, device=dev) for _ in range(w.M)]
+    rng = np.random.default_rng(3)
+    idx_np = np.unique(np.concatenate([rng.integers(0, n, 1 << 15), np.arange(n - 64, n)]))
+    idx = torch.from_numpy(idx_np).to(dev)
+    o = [f32(pairs[0][0][idx]), f32(pairs[1][0][idx]), f32(pairs[2][0][idx])]
+    o_params = np.zeros(idx_np.size, np.uint16)
+    for attempt in range(1, 5):
+        injected = 0
+        for r, g in enumerate(grads):
+            g.copy_(synth.normal_bf16(n, w.grad_std * sc.scale, synth.seed_of(w.seed, 100 + attempt, r), dev))
+            if attempt == w.inf_attempt:
+                injected += synth.set_inf(g, w.inf_prob, synth.seed_of(w.seed, 900 + attempt, r))
+        g_s = [u16(g[idx]) for g in grads]
+        z.zero1_step_dynamic_pingpong(plan, 0, w.M, grads, *pairs, params, hp, scaler, policy)
+        torch.cuda.synchronize()
+        expect = 1 if attempt == w.inf_attempt else 0           # known from the draws
+        assert (injected > 0) == bool(expect)
+        ohp = oracle.AdamW(lr=hp.lr, beta1=hp.beta1, beta2=hp.beta2, eps=hp.eps, weight_decay=hp.weight_decay,
+                           global_batch=hp.global_batch, loss_scale=sc.scale, step=sc.step)
+        oracle.zero1_step(g_s, idx_np.size, *o, o_params, ohp, flag=np.array([expect], np.uint32),
+                          skip_if_flag=True)
+        sc.update(expect, oracle_policy(policy))
+        check_scaler(z.scaler_state(scaler), sc, hp)
+        cm, cmo, cv = z.current_state(scaler, *pairs)
+        assert_f32_bits(f32(cm[idx]), o[0], f"master attempt {attempt}")
+        assert_f32_bits(f32(cmo[idx]), o[1], f"m attempt {attempt}")
+        assert_f32_bits(f32(cv[idx]), o[2], f"v attempt {attempt}")
+        assert_bf16_bits(u16(params[idx]), o_params, f"params attempt {attempt}")
+    st = z.scaler_state(scaler)
+    assert st["step"] == 4 and st["skipped"] == 1 and st["scale"] == w.S and st["current"] == 1
+    del grads, pairs, params, master
+    torch.cuda.empty_cache()

@@ -267,6 +267,15 @@ int zero1_step_tma(const zero1_plan_t *plan, int32_t shard_begin, int32_t shard_
  * device) and clears it if `clear` is nonzero. */
 int zero1_device_status(uint32_t *status, int32_t clear);
 
+/* Failure-detection self-test of the bounded waits (no counterpart in the
+ * pages): one thread arms a shared-memory mbarrier that expects two arrivals,
+ * arrives once and waits for the phase with the same bounded wait the staged
+ * kernel uses, limited to limit_us microseconds (1 .. 1,000,000).  The wait
+ * must run out: the kernel writes 1 to *gave_up (device uint32), sets bit 0
+ * of the device status word (zero1_device_status) and returns, leaving the
+ * context usable.  Nothing else is read or written. */
+int zero1_bounded_wait_selftest(uint32_t limit_us, uint32_t *gave_up, zero1_stream_t stream);
+
 /* Overflow check [OPT]: ORs 1 into *flag (device uint32) if the rank order
  * fp32 sum of any real element of shards [shard_begin, shard_end) is inf or
  * NaN.  Reads the same nv elements of grads[r] as the fused step (none, and

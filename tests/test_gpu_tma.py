@@ -88,3 +88,46 @@ def test_staged_step_skips_and_rejects_host_memory(cuda_device):
     with pytest.raises(z.Zero1Error):
         z.zero1_step_tma(plan, 0, M, [g.cpu().pin_memory() for g in grads], master, m, v, params,
                          z.AdamW(global_batch=64))
+
+
+@pytest.mark.parametrize("limit_us", [200, 5000])
+def test_bounded_wait_gives_up_reports_and_leaves_the_context_usable(cuda_device, limit_us):
+    """Failure detection without a fault: a wait that can never complete (a
+    barrier that expects two arrivals and gets one) gives up after its limit,
+    reports through the device status word and returns; the context then
+    runs the staged step correctly with a clean status."""
+    import time
+    dev = cuda_device
+    assert z.zero1_device_status(clear=True) in (0, 1)
+    gave_up = torch.zeros(1, dtype=torch.int32, device=dev)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    z.zero1_bounded_wait_selftest(limit_us, gave_up)
+    torch.cuda.synchronize()
+    elapsed = time.perf_counter() - t0
+    assert int(gave_up.item()) == 1
+    assert elapsed >= limit_us * 1e-6
+    assert z.zero1_device_status(clear=True) == 1
+    assert z.zero1_device_status(clear=True) == 0
+    M, n = 4, 50_003
+    plan = z.zero1_plan(n, M, 8)
+    a = make_state(n, plan.padded_n, 11, dev, nonzero_moments=True)
+    b = [t.clone() for t in a]
+    pa = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+    pb = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+    grads = make_grads(M, n, 1e-2, 12, 1, dev)
+    hp = z.AdamW(global_batch=64)
+    z.zero1_step_tma(plan, 0, M, grads, *a, pa, hp)
+    z.zero1_reduce_scatter_adamw_allgather(plan, 0, M, grads, *b, pb, hp)
+    torch.cuda.synchronize()
+    for x, y, what in zip(a, b, ("master", "m", "v")):
+        assert_f32_bits(f32(x), f32(y), what)
+    assert_bf16_bits(u16(pa), u16(pb), "params")
+    assert z.zero1_device_status(clear=True) == 0
+
+
+def test_bounded_wait_selftest_validates(cuda_device):
+    gave_up = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    for bad in (0, 1_000_001):
+        with pytest.raises(z.Zero1Error):
+            z.zero1_bounded_wait_selftest(bad, gave_up)

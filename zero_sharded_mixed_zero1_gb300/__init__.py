@@ -37,6 +37,7 @@ from ._lib import (  # noqa: F401
     zero1_step_bucket,
     zero1_step_tma,
     zero1_device_status,
+    zero1_bounded_wait_selftest,
     zero1_checksum,
     zero1_step_dynamic,
     zero1_step_dynamic_noalloc,

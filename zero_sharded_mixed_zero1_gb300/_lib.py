@@ -141,6 +141,7 @@ def load() -> ctypes.CDLL:
         "zero1_step_bucket": [P, i64, i64, vp, vp, vp, vp, vp, A, vp, vp],
         "zero1_step_tma": [P, i32, i32, vp, vp, vp, vp, vp, A, vp, i32, vp],
         "zero1_device_status": [vp, i32],
+        "zero1_bounded_wait_selftest": [ctypes.c_uint32, vp, vp],
         "zero1_checksum": [vp, i64, vp, vp],
         "zero1_step_dynamic": [P, i32, i32, vp, vp, vp, vp, vp, A, vp, ctypes.POINTER(_PolicyStruct), vp, vp],
         "zero1_step_dynamic_noalloc": [P, i32, i32, vp, vp, vp, vp, vp, A, vp, ctypes.POINTER(_PolicyStruct), vp],
@@ -273,6 +274,14 @@ def zero1_step_tma(plan: Plan, shard_begin: int, shard_end: int, grads, master, 
         _dev(master, torch.float32, L, "master"), _dev(m, torch.float32, L, "m"), _dev(v, torch.float32, L, "v"),
         _dev(params, torch.bfloat16, nv, "params"), ctypes.byref(hp.c_struct()), flag or None,
         int(bool(skip_if_flag)), _stream(stream)))
+
+
+def zero1_bounded_wait_selftest(limit_us: int, gave_up: torch.Tensor, stream=None) -> None:
+    """Launch the bounded-wait self-test: a wait that cannot complete must give
+    up after limit_us, write 1 to gave_up (device int32) and set bit 0 of the
+    device status word."""
+    _check_rc(load().zero1_bounded_wait_selftest(int(limit_us), _dev(gave_up, torch.int32, 1, "gave_up"),
+                                                 _stream(stream)))
 
 
 def zero1_checksum(t: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:

@@ -64,18 +64,35 @@ __device__ __forceinline__ uint64_t global_ns()
 }
 
 // Wait for the phase of the given parity; false (and the status bit set)
-// if it has not completed within kWaitNs.
-__device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity)
+// if it has not completed within limit_ns of %globaltimer, or within
+// kWaitPolls polls should the timer not advance.
+constexpr uint64_t kWaitPolls = 1ull << 24;
+
+__device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity, uint64_t limit_ns = kWaitNs)
 {
     if (mbar_try(b, parity)) return true;
     const uint64_t t0 = global_ns();
-    while (!mbar_try(b, parity)) {
-        if (global_ns() - t0 > kWaitNs) {
+    for (uint64_t polls = 1; !mbar_try(b, parity); ++polls) {
+        if (global_ns() - t0 > limit_ns || polls >= kWaitPolls) {
             atomicOr(&g_zero1_status, 1u);
             return false;
         }
     }
     return true;
+}
+
+// Self-test of the bounded wait: a barrier that expects two arrivals gets
+// one, so its phase never completes; the wait must give up after limit_ns,
+// set bit 0 of g_zero1_status and return.  Only shared memory and the status
+// word are touched.
+__global__ void k_wait_selftest(uint64_t limit_ns, uint32_t *gave_up)
+{
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(&bar, 2);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_arrive(&bar);
+    *gave_up = mbar_wait(&bar, 0, limit_ns) ? 0u : 1u;
 }
 
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
@@ -305,3 +322,15 @@ extern "C" int zero1_device_status(uint32_t *status, int32_t clear)
     return ZERO1_OK;
 }
 
+
+extern "C" int zero1_bounded_wait_selftest(uint32_t limit_us, uint32_t *gave_up, zero1_stream_t stream)
+{
+    Z1Trace trace("zero1_bounded_wait_selftest");
+    if (limit_us < 1 || limit_us > 1000000)
+        return z1_fail(ZERO1_EINVAL, "wait self-test: limit of %u us not in [1, 1000000]", limit_us);
+    if (!gave_up) return z1_fail(ZERO1_EINVAL, "wait self-test: gave_up is NULL");
+    int rc;
+    if ((rc = check_natural(gave_up, 4, "gave_up")) != ZERO1_OK) return rc;
+    k_wait_selftest<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>((uint64_t)limit_us * 1000ull, gave_up);
+    return launch_status("wait self-test launch");
+}

@@ -362,7 +362,19 @@ def run_ours(args, w) -> None:
                                    hysteresis=2, min_scale=1.0)
         scaler = z.new_scaler(dev)
         z.zero1_scaler_init(scaler, policy, hp(1))
-        if op == "dynamic":
+        if op == "dynamic" and args.state_on_host and args.offload_transfer == "copy_engines":
+            # the fp16 block with offload_optimizer: state staged through HBM,
+            # the skip decided by an overflow pass before any chunk is updated
+            staged = {id(gs): z.HostStreamedStep(plan, sb, se, gs, master, m, v, params,
+                                                 chunk_elems=args.chunk_elems, stream=stream) for gs in gsets}
+
+            def launch(gr, tt, st=None):
+                staged[id(gr)].dynamic(hp(tt), scaler, policy)
+            n_chunks = len(staged[id(gsets[0])].pieces)
+            op_kernel = (f"staged dynamic step: k_overflow + k_fused_step_scaled per {args.chunk_elems}-element "
+                         "chunk (state staged through HBM by the copy engines) + k_scaler_update")
+            launches_per_step, op_bytes = n_chunks + 2, algorithmic_bytes(nv, L - nv, w.M) + 2 * w.M * nv
+        elif op == "dynamic":
             sums = torch.empty(L, dtype=torch.float32, device=dev)
 
             def launch(gr, tt, st=None):
@@ -571,7 +583,7 @@ def run_ours(args, w) -> None:
     # with the state in host memory the step is bound by the host link: 12 B
     # of master/m/v in and 12 B out per element, measured against the link
     offload_link = None
-    if args.state_on_host and op == "step":
+    if args.state_on_host and op in ("step", "dynamic"):
         offload_link = link_roofline(host_link_rates(dev), 12 * L, 12 * L, ms_total * 1e-3 / args.steps)
         # host-link steps see occasional stalls from other work on the shared
         # host: the median step against the same bound

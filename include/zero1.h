@@ -239,6 +239,7 @@ int zero1_staged_step(zero1_staged_t *handle, const void *const *grads, float *m
                       void *params, void *params_host, const zero1_adamw_t *hp, uint32_t *overflow_flag,
                       zero1_stream_t stream);
 int zero1_staged_destroy(zero1_staged_t *handle);
+
 /* The handle's chunk boundaries: *count = chunks + 1 values 0 = cuts[0] <
  * ... < cuts[chunks] = L, written to cuts (if not NULL; ERANGE if cap is
  * smaller): chunks of chunk_elems (rounded up to a multiple of 8) elements,
@@ -439,6 +440,23 @@ int zero1_pingpong_bucket(const zero1_plan_t *plan, int64_t elem_begin, int64_t 
 int zero1_pingpong_finish(const zero1_plan_t *plan, int32_t shard_begin, int32_t shard_end,
                           float *const *master, void *params, const zero1_adamw_t *hp, zero1_scaler_t *scaler,
                           const zero1_loss_scale_policy_t *policy, zero1_stream_t stream);
+
+/* The staged step with dynamic loss scaling [OPT] (the fp16 block together
+ * with offload_optimizer: the fp32 state in host memory, S and t on the
+ * device): an overflow pass over the attempt's gradients ORs the flag into
+ * scaler->overflow; every chunk is then staged as in zero1_staged_step, and
+ * its kernel takes 1/(B*S) and the bias corrections from the scaler and
+ * returns at once when the flag is set, so an overflowing attempt changes no
+ * state and no parameter (its copies move unchanged values); the scaler then
+ * advances by the loss-scale rule.  Bit for bit zero1_step_dynamic on the
+ * same buffers in device memory.  scaler: device zero1_scaler_t started with
+ * zero1_scaler_init; hp as for zero1_step_dynamic (loss_scale and step are
+ * the scaler's).  Arguments and errors otherwise as zero1_staged_step.  The
+ * overflow pass reads the gradients where they are: over the host link when
+ * they are staged. */
+int zero1_staged_step_dynamic(zero1_staged_t *handle, const void *const *grads, float *master, float *m, float *v,
+                              void *params, void *params_host, const zero1_adamw_t *hp, zero1_scaler_t *scaler,
+                              const zero1_loss_scale_policy_t *policy, zero1_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * The dynamically scaled step without any device allocation by the caller.

@@ -166,6 +166,11 @@ def test_staged_handle_rejects_bad_arguments(lib):
     assert h.value is None
     assert lib.zero1_staged_step(None, None, None, None, None, None, None, ctypes.byref(_hp()), None, None) == -1
     assert lib.zero1_staged_destroy(None) == 0
+    pol = ctypes.byref(z.LossScalePolicy().c_struct())
+    assert lib.zero1_staged_step_dynamic(None, None, None, None, None, None, None, ctypes.byref(_hp()), None, pol,
+                                         None) == -1                    # no scaler
+    assert lib.zero1_staged_step_dynamic(None, None, None, None, None, None, None, ctypes.byref(_hp()), A, pol,
+                                         None) == -1                    # no handle
     assert lib.zero1_bounded_wait_selftest(0, A, None) == -1          # limit out of range
     assert lib.zero1_bounded_wait_selftest(100, None, None) == -1
     assert lib.zero1_bounded_wait_selftest(100, A + 2, None) == -2    # misaligned result word

@@ -234,3 +234,50 @@ def test_staged_step_close(cuda_device):
     step.close()
     with pytest.raises(ValueError):
         step(z.AdamW(global_batch=64, step=2))
+
+
+@pytest.mark.parametrize("M,n,align,chunk", [(8, 100_003, 128, 8192), (13, 9_999, 8, 1000), (3, 50_000, 1, 7000)])
+@pytest.mark.parametrize("where", ["state", "grads_state", "state_params"])
+def test_staged_dynamic_step_equals_device_dynamic_step(cuda_device, M, n, align, chunk, where):
+    """Dynamic loss scaling with the optimizer state in pinned host memory
+    (the fp16 block with offload_optimizer): every attempt bit for bit the
+    two-pass dynamic step on device buffers, overflowing attempts included
+    (consecutive ones that halve S), and the same scaler."""
+    dev = cuda_device
+    plan = z.zero1_plan(n, M, align)
+    P = plan.padded_n
+    policy = z.LossScalePolicy(initial_scale=1024.0, factor=2.0, window=2, hysteresis=1, min_scale=1.0)
+    hp = z.AdamW(global_batch=max(M, 64), step=1)
+    a = make_state(n, P, 130 + M, dev, nonzero_moments=True)
+    b = [pinned(t) for t in a]
+    pa = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+    pb = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+    host_p = torch.zeros(n, dtype=torch.bfloat16).pin_memory() if where == "state_params" else None
+    gb = [torch.zeros(n, dtype=torch.bfloat16, device=dev) for _ in range(M)]
+    if where == "grads_state":
+        gb = [pinned(g) for g in gb]
+    s_a, s_b = z.new_scaler(dev), z.new_scaler(dev)
+    z.zero1_scaler_init(s_a, policy, hp)
+    z.zero1_scaler_init(s_b, policy, hp)
+    sums = torch.empty(P, dtype=torch.float32, device=dev)
+    step = z.HostStreamedStep(plan, 0, M, gb, *b, pb, chunk_elems=chunk, params_host=host_p)
+    for k in range(7):
+        S = z.scaler_state(s_a)["scale"]
+        grads = make_grads(M, n, 1e-3 * S, 140 + M, k, dev)
+        if k in (2, 3, 5):
+            grads[k % M][(97 * k) % n] = float("inf") if k != 3 else float("nan")
+        for x, g in zip(gb, grads):
+            x.copy_(g)
+        torch.cuda.synchronize()
+        z.zero1_step_dynamic(plan, 0, M, grads, *a, pa, hp, s_a, policy, sums)
+        step.dynamic(hp, s_b, policy)
+        torch.cuda.synchronize()
+        for x, y, what in zip(a, b, ("master", "m", "v")):
+            assert_f32_bits(f32(y), f32(x), f"{where}: {what} attempt {k}")
+        assert_bf16_bits(u16(pb), u16(pa), f"{where}: params attempt {k}")
+        if host_p is not None:
+            assert_bf16_bits(u16(host_p), u16(pa), f"{where}: params on host attempt {k}")
+        assert z.scaler_state(s_b) == z.scaler_state(s_a)
+    st = z.scaler_state(s_b)
+    assert st["skipped"] == 3 and st["step"] == 5
+    step.close()

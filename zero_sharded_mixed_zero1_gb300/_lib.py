@@ -152,6 +152,7 @@ def load() -> ctypes.CDLL:
         "zero1_staged_step": [vp, vp, vp, vp, vp, vp, vp, A, vp, vp],
         "zero1_staged_destroy": [vp],
         "zero1_staged_chunks": [vp, vp, i32, vp],
+        "zero1_staged_step_dynamic": [vp, vp, vp, vp, vp, vp, vp, A, vp, ctypes.POINTER(_PolicyStruct), vp],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)

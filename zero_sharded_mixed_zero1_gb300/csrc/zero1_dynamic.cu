@@ -205,6 +205,54 @@ k_fused_step_pingpong(const __grid_constant__ GradPtrs g, int M, const PingPong 
     warp_flag(&sc->overflow, bad);
 }
 
+// The fused step in place, with S and t taken from the scaler, for a range
+// whose overflow flag is already final (an overflow pass over all of the
+// attempt's gradients ran before it): the kernel returns at once when
+// scaler->overflow is set, so an overflowing attempt writes nothing.  The
+// staged step with dynamic loss scaling uses it on its HBM slots: there the
+// state lives in host memory, where a second copy would cost host memory and
+// twice the link traffic.
+template <int MT>
+__global__ void __launch_bounds__(kBlock, MT == 0 ? 2 : (MT <= 2 ? 2 : 1))
+k_fused_step_scaled(const __grid_constant__ GradPtrs g, int M, float *__restrict__ master,
+                    float *__restrict__ mom, float *__restrict__ var, uint16_t *__restrict__ params, const Walk w,
+                    Z1Consts c, const zero1_scaler_t *sc)
+{
+    if (*reinterpret_cast<const volatile uint32_t *>(&sc->overflow) != 0u) return;
+    c.inv = sc->inv;
+    c.bc1 = sc->bc1;
+    c.bc2 = sc->bc2;
+    const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
+    const int64_t nthr = (int64_t)gridDim.x * kBlock;
+    bool bad = false;  // the flag is final already; nothing is reported
+    if constexpr (MT > 0) {
+        pipelined<VecLoads<MT>>(
+            w.nvec, tid, nthr,
+            [&](VecLoads<MT> &x, int64_t i) { x.load(g, master, mom, var, w.head + i * kVec); },
+            [&](const VecLoads<MT> &x, int64_t i) {
+                const int64_t j = w.head + i * kVec;
+                float sum[kVec];
+                unpack8(x.q[0], sum);
+#pragma unroll
+                for (int r = 1; r < MT; ++r) add8(x.q[r], sum);
+                store_vec(sum, x.w0, x.w1, x.m0, x.m1, x.v0, x.v1, master + j, mom + j, var + j, params + j, c,
+                          bad);
+            });
+    } else {
+        for (int64_t i = tid; i < w.nvec; i += nthr) {
+            const int64_t j = w.head + i * kVec;
+            const float4 *pw = reinterpret_cast<const float4 *>(master + j);
+            const float4 *pm = reinterpret_cast<const float4 *>(mom + j);
+            const float4 *pv = reinterpret_cast<const float4 *>(var + j);
+            const float4 w0 = pw[0], w1 = pw[1], m0 = pm[0], m1 = pm[1], v0 = pv[0], v1 = pv[1];
+            float sum[kVec];
+            sum8<0>(g, M, j, sum);
+            store_vec(sum, w0, w1, m0, m1, v0, v1, master + j, mom + j, var + j, params + j, c, bad);
+        }
+    }
+    fused_scalar_rest(g, M, master, mom, var, params, w, c, tid, nthr, bad);
+}
+
 // After an attempt that overflowed, put back params = bf16(current master);
 // after a clean attempt, return at once.
 __global__ void __launch_bounds__(kBlock)
@@ -460,6 +508,68 @@ extern "C" int zero1_pingpong_finish(const zero1_plan_t *plan, int32_t shard_beg
     if (rc != ZERO1_OK) return rc;
     return launch_pingpong_finish(plan, r.L, r.nv, master, params, hp, scaler, policy,
                                   reinterpret_cast<cudaStream_t>(stream), "ping-pong finish");
+}
+
+// ------------------------------------- pieces of the staged dynamic step --
+
+int z1_scaled_range(const zero1_plan_t *plan, int64_t elem_begin, int64_t elem_end, const void *const *grads,
+                    float *master, float *m, float *v, void *params, const zero1_adamw_t *hp,
+                    const zero1_scaler_t *scaler, zero1_stream_t stream)
+{
+    int rc = z1_check_plan(plan);
+    if (rc != ZERO1_OK) return rc;
+    if (elem_begin < 0 || elem_end > plan->padded_n || elem_begin >= elem_end)
+        return z1_fail(ZERO1_EINVAL, "scaled range [%lld, %lld) not inside [0, %lld)", (long long)elem_begin,
+                       (long long)elem_end, (long long)plan->padded_n);
+    const int64_t L = elem_end - elem_begin;
+    int64_t nv = plan->n - elem_begin;
+    nv = nv < 0 ? 0 : (nv > L ? L : nv);
+    Z1Consts c;
+    if ((rc = dynamic_constants(hp, plan->M, &c)) != ZERO1_OK) return rc;
+    if ((rc = check_scaler_ptr(scaler)) != ZERO1_OK) return rc;
+    if (!master || !m || !v) return z1_fail(ZERO1_EINVAL, "scaled range: master, m and v must be non-NULL");
+    if (nv > 0 && !params)
+        return z1_fail(ZERO1_EINVAL, "scaled range: params must be non-NULL when the range holds parameters");
+    GradPtrs g{};
+    if (nv > 0 && (rc = load_grads(plan, grads, &g, "scaled range")) != ZERO1_OK) return rc;
+    if ((rc = check_natural(master, 4, "master")) || (rc = check_natural(m, 4, "m")) ||
+        (rc = check_natural(v, 4, "v")) || (rc = check_natural(params, 2, "params")))
+        return rc;
+    ArrayRef arr[ZERO1_MAX_REPLICAS + 4] = {{master, 4}, {m, 4}, {v, 4}, {params, 2}};
+    const int M = plan->M;
+    for (int k = 0; k < M; ++k) arr[4 + k] = {g.p[k], 2};
+    const Walk w = make_walk(L, nv, arr, 4 + M);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint16_t *pp = static_cast<uint16_t *>(params);
+    dispatch_m(M, [&](auto mt) {
+        constexpr int MT = decltype(mt)::value;
+        const int grid = grid_for(k_fused_step_scaled<MT>, work_of(w));
+        k_fused_step_scaled<MT><<<grid, kBlock, 0, st>>>(g, M, master, m, v, pp, w, c, scaler);
+    });
+    return launch_status("scaled range launch");
+}
+
+int z1_scaler_advance(zero1_scaler_t *scaler, const zero1_loss_scale_policy_t *policy, const zero1_adamw_t *hp,
+                      int32_t M, zero1_stream_t stream)
+{
+    int rc;
+    Z1Consts c;
+    if ((rc = dynamic_constants(hp, M, &c)) != ZERO1_OK) return rc;
+    if ((rc = check_scaler_ptr(scaler)) != ZERO1_OK || (rc = check_policy(policy)) != ZERO1_OK) return rc;
+    const ScalePolicy pol{policy->factor, policy->window, policy->hysteresis, policy->min_scale};
+    k_scaler_update<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(scaler, pol, hp->global_batch, hp->beta1,
+                                                                          hp->beta2, 0);
+    return launch_status("scaler update launch");
+}
+
+int z1_check_scaler_and_policy(const zero1_scaler_t *scaler, const zero1_loss_scale_policy_t *policy,
+                               const zero1_adamw_t *hp, int32_t M)
+{
+    int rc;
+    Z1Consts c;
+    if ((rc = dynamic_constants(hp, M, &c)) != ZERO1_OK) return rc;
+    if ((rc = check_scaler_ptr(scaler)) != ZERO1_OK) return rc;
+    return check_policy(policy);
 }
 
 // ------------------------------------------- step without caller allocation --

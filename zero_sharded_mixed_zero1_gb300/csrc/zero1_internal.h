@@ -53,3 +53,20 @@ double z1_pow_int(double b, int64_t t);
 // Validate hyperparameters and evaluate the constants: double precision,
 // rounded once to float, beta^t from z1_pow_int.
 int z1_adamw_constants(const zero1_adamw_t *hp, int32_t M, Z1Consts *out);
+
+// Pieces of the staged step with dynamic loss scaling (zero1_dynamic.cu):
+//  z1_scaled_range launches the in-place fused step on the element range
+//  [elem_begin, elem_end) with S and t read from the device scaler; it returns
+//  at once on the device when scaler->overflow is set, which must therefore
+//  be final before the launch.  Pointers start at elem_begin, as for
+//  zero1_step_bucket.
+//  z1_scaler_advance launches the scaler update (the loss-scale rule; the
+//  attempt's flag is read and cleared).
+//  z1_check_scaler_and_policy validates what both need, without launching.
+int z1_scaled_range(const zero1_plan_t *plan, int64_t elem_begin, int64_t elem_end, const void *const *grads,
+                    float *master, float *m, float *v, void *params, const zero1_adamw_t *hp,
+                    const zero1_scaler_t *scaler, zero1_stream_t stream);
+int z1_scaler_advance(zero1_scaler_t *scaler, const zero1_loss_scale_policy_t *policy, const zero1_adamw_t *hp,
+                      int32_t M, zero1_stream_t stream);
+int z1_check_scaler_and_policy(const zero1_scaler_t *scaler, const zero1_loss_scale_policy_t *policy,
+                               const zero1_adamw_t *hp, int32_t M);

@@ -195,11 +195,17 @@ extern "C" int zero1_staged_destroy(zero1_staged_t *h)
     return ZERO1_OK;
 }
 
-extern "C" int zero1_staged_step(zero1_staged_t *h, const void *const *grads, float *master, float *m,
-                                 float *v, void *params, void *params_host, const zero1_adamw_t *hp,
-                                 uint32_t *overflow_flag, zero1_stream_t stream)
+namespace {
+
+// One staged step.  With a scaler (dynamic loss scaling) an overflow pass
+// over the attempt's gradients sets scaler->overflow first, every chunk runs
+// the in-place kernel that takes S and t from the scaler and returns at once
+// on overflow, and the scaler advances after the last chunk; without one,
+// every chunk runs zero1_step_bucket with the host's constants.
+int staged_run(zero1_staged_t *h, const void *const *grads, float *master, float *m, float *v, void *params,
+               void *params_host, const zero1_adamw_t *hp, uint32_t *overflow_flag, zero1_scaler_t *scaler,
+               const zero1_loss_scale_policy_t *policy, zero1_stream_t stream)
 {
-    Z1Trace trace("zero1_staged_step");
     if (!h) return z1_fail(ZERO1_EINVAL, "staged step: handle is NULL");
     int rc;
     int dev = -1;
@@ -208,8 +214,13 @@ extern "C" int zero1_staged_step(zero1_staged_t *h, const void *const *grads, fl
     if (dev != h->device)
         return z1_fail(ZERO1_EINVAL, "staged step: current device %d, the handle belongs to device %d", dev,
                        h->device);
-    Z1Consts c;
-    if ((rc = z1_adamw_constants(hp, h->plan.M, &c)) != ZERO1_OK) return rc;
+    if (scaler) {
+        if ((rc = z1_check_scaler_and_policy(scaler, policy, hp, h->plan.M)) != ZERO1_OK) return rc;
+        if ((rc = check_buffer(scaler, false, 8, "scaler")) != ZERO1_OK) return rc;
+    } else {
+        Z1Consts c;
+        if ((rc = z1_adamw_constants(hp, h->plan.M, &c)) != ZERO1_OK) return rc;
+    }
     const bool sg = h->what & ZERO1_STAGE_GRADS, ss = h->what & ZERO1_STAGE_STATE,
                sp = h->what & ZERO1_STAGE_PARAMS;
     const int M = h->plan.M;
@@ -245,6 +256,11 @@ extern "C" int zero1_staged_step(zero1_staged_t *h, const void *const *grads, fl
         Z1_CUDA(cudaStreamWaitEvent(q, h->entry, 0));
         if (h->last_recorded) Z1_CUDA(cudaStreamWaitEvent(q, h->last, 0));
     }
+    // the attempt's flag is final before any chunk's kernel reads it
+    if (scaler && h->nv > 0 &&
+        (rc = zero1_overflow_check(&h->plan, h->shard_begin, h->shard_end, grads, &scaler->overflow, stream)) !=
+            ZERO1_OK)
+        return rc;
     for (size_t k = 0; k + 1 < h->cuts.size(); ++k) {
         const int64_t e0 = h->cuts[k], e1 = h->cuts[k + 1];
         const int64_t len = e1 - e0;
@@ -282,9 +298,11 @@ extern "C" int zero1_staged_step(zero1_staged_t *h, const void *const *grads, fl
             Z1_CUDA(cudaStreamWaitEvent(st, h->copied_in[slot][q], 0));
         }
         void *pp = real > 0 ? static_cast<uint16_t *>(params) + e0 : nullptr;
-        if ((rc = zero1_step_bucket(&h->plan, h->base + e0, h->base + e1, real > 0 ? gp : nullptr, sp3[0], sp3[1],
-                                    sp3[2], pp, hp, overflow_flag, stream)) != ZERO1_OK)
-            return rc;
+        rc = scaler ? z1_scaled_range(&h->plan, h->base + e0, h->base + e1, real > 0 ? gp : nullptr, sp3[0], sp3[1],
+                                      sp3[2], pp, hp, scaler, stream)
+                    : zero1_step_bucket(&h->plan, h->base + e0, h->base + e1, real > 0 ? gp : nullptr, sp3[0],
+                                        sp3[1], sp3[2], pp, hp, overflow_flag, stream);
+        if (rc != ZERO1_OK) return rc;
         Z1_CUDA(cudaEventRecord(h->computed[slot], st));
         if (has_out) {
             Z1_CUDA(cudaStreamWaitEvent(h->out, h->computed[slot], 0));
@@ -303,10 +321,31 @@ extern "C" int zero1_staged_step(zero1_staged_t *h, const void *const *grads, fl
         Z1_CUDA(cudaEventRecord(h->done, h->out));
         Z1_CUDA(cudaStreamWaitEvent(st, h->done, 0));
     }
+    if (scaler && (rc = z1_scaler_advance(scaler, policy, hp, M, stream)) != ZERO1_OK) return rc;
     Z1_CUDA(cudaEventRecord(h->last, st));
 #undef Z1_CUDA
     h->last_recorded = true;
     return ZERO1_OK;
+}
+
+}  // namespace
+
+extern "C" int zero1_staged_step(zero1_staged_t *h, const void *const *grads, float *master, float *m,
+                                 float *v, void *params, void *params_host, const zero1_adamw_t *hp,
+                                 uint32_t *overflow_flag, zero1_stream_t stream)
+{
+    Z1Trace trace("zero1_staged_step");
+    return staged_run(h, grads, master, m, v, params, params_host, hp, overflow_flag, nullptr, nullptr, stream);
+}
+
+extern "C" int zero1_staged_step_dynamic(zero1_staged_t *h, const void *const *grads, float *master, float *m,
+                                         float *v, void *params, void *params_host, const zero1_adamw_t *hp,
+                                         zero1_scaler_t *scaler, const zero1_loss_scale_policy_t *policy,
+                                         zero1_stream_t stream)
+{
+    Z1Trace trace("zero1_staged_step_dynamic");
+    if (!scaler) return z1_fail(ZERO1_EINVAL, "staged dynamic step: scaler is NULL");
+    return staged_run(h, grads, master, m, v, params, params_host, hp, nullptr, scaler, policy, stream);
 }
 
 extern "C" int zero1_staged_chunks(const zero1_staged_t *h, int64_t *cuts, int32_t cap, int32_t *count)

@@ -98,6 +98,19 @@ class HostStreamedStep:
                 self._handle, self._grads, *self._state, self._params, self._params_host,
                 ctypes.byref(hp.c_struct()), self._flag, _lib._stream(self._stream)))
 
+    def dynamic(self, hp: _lib.AdamW, scaler: torch.Tensor, policy: _lib.LossScalePolicy) -> None:
+        """One attempt with dynamic loss scaling (zero1_staged_step_dynamic):
+        S and t come from the device scaler, an overflow pass decides the skip
+        before any chunk is updated, and the scaler advances afterwards.  The
+        overflow_flag given at construction is not used."""
+        if self._handle is None:
+            raise ValueError("the staged step has been closed")
+        with torch.cuda.device(self._device):
+            _lib._check_rc(self._lib.zero1_staged_step_dynamic(
+                self._handle, self._grads, *self._state, self._params, self._params_host,
+                ctypes.byref(hp.c_struct()), _lib._scaler_ptr(scaler), ctypes.byref(policy.c_struct()),
+                _lib._stream(self._stream)))
+
     def close(self) -> None:
         """Wait for the handle's queued work and free its staging memory."""
         if getattr(self, "_handle", None) is not None:

@@ -125,7 +125,7 @@ def test_offload_and_staged_steps_stay_in_bounds(cuda_device, M, n, align, shard
     sb, se = shards or (0, M)
     base, L, nv = plan.shard_range(sb, se)
     hp = z.AdamW(global_batch=max(M, 64), step=2)
-    for entry in ("offload_kernel", "staged_state", "staged_grads"):
+    for entry in ("offload_kernel", "staged_state", "staged_grads", "staged_dynamic"):
         grads = _grads(M, nv, dev, ph, pinned=(entry == "staged_grads"))
         state = _state(L, nv, dev, ph, pinned=(entry != "staged_grads"))
         params = Guarded(nv, torch.bfloat16, dev, ph())
@@ -136,7 +136,13 @@ def test_offload_and_staged_steps_stay_in_bounds(cuda_device, M, n, align, shard
         else:
             step = z.HostStreamedStep(plan, sb, se, gv, *sv, params.view, chunk_elems=int(rng.integers(500, 70_000)),
                                       params_host=host_p.view)
-            step(hp)
+            if entry == "staged_dynamic":
+                policy = z.LossScalePolicy(initial_scale=64.0, window=1000, hysteresis=2)
+                scaler = z.new_scaler(dev)
+                z.zero1_scaler_init(scaler, policy, hp)
+                step.dynamic(hp, scaler, policy)
+            else:
+                step(hp)
             step.close()
         torch.cuda.synchronize()
         for i, b in enumerate(grads + state + [params, host_p]):

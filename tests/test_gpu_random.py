@@ -4,7 +4,7 @@ buffer (so the vector head, the per-element fallback and the ragged tail all
 occur), hyperparameters and step, and every entry point that computes the
 step (one-shot, prepared, bucketed, shared-memory staged, dynamic, ping-pong
 whole and in buckets, and the copy-engine staged step with state or
-gradients in pinned host memory)."""
+gradients in pinned host memory, with and without dynamic loss scaling)."""
 import numpy as np
 import pytest
 import torch
@@ -16,7 +16,7 @@ from gpu_helpers import assert_bf16_bits, assert_f32_bits, f32, oracle_hp, u16
 pytestmark = pytest.mark.gpu
 
 ENTRIES = ["fused", "prepared", "bucket", "tma", "dynamic", "pingpong", "pingpong_buckets", "staged_state",
-           "staged_grads"]
+           "staged_grads", "staged_dynamic"]
 
 
 def _buf(numel, dtype, phase, dev):
@@ -36,7 +36,7 @@ def _cuts(rng, L):
     return sorted({0, L, *[int(x) for x in rng.integers(0, L + 1, int(rng.integers(1, 6)))]})
 
 
-@pytest.mark.parametrize("case", range(126))
+@pytest.mark.parametrize("case", range(140))
 def test_random_configuration(cuda_device, case):
     dev = cuda_device
     rng = np.random.default_rng(20_000 + case)
@@ -102,9 +102,16 @@ def test_random_configuration(cuda_device, case):
                 attempt.bucket(e0, e1, [g[e0:e0 + k] for g in grads], hp)
             attempt.finish(hp)
         state = list(z.current_state(scaler, *pairs))
-    elif entry == "staged_state":
+    elif entry in ("staged_state", "staged_dynamic"):
         state = [_pinned_like(t, ph()) for t in state]
-        z.HostStreamedStep(plan, sb, se, grads, *state, params, chunk_elems=int(rng.integers(1, 6000)))(hp)
+        step = z.HostStreamedStep(plan, sb, se, grads, *state, params, chunk_elems=int(rng.integers(1, 6000)))
+        if entry == "staged_dynamic":
+            policy = z.LossScalePolicy(initial_scale=S, window=1000, hysteresis=2)
+            scaler = z.new_scaler(dev)
+            z.zero1_scaler_init(scaler, policy, hp)
+            step.dynamic(hp, scaler, policy)
+        else:
+            step(hp)
     elif entry == "staged_grads":
         grads = [_pinned_like(g, ph()) for g in grads]
         host_p = _pinned_like(params, ph())

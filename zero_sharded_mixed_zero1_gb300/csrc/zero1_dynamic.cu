@@ -144,23 +144,21 @@ struct PingPong {
 // 64-replica shard: state read with the default policy at two blocks per SM
 // (107 registers) beat three blocks per SM, whose 85-register cap spilled
 // (2.64 against 2.75-2.85 ms).
-template <int MT>
-__global__ void __launch_bounds__(kBlock, MT == 0 ? 2 : (MT <= 2 ? 2 : 1))
-k_fused_step_pingpong(const __grid_constant__ GradPtrs g, int M, const PingPong s, uint16_t *__restrict__ params,
-                      const Walk w, Z1Consts c, zero1_scaler_t *sc)
+// The body for a copy index known at compile time: every pointer is then a
+// kernel parameter, which the compiler can reload instead of holding it in a
+// register (169 registers at M = 8 against 179 with the copy picked at run
+// time; the same speed on the same box).
+template <int MT, int CUR>
+__device__ __forceinline__ void pingpong_body(const GradPtrs &g, int M, const PingPong &s,
+                                              uint16_t *__restrict__ params, const Walk &w, const Z1Consts &c,
+                                              zero1_scaler_t *sc)
 {
-    const int cur = (int)(*reinterpret_cast<const volatile uint32_t *>(&sc->current) & 1u);
-    c.inv = sc->inv;
-    c.bc1 = sc->bc1;
-    c.bc2 = sc->bc2;
-    // selects, not s.x[cur]: indexing the parameter struct by a runtime value
-    // would copy it to local memory
-    const float *__restrict__ sw = cur ? s.master[1] : s.master[0];
-    const float *__restrict__ sm = cur ? s.mom[1] : s.mom[0];
-    const float *__restrict__ sv = cur ? s.var[1] : s.var[0];
-    float *__restrict__ dw = cur ? s.master[0] : s.master[1];
-    float *__restrict__ dm = cur ? s.mom[0] : s.mom[1];
-    float *__restrict__ dv = cur ? s.var[0] : s.var[1];
+    const float *__restrict__ sw = s.master[CUR];
+    const float *__restrict__ sm = s.mom[CUR];
+    const float *__restrict__ sv = s.var[CUR];
+    float *__restrict__ dw = s.master[CUR ^ 1];
+    float *__restrict__ dm = s.mom[CUR ^ 1];
+    float *__restrict__ dv = s.var[CUR ^ 1];
     const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
     const int64_t nthr = (int64_t)gridDim.x * kBlock;
     bool bad = false;
@@ -203,6 +201,21 @@ k_fused_step_pingpong(const __grid_constant__ GradPtrs g, int M, const PingPong 
         if (j < w.nv) params[j] = to_bf16(ww);
     }
     warp_flag(&sc->overflow, bad);
+}
+
+template <int MT>
+__global__ void __launch_bounds__(kBlock, MT == 0 ? 2 : (MT <= 2 ? 2 : 1))
+k_fused_step_pingpong(const __grid_constant__ GradPtrs g, int M, const __grid_constant__ PingPong s,
+                      uint16_t *__restrict__ params, const Walk w, Z1Consts c, zero1_scaler_t *sc)
+{
+    const uint32_t cur = *reinterpret_cast<const volatile uint32_t *>(&sc->current) & 1u;
+    c.inv = sc->inv;
+    c.bc1 = sc->bc1;
+    c.bc2 = sc->bc2;
+    if (cur)
+        pingpong_body<MT, 1>(g, M, s, params, w, c, sc);
+    else
+        pingpong_body<MT, 0>(g, M, s, params, w, c, sc);
 }
 
 // The fused step in place, with S and t taken from the scaler, for a range

@@ -252,8 +252,12 @@ int staged_run(zero1_staged_t *h, const void *const *grads, float *master, float
         if ((e = (call)) != cudaSuccess) return cuda_fail(e, #call); \
     } while (0)
     Z1_CUDA(cudaEventRecord(h->entry, st));
+    // and once this handle's outbound copies are done, including those of a
+    // call that failed part way (it did not reach its own join)
+    Z1_CUDA(cudaEventRecord(h->done, h->out));
     for (cudaStream_t q : h->in) {
         Z1_CUDA(cudaStreamWaitEvent(q, h->entry, 0));
+        Z1_CUDA(cudaStreamWaitEvent(q, h->done, 0));
         if (h->last_recorded) Z1_CUDA(cudaStreamWaitEvent(q, h->last, 0));
     }
     // the attempt's flag is final before any chunk's kernel reads it

@@ -536,7 +536,9 @@ class FusedStep:
         _replicas(plan, grads, "grads")
         _, L, nv = _range(plan, shard_begin, shard_end)
         self._plan = plan
-        self._keep = (grads, master, m, v, params, overflow_flag)
+        # a copy of the list: the cached addresses stay valid even if the
+        # caller later replaces an element of its own list
+        self._keep = (tuple(grads), master, m, v, params, overflow_flag)
         self._grads = _ptrs(grads, torch.bfloat16, nv, "grads")
         flag = 0 if overflow_flag is None else _dev(overflow_flag, torch.int32, 1, "overflow_flag")
         self._args = (ctypes.byref(plan), shard_begin, shard_end, self._grads,

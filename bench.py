@@ -7,9 +7,10 @@ A step is one pass of the whole hot path over one batch: the M replicas'
 bf16 gradients are reduce-scattered (rank-order fp32 sum, scaled by 1/(B*S)),
 the fp32 master/m/v get the AdamW update, the overflow flag is ORed and the
 bf16 parameters are written once (all-gather) - one fused kernel launch.  The
-default workload is the GPT-2-small-sized flat buffer (124,439,808 parameters,
-M = 8 replicas, B = 512); its 5.2 GB of traffic per step is far larger than
-the 129 MB L2, so no flush is needed between steps.
+default workload is the largest flat buffer that the method is stated on
+that fits one GPU: 1.3B parameters (P = 1,300,000,768 after padding to
+multiples of 8*128), M = 8 replicas, B = 1024; its 54.6 GB of traffic per step
+is far larger than the 129 MB L2, so no flush is needed between steps.
 
 Under torchrun (N > 1) every rank runs an independent replica of the
 workload on its own GPU (weak scaling, no collective on the data path); the
@@ -60,19 +61,50 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "source": "fallback"}
 
 
-def recorded_traffic(workload: str):
-    """dram read+write bytes per launch from the committed ncu summary, if it
-    was taken on the kernel source as it stands now (else None)."""
-    path = os.path.join(ROOT, "profiles", f"k_fused_step_{workload}.md")
-    if not os.path.exists(path):
-        return None
-    text = open(path).read()
+# ncu DRAM counters of the fused kernel, captured on a small case of the same
+# kernel (16,777,216 parameters, M = 8: 705 MB per launch, above L2) and
+# scaled to a launch of the timed workload by its algorithmic bytes.
+TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "k_fused_step_dram_prof_16M_M8.md")
+
+
+def recorded_traffic(M: int, bytes_launch: int):
+    """DRAM read+write bytes per launch, scaled from the committed ncu
+    summary of the small case, if that was taken on the kernel source as it
+    stands now and with the same replica count (else None).  Returns
+    (bytes, note)."""
+    if not os.path.exists(TRAFFIC_PROFILE):
+        return None, None
+    text = open(TRAFFIC_PROFILE).read()
     sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
     tr = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
-    if not sha or not tr:
-        return None
+    alg = re.search(r"algorithmic_bytes_per_launch:\s*([0-9]+)", text)
+    reps = re.search(r"replicas:\s*([0-9]+)", text)
+    if not (sha and tr and alg and reps) or int(reps.group(1)) != M:
+        return None, None
     cur = hashlib.sha256(b"".join(open(f, "rb").read() for f in KERNEL_SOURCES)).hexdigest()
-    return int(tr.group(1)) if sha.group(1) == cur else None
+    if sha.group(1) != cur:
+        return None, None
+    ratio = int(tr.group(1)) / int(alg.group(1))
+    return int(round(ratio * bytes_launch)), (
+        f"ncu dram__bytes_read.sum + dram__bytes_write.sum of a steady-state launch on the 16,777,216-parameter "
+        f"case ({int(tr.group(1))} B against {int(alg.group(1))} B algorithmic, ratio {ratio:.4f}), scaled to "
+        f"this launch's {bytes_launch} algorithmic bytes")
+
+
+def host_cpu() -> dict:
+    """This host's logical CPU count and CPU model."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        m = re.search(r"^Model name:\s*(.+)$", out, re.M)
+        model = m.group(1).strip() if m else None
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None and os.path.exists("/proc/cpuinfo"):
+        m = re.search(r"^model name\s*:\s*(.+)$", open("/proc/cpuinfo").read(), re.M)
+        model = m.group(1).strip() if m else None
+    import platform
+    return {"host_cpu_count": os.cpu_count(), "cpu_model": model or "unknown", "machine": platform.machine()}
 
 
 class ClockSampler:
@@ -81,7 +113,7 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int, period_ms: int = 100):
+    def __init__(self, gpu_index: int, period_ms: int = 20):
         self.proc = None
         try:
             self.f = tempfile.NamedTemporaryFile("w", prefix="clocks_", suffix=".csv", delete=False)
@@ -225,7 +257,8 @@ def run_reference(args, w) -> None:
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic", "config": config_of(w),
-        "cpu_baseline": {"value": value, "unit": "params/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "params/s", "cores": 1, "kind": "oracle", "sample": sample,
+                         **host_cpu()},
         "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -328,7 +361,7 @@ def run_ours(args, w) -> None:
         rate, nsteps = oracle_sample_rate(w, sample, args.cpu_seconds)
         cpu_baseline = {"value": rate, "unit": "params/s", "cores": 1, "kind": "oracle",
                         "sample": f"{nsteps} steps over {sample} of {w.n} elements, M={w.M} replicas, "
-                                  f"single-threaded C oracle"}
+                                  f"single-threaded C oracle", **host_cpu()}
 
     if rank == 0 and zbuild.is_stale():
         zbuild.build()
@@ -520,7 +553,8 @@ def run_ours(args, w) -> None:
         sampler.stop()
     ms_total = max_over_ranks(ms_local, world)
     overflow = int(flag.item())
-    del gsets
+    if args.no_e2e or op != "step":
+        del gsets
 
     # end to end through the public API with host buffers: each step's
     # gradients start in pinned host memory and the step's parameters and
@@ -531,10 +565,16 @@ def run_ours(args, w) -> None:
     e2e = e2e_staged = None
     if not args.no_e2e and op == "step":
         e2e_steps = max(3, min(args.steps, args.e2e_steps))
-        host_g = [synth.normal_bf16(nv, w.grad_std * w.S, synth.seed_of(w.seed, 7, r, rank)).pin_memory()
-                  for r in range(w.M)]
-        host_p = torch.empty(nv, dtype=torch.bfloat16).pin_memory()
-        host_f = torch.empty(1, dtype=torch.int32).pin_memory()
+        # the e2e gradients: drawn on the device (fast even at 1.3B x 8), then
+        # placed in pinned host memory before anything is timed
+        host_g = []
+        for r in range(w.M):
+            h = torch.empty(nv, dtype=torch.bfloat16, pin_memory=True)
+            h.copy_(synth.normal_bf16(nv, w.grad_std * w.S, synth.seed_of(w.seed, 7, r, rank), dev))
+            host_g.append(h)
+        del gsets
+        host_p = torch.empty(nv, dtype=torch.bfloat16, pin_memory=True)
+        host_f = torch.empty(1, dtype=torch.int32, pin_memory=True)
         streamed = z.HostStreamedStep(plan, sb, se, host_g, master, m, v, params, chunk_elems=args.chunk_elems,
                                       params_host=host_p, overflow_flag=flag, stream=stream)
 
@@ -550,34 +590,52 @@ def run_ours(args, w) -> None:
             stream.synchronize()
 
         def timed(fn):
+            """Whole-loop seconds (slowest rank) and each step's seconds:
+            every step ends with a stream synchronize, so the wall-clock
+            delta of one step is that step's end-to-end time."""
             nonlocal t
             fn(t)
             t += 1
             barrier(world)
             w0 = time.perf_counter()
+            per_step = []
             for _ in range(e2e_steps):
+                s0 = time.perf_counter()
                 fn(t)
+                per_step.append(time.perf_counter() - s0)
                 t += 1
             barrier(world)
-            return max_over_ranks(time.perf_counter() - w0, world)
+            return max_over_ranks(time.perf_counter() - w0, world), np.array(per_step)
 
-        copy_s = timed(copy_step)
-        zero_s = timed(zero_copy_step)
+        copy_s, copy_steps = timed(copy_step)
+        zero_s, zero_steps = timed(zero_copy_step)
         del streamed
         link = host_link_rates(dev)
         bi, bo = w.M * nv * 2, nv * 2 + 4
+
+        def step_stats(steps_s):
+            return {"ms_per_step_median": float(np.median(steps_s)) * 1e3, "ms_per_step_min": float(steps_s.min()) * 1e3,
+                    "ms_per_step_max": float(steps_s.max()) * 1e3}
+
+        def roof(total_s, steps_s):
+            r = link_roofline(link, bi, bo, total_s / e2e_steps)
+            r["frac_median_step"] = r["bound_ms"] / (float(np.median(steps_s)) * 1e3)
+            return r
+
         e2e_staged = {"value": world * nv * e2e_steps / copy_s, "unit": "params/s",
                       "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": e2e_steps,
+                      **step_stats(copy_steps),
                       "transfer": f"the gradients staged to HBM in {args.chunk_elems}-element chunks by the copy "
                                   "engines (zero1_staged_step), overlapping the step on the previous chunk; params "
                                   "and flag copied back",
-                      "roofline": link_roofline(link, bi, bo, copy_s / e2e_steps)}
+                      "roofline": roof(copy_s, copy_steps)}
         e2e = {"value": world * nv * e2e_steps / zero_s, "unit": "params/s",
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": e2e_steps,
+               **step_stats(zero_steps),
                "transfer": "every step the fused kernel reads the M gradient buffers from pinned host memory and "
                            "writes the bf16 params to pinned host memory over NVLink-C2C (no staging copy); "
                            "the flag is copied back and the stream synchronised",
-               "roofline": link_roofline(link, bi, bo, zero_s / e2e_steps)}
+               "roofline": roof(zero_s, zero_steps)}
         del host_g
 
     # with the state in host memory the step is bound by the host link: 12 B
@@ -588,12 +646,16 @@ def run_ours(args, w) -> None:
         # host-link steps see occasional stalls from other work on the shared
         # host: the median step against the same bound
         offload_link["frac_median_step"] = offload_link["bound_ms"] / float(np.median(launch_ms))
+        offload_link["ms_per_step_median"] = float(np.median(launch_ms))
+        offload_link["ms_per_step_min"] = float(launch_ms.min())
 
     if rank != 0:
         return
     peaks = measured_peaks()
     bytes_launch = op_bytes
     achieved = bytes_launch / (kernel_ms * 1e-3) / 1e9
+    traffic, traffic_note = (recorded_traffic(w.M, bytes_launch)
+                             if op == "step" and not args.state_on_host else (None, None))
     line = {
         "metric": METRIC,
         "value": world * nv * args.steps / (ms_total * 1e-3),
@@ -611,7 +673,7 @@ def run_ours(args, w) -> None:
         "hbm_gbs": bytes_launch * args.steps / (ms_total * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "peak_source": peaks["source"],
-                     "traffic": recorded_traffic(w.name) if op == "step" else None,
+                     "traffic": traffic, "traffic_source": traffic_note,
                      "kernel": op_kernel,
                      "bytes_per_launch": bytes_launch, "kernel_ms": kernel_ms,
                      "kernel_ms_median": float(np.median(launch_ms)), "kernel_ms_min": float(launch_ms.min())},
@@ -629,10 +691,10 @@ def run_ours(args, w) -> None:
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="gpt2_small_124M_M8")
+    ap.add_argument("--workload", default="flat_1.3B_M8")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-e2e", action="store_true")

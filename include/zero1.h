@@ -90,13 +90,16 @@ typedef struct CUstream_st *zero1_stream_t;
 #define ZERO1_DTYPE_F32 1
 
 /* Shard plan [PART], [Z1].  n real parameters in one flat buffer, padded to
- * P = ceil(n / (M*align)) * M*align; shard i is [i*s, (i+1)*s), s = P/M. */
+ * P = ceil(n / (M*align)) * M*align; shard i is [i*s, (i+1)*s), s = P/M.
+ * The flat buffer may be the concatenation of n_tensors tensors (a model's
+ * parameter list, flattened in order); shard cuts may fall inside a tensor. */
 typedef struct zero1_plan {
-    int64_t n;        /* |theta|, real parameters, >= 1 */
-    int64_t padded_n; /* P */
-    int64_t shard;    /* s = P / M */
-    int32_t M;        /* data-parallel degree (replicas), 1..ZERO1_MAX_REPLICAS */
-    int32_t align;    /* shard alignment unit in elements, >= 1 */
+    int64_t n;         /* |theta|, real parameters, >= 1 */
+    int64_t padded_n;  /* P */
+    int64_t shard;     /* s = P / M */
+    int32_t M;         /* data-parallel degree (replicas), 1..ZERO1_MAX_REPLICAS */
+    int32_t align;     /* shard alignment unit in elements, >= 1 */
+    int32_t n_tensors; /* tensors in the flat buffer; 0 when built without a list */
 } zero1_plan_t;
 
 /* AdamW hyperparameters of one step [OPT], the batch of [DP] and the loss
@@ -112,19 +115,27 @@ typedef struct zero1_adamw {
     int64_t step;        /* t >= 1; a skipped step does not advance it */
 } zero1_adamw_t;
 
-/* Build a plan [PART], [Z1].  Host only.  EINVAL if n < 1, align < 1 or
- * M < 1; ERANGE if M > ZERO1_MAX_REPLICAS or P overflows int64. */
-int zero1_plan(int64_t n, int32_t M, int32_t align, zero1_plan_t *out);
+/* Build a plan [PART], [Z1].  Host only; allocates nothing.
+ *  n, M, align:   as in zero1_plan_t;
+ *  tensor_numels: NULL (one flat buffer; n_tensors must be 0), or a host
+ *                 array of n_tensors >= 1 tensor sizes (each >= 0) that sum
+ *                 to n; the plan records n_tensors for zero1_plan_segments.
+ * EINVAL if n < 1, align < 1, M < 1 or the tensor list is inconsistent;
+ * ERANGE if M > ZERO1_MAX_REPLICAS or P overflows int64. */
+int zero1_plan(int64_t n, int32_t M, int32_t align, const int64_t *tensor_numels, int32_t n_tensors,
+               zero1_plan_t *out);
 
-/* Per-tensor pieces of shard `shard_index` when the flat buffer is the
- * concatenation of n_tensors tensors of tensor_numels[k] elements (their sum
- * must equal plan->n).  Host only.  Writes up to `cap` pieces: tensor index,
- * offset inside that tensor, offset inside the shard, length; *count gets the
- * number of pieces.  Padding belongs to no tensor.  EINVAL on bad arguments,
- * ERANGE if more than cap pieces are needed. */
-int zero1_plan_segments(const zero1_plan_t *plan, const int64_t *tensor_numels, int32_t n_tensors,
-                        int32_t shard_index, int32_t cap, int64_t *seg_tensor,
-                        int64_t *seg_tensor_offset, int64_t *seg_shard_offset, int64_t *seg_len,
+/* Per-tensor pieces of shard `shard_index` [PART], [Z1], for a plan built
+ * with a tensor list: tensor_numels is that list again (plan->n_tensors host
+ * int64 sizes summing to plan->n).  Host only.  Writes up to `cap` pieces, in
+ * shard order: the tensor index, the piece's first element inside that
+ * tensor (seg_begin) and its length.  The pieces tile the shard's real
+ * elements from the shard's first element on, so a piece's offset inside the
+ * shard is the sum of the lengths before it; padding belongs to no tensor.
+ * *count gets the number of pieces.  EINVAL on bad arguments or a plan built
+ * without tensors, ERANGE if more than cap pieces are needed. */
+int zero1_plan_segments(const zero1_plan_t *plan, const int64_t *tensor_numels, int32_t shard_index,
+                        int64_t *seg_tensor, int64_t *seg_begin, int64_t *seg_len, int32_t cap,
                         int32_t *count);
 
 /* Bytes per rank [MEM], [Z1]: naive data parallelism keeps 16 bytes of every
@@ -232,6 +243,9 @@ int zero1_step_bucket(const zero1_plan_t *plan, int64_t elem_begin, int64_t elem
 #define ZERO1_STAGE_GRADS 1
 #define ZERO1_STAGE_STATE 2
 #define ZERO1_STAGE_PARAMS 4
+/* Tracing: with this bit in `what` the handle also records CUDA timing
+ * events around each chunk's copies and kernel (zero1_staged_timeline). */
+#define ZERO1_STAGE_TIMELINE 8
 typedef struct zero1_staged zero1_staged_t;
 int zero1_staged_create(const zero1_plan_t *plan, int32_t shard_begin, int32_t shard_end, int32_t what,
                         int64_t chunk_elems, zero1_staged_t **out);
@@ -245,6 +259,17 @@ int zero1_staged_destroy(zero1_staged_t *handle);
  * smaller): chunks of chunk_elems (rounded up to a multiple of 8) elements,
  * the last one shorter. */
 int zero1_staged_chunks(const zero1_staged_t *handle, int64_t *cuts, int32_t cap, int32_t *count);
+
+/* Timeline of the handle's last step (tracing; the handle must have been
+ * created with ZERO1_STAGE_TIMELINE).  *count = chunks; if ms is not NULL it
+ * gets 6 floats per chunk, in chunk order, in milliseconds since the step
+ * started on the caller's stream: inbound copies start, inbound copies end,
+ * kernel start, kernel end, outbound copies start, outbound copies end (the
+ * last two -1 when nothing is copied back).  A start is when that stream
+ * reached the chunk, after its waits for the previous stage.  Waits for the
+ * last step to finish (synchronous).  EINVAL without the bit or before any
+ * step; ERANGE if cap < 6 x chunks. */
+int zero1_staged_timeline(zero1_staged_t *handle, float *ms, int32_t cap, int32_t *count);
 
 /* The fused step with its vector body staged through shared memory by the
  * Tensor Memory Accelerator [Z1], [DP], [MEM]: a producer warp issues 1-D bulk
@@ -471,13 +496,19 @@ int zero1_staged_step_dynamic(zero1_staged_t *handle, const void *const *grads, 
  * inside the library: ZERO1_NOALLOC_MAX_ELEMS floats (64 MiB) that every GPU
  * loading libzero1.so holds until the process exits.  The caller still
  * passes gradients, state, parameters, scaler and policy.
- *  - The range must satisfy L = (shard_end - shard_begin) * s <=
- *    ZERO1_NOALLOC_MAX_ELEMS; larger ranges return ZERO1_ERANGE before
- *    anything is launched (call it once per group of shards instead).
+ *  - One call is one whole attempt: it decides the skip for its whole range
+ *    and advances the scaler (t, S, the counters) once.  So the range must
+ *    fit: L = (shard_end - shard_begin) * s <= ZERO1_NOALLOC_MAX_ELEMS.  A
+ *    longer range returns ZERO1_ERANGE before anything is launched, with the
+ *    scaler untouched; it needs zero1_step_dynamic and a caller-provided
+ *    workspace (splitting one attempt over several calls would advance the
+ *    scaler several times and could skip only part of an overflowing step).
  *  - The first call on a device looks up the array's device address on that
  *    device (cudaGetSymbolAddress, with that device current); make that first
- *    call before any stream capture.  No cudaMalloc, cudaFree or other
- *    allocating routine is called.
+ *    call before any stream capture.  The address is looked up again only if
+ *    the device's current context is no longer the one it was looked up in
+ *    (after cudaDeviceReset).  No cudaMalloc, cudaFree or other allocating
+ *    routine is called.
  *  - All calls share the one array and it keeps the last call's sums; nothing
  *    in it needs to start at zero (each call writes all L sums before reading
  *    them).  Calls that overlap on the GPU (other streams, other threads) race
@@ -510,6 +541,16 @@ const char *zero1_last_error(void);
 
 /* ABI version, incremented on any incompatible change. */
 int zero1_abi_version(void);
+
+/* Introspection for tests and tuning (no counterpart in the pages): the last
+ * kernel that a library call launched on this host thread.  *kernel_name
+ * gets its (mangled) name, owned by the CUDA runtime; *grid the blocks it was
+ * launched with; *blocks_per_sm the resident blocks per SM the grid was
+ * sized from (one wave = SMs x blocks_per_sm, each kernel's own occupancy);
+ * *w32 1 if its vector body moved the fp32 arrays in 32-byte accesses, 0 if
+ * in 16-byte ones.  Any pointer may be NULL.  EINVAL if this thread has
+ * launched nothing yet; ECUDA if the runtime cannot name the kernel. */
+int zero1_debug_last_launch(const char **kernel_name, int32_t *grid, int32_t *blocks_per_sm, int32_t *w32);
 
 #ifdef __cplusplus
 }

@@ -39,7 +39,7 @@ def test_header_declares_the_boundary():
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), f"{name} declared in zero1.h but not exported"
-    assert lib.zero1_abi_version() == 1
+    assert lib.zero1_abi_version() == 2
 
 
 @pytest.mark.parametrize("n", [1, 2, 7, 8, 9, 1000, 4099, 10**6 + 3, 1_300_000_000, 7_500_000_000])
@@ -59,9 +59,30 @@ def test_segments_equal_oracle(lib):
     for numels in cases:
         n = sum(numels)
         for M in [1, 3, 8]:
-            p = z.zero1_plan(n, M, int(rng.choice([1, 8, 128])))
+            p = z.zero1_plan(n, M, int(rng.choice([1, 8, 128])), tensor_numels=numels)
+            assert p.n_tensors == len(numels)
             for i in range(M):
-                assert z.zero1_plan_segments(p, numels, i) == oracle.segments(numels, p.shard, i)
+                want = oracle.segments(numels, p.shard, i)
+                assert z.zero1_plan_segments(p, numels, i) == [(k, toff, ln) for k, toff, _, ln in want]
+                # the pieces tile the shard from its first element: the
+                # oracle's offsets inside the shard are the running lengths
+                assert [soff for _, _, soff, _ in want] == list(np.cumsum([0] + [ln for *_, ln in want])[:-1])
+
+
+def test_plan_tensor_list_validation(lib):
+    """The tensor list given to zero1_plan must sum to n; segments need it."""
+    p = z.Plan()
+    nums = (ctypes.c_int64 * 3)(5, 7, 11)
+    assert lib.zero1_plan(23, 2, 4, nums, 3, ctypes.byref(p)) == 0 and p.n_tensors == 3
+    assert lib.zero1_plan(24, 2, 4, nums, 3, ctypes.byref(p)) == -1     # sizes sum to 23, not 24
+    assert lib.zero1_plan(23, 2, 4, nums, 0, ctypes.byref(p)) == -1     # a list needs n_tensors >= 1
+    assert lib.zero1_plan(23, 2, 4, None, 2, ctypes.byref(p)) == -1     # no list: n_tensors must be 0
+    neg = (ctypes.c_int64 * 3)(30, -7, 0)
+    assert lib.zero1_plan(23, 2, 4, neg, 3, ctypes.byref(p)) == -1
+    flat = z.zero1_plan(23, 2, 4)
+    assert flat.n_tensors == 0
+    with pytest.raises(z.Zero1Error):
+        z.zero1_plan_segments(flat, [5, 7, 11], 0)                    # built without the list
 
 
 # --------------------------------------------------------- validation ------
@@ -96,12 +117,12 @@ def _fused(lib, plan, sb=0, se=None, grads=None, master=A, m=A + 4096, v=A + 819
 @no_gpu
 def test_plan_rejects_bad_arguments(lib):
     p = z.Plan()
-    assert lib.zero1_plan(0, 4, 1, ctypes.byref(p)) == -1
-    assert lib.zero1_plan(10, 0, 1, ctypes.byref(p)) == -1
-    assert lib.zero1_plan(10, 4, 0, ctypes.byref(p)) == -1
-    assert lib.zero1_plan(10, 65, 1, ctypes.byref(p)) == -3
-    assert lib.zero1_plan(2**63 - 6, 64, 1024, ctypes.byref(p)) == -3  # padding overflows int64
-    assert lib.zero1_plan(10, 4, 1, None) == -1
+    assert lib.zero1_plan(0, 4, 1, None, 0, ctypes.byref(p)) == -1
+    assert lib.zero1_plan(10, 0, 1, None, 0, ctypes.byref(p)) == -1
+    assert lib.zero1_plan(10, 4, 0, None, 0, ctypes.byref(p)) == -1
+    assert lib.zero1_plan(10, 65, 1, None, 0, ctypes.byref(p)) == -3
+    assert lib.zero1_plan(2**63 - 6, 64, 1024, None, 0, ctypes.byref(p)) == -3  # padding overflows int64
+    assert lib.zero1_plan(10, 4, 1, None, 0, None) == -1
 
 
 @no_gpu
@@ -158,7 +179,8 @@ def test_staged_handle_rejects_bad_arguments(lib):
     P = ctypes.byref(plan)
     h = ctypes.c_void_p()
     assert lib.zero1_staged_create(P, 0, 4, 0, 1024, ctypes.byref(h)) == -1        # nothing staged
-    assert lib.zero1_staged_create(P, 0, 4, 8, 1024, ctypes.byref(h)) == -1        # unknown bit
+    assert lib.zero1_staged_create(P, 0, 4, 8, 1024, ctypes.byref(h)) == -1        # tracing alone stages nothing
+    assert lib.zero1_staged_create(P, 0, 4, 16 | 2, 1024, ctypes.byref(h)) == -1   # unknown bit
     assert lib.zero1_staged_create(P, 0, 4, z.ZERO1_STAGE_STATE, 0, ctypes.byref(h)) == -1
     assert lib.zero1_staged_create(P, 2, 2, z.ZERO1_STAGE_STATE, 64, ctypes.byref(h)) == -1   # empty range
     assert lib.zero1_staged_create(P, 0, 5, z.ZERO1_STAGE_STATE, 64, ctypes.byref(h)) == -1
@@ -166,6 +188,8 @@ def test_staged_handle_rejects_bad_arguments(lib):
     assert h.value is None
     assert lib.zero1_staged_step(None, None, None, None, None, None, None, ctypes.byref(_hp()), None, None) == -1
     assert lib.zero1_staged_destroy(None) == 0
+    cnt = ctypes.c_int32()
+    assert lib.zero1_staged_timeline(None, None, 0, ctypes.byref(cnt)) == -1
     pol = ctypes.byref(z.LossScalePolicy().c_struct())
     assert lib.zero1_staged_step_dynamic(None, None, None, None, None, None, None, ctypes.byref(_hp()), None, pol,
                                          None) == -1                    # no scaler
@@ -221,20 +245,19 @@ int main(void)
     zero1_plan_t p;
     int64_t naive = 0, z1 = 0;
     int64_t numels[3] = {5, 7, 11};
-    int64_t t[4], toff[4], soff[4], len[4];
+    int64_t t[4], toff[4], len[4];
     int32_t count = 0;
-    if (zero1_plan(1300000000LL, 8, 128, &p) != ZERO1_OK) return 1;
-    if (p.padded_n != 1300000768LL || p.shard != 162500096LL) return 2;
+    if (zero1_plan(1300000000LL, 8, 128, NULL, 0, &p) != ZERO1_OK) return 1;
+    if (p.padded_n != 1300000768LL || p.shard != 162500096LL || p.n_tensors != 0) return 2;
     if (zero1_plan_memory(&p, &naive, &z1) != ZERO1_OK || naive != 16LL * 1300000000LL) return 3;
-    if (zero1_plan(23, 2, 4, &p) != ZERO1_OK) return 4;
-    if (zero1_plan_segments(&p, numels, 3, 1, 4, t, toff, soff, len, &count) != ZERO1_OK) return 5;
+    if (zero1_plan(23, 2, 4, numels, 3, &p) != ZERO1_OK || p.n_tensors != 3) return 4;
+    if (zero1_plan_segments(&p, numels, 1, t, toff, len, 4, &count) != ZERO1_OK) return 5;
     printf("%lld %lld %d", (long long)p.padded_n, (long long)p.shard, count);
-    for (int i = 0; i < count; ++i) printf(" (%lld,%lld,%lld,%lld)", (long long)t[i], (long long)toff[i],
-                                           (long long)soff[i], (long long)len[i]);
-    if (zero1_plan(10, 65, 1, &p) != ZERO1_ERANGE) return 6;
+    for (int i = 0; i < count; ++i) printf(" (%lld,%lld,%lld)", (long long)t[i], (long long)toff[i], (long long)len[i]);
+    if (zero1_plan(10, 65, 1, NULL, 0, &p) != ZERO1_ERANGE) return 6;
     if (strcmp(zero1_strerror(ZERO1_ERANGE), "size or replica count out of the supported range") != 0) return 7;
     printf(" | %s\n", zero1_last_error());
-    return zero1_abi_version() == 1 ? 0 : 8;
+    return zero1_abi_version() == 2 ? 0 : 8;
 }
 """
 
@@ -255,5 +278,5 @@ def test_header_is_plain_c_and_links(lib, tmp_path):
     P, s, count, *segs = head.split(" ")
     assert (int(P), int(s)) == oracle.plan(23, 2, 4)
     want = oracle.segments([5, 7, 11], int(s), 1)
-    assert int(count) == len(want) and segs == [f"({a},{b},{c},{d})" for a, b, c, d in want]
+    assert int(count) == len(want) and segs == [f"({a},{b},{d})" for a, b, c, d in want]
     assert "M = 65" in err

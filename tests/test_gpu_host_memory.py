@@ -11,6 +11,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import zero_sharded_mixed_zero1_gb300 as z
 from zero_sharded_mixed_zero1_gb300 import synth
 from gpu_helpers import assert_bf16_bits, assert_f32_bits, f32, oracle_hp, u16
@@ -103,6 +104,7 @@ def test_host_streamed_step_equals_fused_step(cuda_device, M, n, align, chunk, s
         gb = [pinned(g) for g in gb]
     host_p = torch.zeros(max(nv, 1), dtype=torch.bfloat16).pin_memory()
     step = z.HostStreamedStep(plan, sb, se, gb, *b, pb, chunk_elems=chunk, params_host=host_p)
+    o = [f32(t).copy() for t in a]                 # the oracle's copy of the range's state
     for t in (1, 2, 3, 4):
         grads = [g[base:base + nv] for g in make_grads(M, n, 1e-2, 91 + M, t, dev)]
         for x, g in zip(gb, grads):
@@ -112,10 +114,14 @@ def test_host_streamed_step_equals_fused_step(cuda_device, M, n, align, chunk, s
         z.zero1_reduce_scatter_adamw_allgather(plan, sb, se, grads, *a, pa, hp)
         step(hp)
         torch.cuda.synchronize()
-        for x, y, what in zip(a, b, ("master", "m", "v")):
+        o_p = np.zeros(nv, np.uint16)
+        oracle.zero1_step([np.ascontiguousarray(u16(g)) for g in grads], nv, *o, o_p, oracle_hp(hp))
+        for x, y, want, what in zip(a, b, o, ("master", "m", "v")):
             assert_f32_bits(f32(y), f32(x), f"{where}: {what} t={t}")
+            assert_f32_bits(f32(y), want, f"{where}: {what} t={t} vs oracle")
         assert_bf16_bits(u16(pb[:nv]), u16(pa[:nv]), f"{where}: params t={t}")
         assert_bf16_bits(u16(host_p[:nv]), u16(pa[:nv]), f"{where}: params on host t={t}")
+        assert_bf16_bits(u16(host_p[:nv]), o_p, f"{where}: params on host t={t} vs oracle")
 
 
 def test_host_streamed_step_is_ordered_on_its_stream(cuda_device):
@@ -261,8 +267,16 @@ def test_staged_dynamic_step_equals_device_dynamic_step(cuda_device, M, n, align
     z.zero1_scaler_init(s_b, policy, hp)
     sums = torch.empty(P, dtype=torch.float32, device=dev)
     step = z.HostStreamedStep(plan, 0, M, gb, *b, pb, chunk_elems=chunk, params_host=host_p)
+    # the oracle's attempts on its own copy of the state
+    o = [f32(t).copy() for t in a]
+    o_p = np.zeros(n, np.uint16)
+    o_policy = oracle.LossScalePolicy(initial_scale=policy.initial_scale, factor=policy.factor,
+                                      window=policy.window, hysteresis=policy.hysteresis, min_scale=policy.min_scale)
+    o_sc = oracle.Scaler.start(o_policy, hp.step)
+    o_hp = oracle_hp(hp)
     for k in range(7):
         S = z.scaler_state(s_a)["scale"]
+        assert S == o_sc.scale
         grads = make_grads(M, n, 1e-3 * S, 140 + M, k, dev)
         if k in (2, 3, 5):
             grads[k % M][(97 * k) % n] = float("inf") if k != 3 else float("nan")
@@ -272,12 +286,70 @@ def test_staged_dynamic_step_equals_device_dynamic_step(cuda_device, M, n, align
         z.zero1_step_dynamic(plan, 0, M, grads, *a, pa, hp, s_a, policy, sums)
         step.dynamic(hp, s_b, policy)
         torch.cuda.synchronize()
-        for x, y, what in zip(a, b, ("master", "m", "v")):
+        flag = oracle.zero1_dynamic_attempt([u16(g) for g in grads], n, *o, o_p, o_hp, o_sc, o_policy)
+        assert flag == (1 if k in (2, 3, 5) else 0)
+        for x, y, want, what in zip(a, b, o, ("master", "m", "v")):
             assert_f32_bits(f32(y), f32(x), f"{where}: {what} attempt {k}")
+            assert_f32_bits(f32(y), want, f"{where}: {what} attempt {k} vs oracle")
         assert_bf16_bits(u16(pb), u16(pa), f"{where}: params attempt {k}")
+        assert_bf16_bits(u16(pb), o_p, f"{where}: params attempt {k} vs oracle")
         if host_p is not None:
             assert_bf16_bits(u16(host_p), u16(pa), f"{where}: params on host attempt {k}")
-        assert z.scaler_state(s_b) == z.scaler_state(s_a)
+        st = z.scaler_state(s_b)
+        assert st == z.scaler_state(s_a)
+        assert (st["scale"], st["step"], st["attempts"], st["skipped"]) == \
+            (o_sc.scale, o_sc.step, o_sc.attempts, o_sc.skipped)
     st = z.scaler_state(s_b)
     assert st["skipped"] == 3 and st["step"] == 5
     step.close()
+
+
+@pytest.mark.parametrize("where", ["grads_params", "state"])
+def test_staged_timeline_is_ordered_and_changes_no_bit(cuda_device, where):
+    """With tracing on, the handle reports per-chunk times of its last step:
+    each chunk's stages in order (copies in, kernel, copies out), the inbound
+    copies of successive chunks one after another on their stream, no kernel
+    before its copies; and the step's results are the untraced step's bits."""
+    dev = cuda_device
+    M, n, chunk = 4, 200_003, 16384
+    plan = z.zero1_plan(n, M, 8)
+    P = plan.padded_n
+    a = make_state(n, P, 31, dev, nonzero_moments=True)
+    b = [t.clone() for t in a]
+    on_host = where == "state"
+    if on_host:
+        a, b = [pinned(t) for t in a], [pinned(t) for t in b]
+    grads = make_grads(M, n, 1e-2, 32, 1, dev)
+    host_g = [pinned(g) for g in grads]
+    gsrc = grads if on_host else host_g
+    pa = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+    pb = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+    ha = None if on_host else torch.zeros(n, dtype=torch.bfloat16).pin_memory()
+    hb = None if on_host else torch.zeros(n, dtype=torch.bfloat16).pin_memory()
+    plain = z.HostStreamedStep(plan, 0, M, gsrc, *a, pa, chunk_elems=chunk, params_host=ha)
+    traced = z.HostStreamedStep(plan, 0, M, gsrc, *b, pb, chunk_elems=chunk, params_host=hb, timeline=True)
+    with pytest.raises(z.Zero1Error):
+        traced.timeline()                            # no step yet
+    for t in (1, 2):
+        hp = z.AdamW(global_batch=64, step=t)
+        plain(hp)
+        traced(hp)
+        torch.cuda.synchronize()
+        tl = traced.timeline()
+        assert tl.shape == (len(traced.pieces), 6)
+        eps = 0.005                                  # event timestamps resolve to about half a microsecond
+        for k in range(tl.shape[0]):
+            i0, i1, c0, c1, o0, o1 = tl[k]
+            assert -eps <= i0 <= i1 + eps and i1 <= c0 + eps and c0 <= c1 + eps
+            assert c1 <= o0 + eps and o0 <= o1 + eps
+            if k:
+                assert tl[k - 1][1] <= i0 + eps      # one inbound stream: chunk after chunk
+        for x, y, what in zip(a, b, ("master", "m", "v")):
+            assert_f32_bits(f32(y), f32(x), f"traced {what} t={t}")
+        assert_bf16_bits(u16(pb), u16(pa), f"traced params t={t}")
+        if ha is not None:
+            assert_bf16_bits(u16(hb), u16(ha), f"traced host params t={t}")
+    with pytest.raises(z.Zero1Error):
+        plain.timeline()                             # created without tracing
+    plain.close()
+    traced.close()

@@ -1,0 +1,57 @@
+"""Launch shapes the library picks: each kernel's grid is one resident wave
+sized from that kernel's own occupancy, whatever ran before it in the
+process, and the vector body moves fp32 in 32-byte accesses whenever the
+buffers allow it.  (Results are checked bit for bit elsewhere; this checks
+the shapes that the measured rooflines rely on.)"""
+import pytest
+import torch
+
+import zero_sharded_mixed_zero1_gb300 as z
+from test_gpu_parity import make_grads, make_state
+
+pytestmark = pytest.mark.gpu
+
+
+def _sms() -> int:
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+def _fused(dev, n, M, state_offset=0):
+    plan = z.zero1_plan(n, M, 1)
+    P = plan.padded_n
+    grads = make_grads(M, n, 1e-3, 7, 1, dev)
+    master, m, v = (torch.cat([torch.zeros(state_offset, device=dev), t])[state_offset:]
+                    for t in make_state(n, P, 8, dev))
+    params = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+    z.zero1_reduce_scatter_adamw_allgather(plan, 0, M, grads, master, m, v, params, z.AdamW(global_batch=64))
+    torch.cuda.synchronize()
+    return z.debug_last_launch()
+
+
+def test_each_kernel_gets_its_own_occupancy(cuda_device):
+    """The small-range kernel (up to four blocks per SM) and the pipelined
+    large-range kernel (one block per SM at M = 8) share a signature; a call
+    of one must not fix the grid of the other."""
+    dev = cuda_device
+    sms = _sms()
+    big, small = 8 << 20, 1 << 16            # 8M elements: pipelined kernel; 64K: small-range kernel
+    first_big = _fused(dev, big, 8)
+    first_small = _fused(dev, small, 8)
+    again_big = _fused(dev, big, 8)
+    assert "k_fused_step_wide" in first_small["kernel"] and "k_fused_step_wide" not in first_big["kernel"]
+    assert first_big == again_big
+    assert first_big["blocks_per_sm"] == 1
+    assert first_small["blocks_per_sm"] >= 2
+    assert first_big["grid"] == sms * first_big["blocks_per_sm"]
+    # the small range needs fewer blocks than a wave: one vector of 8 per thread
+    assert first_small["grid"] == min(sms * first_small["blocks_per_sm"], -(-small // 8 // 256))
+
+
+def test_fp32_arrays_move_in_32_byte_accesses_when_aligned(cuda_device):
+    """torch's allocations are 32-byte aligned: the vector body uses 32-byte
+    fp32 accesses; state starting 16 bytes past a 32-byte boundary falls back
+    to 16-byte accesses (same bits, checked by the parity tests)."""
+    dev = cuda_device
+    assert _fused(dev, 1 << 20, 4)["w32"] is True
+    # master/m/v shifted by 4 floats (16 bytes) against the gradients
+    assert _fused(dev, 1 << 20, 4, state_offset=4)["w32"] is False

@@ -266,8 +266,15 @@ def test_allreduce_matches_oracle_and_equals_rs_plus_ag(cuda_device, M, n):
     for r in range(M):
         assert torch.equal(gathered[r].view(torch.int16), outs[r].view(torch.int16))
     assert not u16(shards[n:]).any()
-    # in place: outputs alias the inputs
+    # separate outputs run the instance that reads the gradients through the
+    # read-only path
+    z.dp_allreduce(plan, grads, outs, scale)
+    last = z.debug_last_launch()
+    assert "k_allreduce" in last["kernel"] and "k_allreduce_inplace" not in last["kernel"]
+    # in place: outputs alias the inputs, so the coherent-load instance runs
     z.dp_allreduce(plan, grads, grads, scale)
+    last = z.debug_last_launch()
+    assert "k_allreduce_inplace" in last["kernel"], last
     for r in range(M):
         assert_bf16_bits(u16(grads[r]), want[r], f"AR in place {r}")
 

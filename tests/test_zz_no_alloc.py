@@ -3,15 +3,17 @@ caller (for programs whose pool allocator owns the device memory, or that
 must not call cudaMalloc/cudaFree because those can synchronise the device).
 
 It is called through the C ABI (ctypes on libzero1.so) and must give the same
-bits as zero1_step_dynamic with a caller-provided workspace, on two calls in
-a row.  This file is collected last so that a run stopping at the first
-failure has run every other test first; it also passes alone in a fresh
-process."""
+bits as zero1_step_dynamic with a caller-provided workspace, and as the CPU
+oracle's dynamically scaled attempt, on two calls in a row.  This file is
+collected last so that a run stopping at the first failure has run every
+other test first; it also passes alone in a fresh process."""
 import ctypes
 
+import numpy as np
 import pytest
 import torch
 
+import oracle
 import zero_sharded_mixed_zero1_gb300 as z
 from zero_sharded_mixed_zero1_gb300 import _lib
 from zero_sharded_mixed_zero1_gb300 import synth
@@ -54,6 +56,14 @@ def test_no_alloc_step_matches_workspace_step_on_two_calls(cuda_device):
     z.zero1_scaler_init(sb, policy, hp)
     sums = torch.empty(P, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream().cuda_stream
+    # the oracle's copy of the state, its scaler and its parameters
+    o = [f32(t).copy() for t in a]
+    o_params = np.zeros(n, np.uint16)
+    o_policy = oracle.LossScalePolicy(initial_scale=policy.initial_scale, factor=policy.factor,
+                                      window=policy.window, hysteresis=policy.hysteresis, min_scale=policy.min_scale)
+    o_scaler = oracle.Scaler.start(o_policy, hp.step)
+    o_hp = oracle.AdamW(lr=hp.lr, beta1=hp.beta1, beta2=hp.beta2, eps=hp.eps, weight_decay=hp.weight_decay,
+                        global_batch=hp.global_batch)
     for call in range(2):
         grads = [synth.normal_bf16(n, 1e-3 * 1024, synth.seed_of(6, call, r), dev) for r in range(M)]
         if call == 1:
@@ -64,10 +74,17 @@ def test_no_alloc_step_matches_workspace_step_on_two_calls(cuda_device):
                 ctypes.byref(hp.c_struct()), sb.data_ptr(), ctypes.byref(policy.c_struct()), stream)
         assert rc == 0, lib.zero1_last_error()
         torch.cuda.synchronize()
-        for x, y, what in zip(a, b, ("master", "m", "v")):
+        flag = oracle.zero1_dynamic_attempt([u16(g) for g in grads], n, *o, o_params, o_hp, o_scaler, o_policy)
+        assert flag == call
+        for x, y, want, what in zip(a, b, o, ("master", "m", "v")):
             assert_f32_bits(f32(y), f32(x), f"{what} call {call}")
+            assert_f32_bits(f32(y), want, f"{what} call {call} against the oracle")
         assert_bf16_bits(u16(pb), u16(pa), f"params call {call}")
-        assert z.scaler_state(sa) == z.scaler_state(sb)
+        assert_bf16_bits(u16(pb), o_params, f"params call {call} against the oracle")
+        st = z.scaler_state(sb)
+        assert z.scaler_state(sa) == st
+        assert (st["scale"], st["step"], st["attempts"], st["skipped"]) == \
+            (o_scaler.scale, o_scaler.step, o_scaler.attempts, o_scaler.skipped)
     st = z.scaler_state(sb)
     assert st["attempts"] == 2 and st["skipped"] == 1 and st["step"] == 2
 
@@ -86,12 +103,17 @@ def test_no_alloc_step_rejects_ranges_beyond_its_workspace(cuda_device):
     hp = z.AdamW(global_batch=8)
     policy = z.LossScalePolicy()
     scaler = z.new_scaler(dev)
+    z.zero1_scaler_init(scaler, policy, hp)
+    before = z.scaler_state(scaler)
     one = torch.zeros(8, dtype=torch.float32, device=dev)
     gp = (ctypes.c_void_p * M)(*[one.data_ptr()] * M)
     rc = fn(ctypes.byref(plan), 0, M, gp, one.data_ptr(), one.data_ptr(), one.data_ptr(), one.data_ptr(),
             ctypes.byref(hp.c_struct()), scaler.data_ptr(), ctypes.byref(policy.c_struct()), None)
     assert rc == -3
     assert b"exceeds the built-in workspace" in lib.zero1_last_error()
+    torch.cuda.synchronize()
+    # nothing was launched: the scaler (S, t, counters) is exactly as before
+    assert z.scaler_state(scaler) == before
     # the binding refuses tensors shorter than the range before reaching the library
     g16 = torch.zeros(8, dtype=torch.bfloat16, device=dev)
     with pytest.raises(ValueError):

@@ -12,6 +12,7 @@ from ._lib import (  # noqa: F401
     ZERO1_STAGE_GRADS,
     ZERO1_STAGE_PARAMS,
     ZERO1_STAGE_STATE,
+    ZERO1_STAGE_TIMELINE,
     ZERO1_MAX_REPLICAS,
     SCALER_BYTES,
     AdamW,
@@ -46,5 +47,6 @@ from ._lib import (  # noqa: F401
     zero1_pingpong_finish,
     PingPongBuckets,
     current_state,
+    debug_last_launch,
 )
 from .host_stream import HostStreamedStep  # noqa: E402,F401

@@ -21,7 +21,7 @@ from . import build as _build
 ZERO1_OK, ZERO1_EINVAL, ZERO1_EALIGN, ZERO1_ERANGE, ZERO1_ECUDA = 0, -1, -2, -3, -4
 ZERO1_MAX_REPLICAS = 64
 ZERO1_DTYPE_BF16, ZERO1_DTYPE_F32 = 0, 1
-ZERO1_STAGE_GRADS, ZERO1_STAGE_STATE, ZERO1_STAGE_PARAMS = 1, 2, 4
+ZERO1_STAGE_GRADS, ZERO1_STAGE_STATE, ZERO1_STAGE_PARAMS, ZERO1_STAGE_TIMELINE = 1, 2, 4, 8
 
 _lib = None
 
@@ -32,11 +32,15 @@ class Zero1Error(RuntimeError):
         self.code = code
 
 
+# zero1_abi_version() of the library this binding is written for.
+ABI_VERSION = 2
+
+
 class Plan(ctypes.Structure):
     """zero1_plan_t: n real parameters padded to P = multiple of M*align,
     shard size s = P/M."""
     _fields_ = [("n", ctypes.c_int64), ("padded_n", ctypes.c_int64), ("shard", ctypes.c_int64),
-                ("M", ctypes.c_int32), ("align", ctypes.c_int32)]
+                ("M", ctypes.c_int32), ("align", ctypes.c_int32), ("n_tensors", ctypes.c_int32)]
 
     def shard_range(self, shard_begin: int, shard_end: int) -> tuple[int, int, int]:
         """(base element, length L, real elements nv) of shards [begin, end)."""
@@ -46,7 +50,7 @@ class Plan(ctypes.Structure):
 
     def __repr__(self):
         return (f"Plan(n={self.n}, padded_n={self.padded_n}, shard={self.shard}, "
-                f"M={self.M}, align={self.align})")
+                f"M={self.M}, align={self.align}, n_tensors={self.n_tensors})")
 
 
 class _AdamWStruct(ctypes.Structure):
@@ -127,8 +131,8 @@ def load() -> ctypes.CDLL:
     P = ctypes.POINTER(Plan)
     A = ctypes.POINTER(_AdamWStruct)
     sig = {
-        "zero1_plan": [i64, i32, i32, P],
-        "zero1_plan_segments": [P, vp, i32, i32, i32, vp, vp, vp, vp, vp],
+        "zero1_plan": [i64, i32, i32, vp, i32, P],
+        "zero1_plan_segments": [P, vp, i32, vp, vp, vp, i32, vp],
         "zero1_plan_memory": [P, vp, vp],
         "zero1_reduce_scatter_adamw_allgather": [P, i32, i32, vp, vp, vp, vp, vp, A, vp, i32, vp],
         "zero1_overflow_check": [P, i32, i32, vp, vp, vp],
@@ -152,6 +156,7 @@ def load() -> ctypes.CDLL:
         "zero1_staged_step": [vp, vp, vp, vp, vp, vp, vp, A, vp, vp],
         "zero1_staged_destroy": [vp],
         "zero1_staged_chunks": [vp, vp, i32, vp],
+        "zero1_staged_timeline": [vp, vp, i32, vp],
         "zero1_staged_step_dynamic": [vp, vp, vp, vp, vp, vp, vp, A, vp, ctypes.POINTER(_PolicyStruct), vp],
     }
     for name, args in sig.items():
@@ -164,6 +169,11 @@ def load() -> ctypes.CDLL:
     lib.zero1_last_error.restype = ctypes.c_char_p
     lib.zero1_abi_version.argtypes = []
     lib.zero1_abi_version.restype = ctypes.c_int
+    lib.zero1_debug_last_launch.argtypes = [ctypes.POINTER(ctypes.c_char_p), vp, vp, vp]
+    lib.zero1_debug_last_launch.restype = ctypes.c_int
+    if lib.zero1_abi_version() != ABI_VERSION:
+        raise ImportError(f"libzero1.so has ABI version {lib.zero1_abi_version()}, the binding expects "
+                          f"{ABI_VERSION}; rebuild it")
     _lib = lib
     return lib
 
@@ -219,21 +229,39 @@ def _replicas(plan: Plan, tensors, what: str) -> None:
 
 # -- plan ---------------------------------------------------------------------
 
-def zero1_plan(n: int, M: int, align: int = 1) -> Plan:
+def zero1_plan(n: int, M: int, align: int = 1, tensor_numels=None) -> Plan:
+    """The shard plan; tensor_numels (optional) lists the tensors the flat
+    buffer concatenates, for zero1_plan_segments."""
     p = Plan()
-    _check_rc(load().zero1_plan(n, M, align, ctypes.byref(p)))
+    if tensor_numels is None:
+        _check_rc(load().zero1_plan(n, M, align, None, 0, ctypes.byref(p)))
+    else:
+        nums = (ctypes.c_int64 * len(tensor_numels))(*tensor_numels)
+        _check_rc(load().zero1_plan(n, M, align, nums, len(tensor_numels), ctypes.byref(p)))
     return p
 
 
 def zero1_plan_segments(plan: Plan, tensor_numels, shard_index: int):
-    """[(tensor index, offset in tensor, offset in shard, length)]."""
+    """[(tensor index, first element inside the tensor, length)] of one
+    shard, in shard order; the plan must have been built with the list."""
     nums = (ctypes.c_int64 * len(tensor_numels))(*tensor_numels)
     cap = len(tensor_numels) + 1
-    outs = [(ctypes.c_int64 * cap)() for _ in range(4)]
+    outs = [(ctypes.c_int64 * cap)() for _ in range(3)]
     count = ctypes.c_int32()
-    _check_rc(load().zero1_plan_segments(ctypes.byref(plan), nums, len(tensor_numels), shard_index, cap,
-                                         *outs, ctypes.byref(count)))
+    _check_rc(load().zero1_plan_segments(ctypes.byref(plan), nums, shard_index, *outs, cap, ctypes.byref(count)))
     return [tuple(int(o[i]) for o in outs) for i in range(count.value)]
+
+
+def debug_last_launch() -> dict:
+    """The last kernel launched by a library call on this host thread: its
+    (mangled) name, grid, the resident blocks per SM the grid was sized from,
+    and whether the vector body moved fp32 in 32-byte accesses."""
+    name = ctypes.c_char_p()
+    grid, per_sm, w32 = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    _check_rc(load().zero1_debug_last_launch(ctypes.byref(name), ctypes.byref(grid), ctypes.byref(per_sm),
+                                             ctypes.byref(w32)))
+    return {"kernel": name.value.decode(), "grid": grid.value, "blocks_per_sm": per_sm.value,
+            "w32": bool(w32.value)}
 
 
 def zero1_plan_memory(plan: Plan) -> tuple[int, int]:

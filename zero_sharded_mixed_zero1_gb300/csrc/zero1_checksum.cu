@@ -75,7 +75,7 @@ extern "C" int zero1_checksum(const void *data, int64_t nbytes, uint64_t *out, z
     if (U == 0) return ZERO1_OK;
     const ArrayRef arr[1] = {{data, 2}};
     const Walk w = make_walk(U, U, arr, 1);
-    const int grid = grid_for(k_checksum16, work_of(w));
+    const int grid = grid_for(k_checksum16, w);
     k_checksum16<<<grid, kBlock, 0, st>>>(static_cast<const uint16_t *>(data), w,
                                          reinterpret_cast<unsigned long long *>(out));
     return launch_status("checksum launch");

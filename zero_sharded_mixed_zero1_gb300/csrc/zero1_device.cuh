@@ -12,6 +12,7 @@
 
 #include <atomic>
 #include <cmath>
+#include <mutex>
 #include <type_traits>
 
 #include "zero1.h"
@@ -32,9 +33,11 @@ struct OutPtrs {
 // How a range of L elements is walked: [0, head) per element, then nvec
 // aligned 8-element vectors [head, head + 8*nvec) that are all real
 // parameters, then [head + 8*nvec, L) per element (real below nv, padding
-// above).
+// above).  w32 != 0 when every fp32 array is also 32-byte aligned at the
+// vectors, so that a vector's 8 floats move in one 32-byte access.
 struct Walk {
     int64_t L, nv, head, nvec;
+    int32_t w32;
 };
 
 // ---------------------------------------------------------------- helpers --
@@ -53,6 +56,35 @@ __device__ __forceinline__ uint16_t ld_stream_u16(const uint16_t *p)
     uint16_t r;
     asm("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(r) : "l"(p));
     return r;
+}
+
+// Gradient loads.  NC: through the read-only (non-coherent) path, for
+// kernels that write nothing overlapping the gradients; otherwise ordinary
+// (coherent) global loads, for an in-place kernel whose outputs alias them.
+template <bool NC>
+__device__ __forceinline__ uint4 ld_grad_u4(const void *p)
+{
+    if constexpr (NC) {
+        return ld_stream_u4(p);
+    } else {
+        uint4 r;
+        asm("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+            : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+            : "l"(p));
+        return r;
+    }
+}
+
+template <bool NC>
+__device__ __forceinline__ uint16_t ld_grad_u16(const uint16_t *p)
+{
+    if constexpr (NC) {
+        return ld_stream_u16(p);
+    } else {
+        uint16_t r;
+        asm("ld.global.L1::no_allocate.u16 %0, [%1];" : "=h"(r) : "l"(p));
+        return r;
+    }
 }
 
 // bf16 -> fp32 is exact: the bf16 code is the upper half of the binary32.
@@ -89,20 +121,20 @@ __device__ __forceinline__ uint16_t to_bf16(float x)
 // Rank-order fp32 sum of 8 consecutive elements starting at j (16-byte
 // aligned in every replica).  MT > 0: M == MT known at compile time, all M
 // loads issued before the first add.  MT == 0: any M >= 8, in groups of 8.
-template <int MT>
+template <int MT, bool NC = true>
 __device__ __forceinline__ void sum8(const GradPtrs &g, int M, int64_t j, float s[kVec])
 {
     if constexpr (MT > 0) {
         uint4 q[MT];
 #pragma unroll
-        for (int r = 0; r < MT; ++r) q[r] = ld_stream_u4(g.p[r] + j);
+        for (int r = 0; r < MT; ++r) q[r] = ld_grad_u4<NC>(g.p[r] + j);
         unpack8(q[0], s);
 #pragma unroll
         for (int r = 1; r < MT; ++r) add8(q[r], s);
     } else {
         uint4 q[8];
 #pragma unroll
-        for (int r = 0; r < 8; ++r) q[r] = ld_stream_u4(g.p[r] + j);
+        for (int r = 0; r < 8; ++r) q[r] = ld_grad_u4<NC>(g.p[r] + j);
         unpack8(q[0], s);
 #pragma unroll
         for (int r = 1; r < 8; ++r) add8(q[r], s);
@@ -110,7 +142,7 @@ __device__ __forceinline__ void sum8(const GradPtrs &g, int M, int64_t j, float 
             const int cnt = M - r0 < 8 ? M - r0 : 8;
 #pragma unroll
             for (int k = 0; k < 8; ++k)
-                if (k < cnt) q[k] = ld_stream_u4(g.p[r0 + k] + j);
+                if (k < cnt) q[k] = ld_grad_u4<NC>(g.p[r0 + k] + j);
 #pragma unroll
             for (int k = 0; k < 8; ++k)
                 if (k < cnt) add8(q[k], s);
@@ -118,10 +150,11 @@ __device__ __forceinline__ void sum8(const GradPtrs &g, int M, int64_t j, float 
     }
 }
 
+template <bool NC = true>
 __device__ __forceinline__ float sum1(const GradPtrs &g, int M, int64_t j)
 {
-    float s = bf_one(ld_stream_u16(g.p[0] + j));
-    for (int r = 1; r < M; ++r) s = __fadd_rn(s, bf_one(ld_stream_u16(g.p[r] + j)));
+    float s = bf_one(ld_grad_u16<NC>(g.p[0] + j));
+    for (int r = 1; r < M; ++r) s = __fadd_rn(s, bf_one(ld_grad_u16<NC>(g.p[r] + j)));
     return s;
 }
 
@@ -200,26 +233,113 @@ __device__ __forceinline__ void st_stream(float *p, float a, float b, float c, f
     __stcs(reinterpret_cast<float4 *>(p), make_float4(a, b, c, d));
 }
 
-// AdamW on one 8-element vector whose replica sums are in s, then the
-// streaming stores of master/m/v and the bf16 parameters.
-__device__ __forceinline__ void store_vec(const float s[kVec], float4 w0, float4 w1, float4 m0, float4 m1,
-                                          float4 v0, float4 v1, float *pw, float *pm, float *pv, uint16_t *pp,
-                                          const Z1Consts &c, bool &bad)
+// The 8 fp32 values of one vector.  With w32 (the walk found every fp32
+// array 32-byte aligned) they move in one 256-bit access per thread, so a
+// warp's access covers 1 KiB of consecutive bytes and uses every 32-byte
+// sector it touches in full; otherwise in two 128-bit accesses, where each
+// warp instruction touches 32 sectors and uses half of each.  w32 is the
+// same for every thread of the grid (a kernel argument), so the branch never
+// diverges.
+struct F8 {
+    float4 lo, hi;
+};
+
+#define Z1_LD8(op, p, r)                                                                              \
+    asm(op " {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"                                                  \
+        : "=f"((r).lo.x), "=f"((r).lo.y), "=f"((r).lo.z), "=f"((r).lo.w), "=f"((r).hi.x), "=f"((r).hi.y), \
+          "=f"((r).hi.z), "=f"((r).hi.w)                                                               \
+        : "l"(p))
+
+// L1::no_allocate, as ld_state.
+__device__ __forceinline__ F8 ld_state8(const float *p, bool w32)
 {
-    float ww[kVec] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-    float mm[kVec] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-    float vv[kVec] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    F8 r;
+    if (w32) {
+        Z1_LD8("ld.global.L1::no_allocate.v8.f32", p, r);
+    } else {
+        r.lo = ld_state(p);
+        r.hi = ld_state(p + 4);
+    }
+    return r;
+}
+
+// Evict-first (.cs): a stream read once.
+__device__ __forceinline__ F8 ld_cs8(const float *p, bool w32)
+{
+    F8 r;
+    if (w32) {
+        Z1_LD8("ld.global.cs.v8.f32", p, r);
+    } else {
+        r.lo = __ldcs(reinterpret_cast<const float4 *>(p));
+        r.hi = __ldcs(reinterpret_cast<const float4 *>(p) + 1);
+    }
+    return r;
+}
+
+// The default cache policy.
+__device__ __forceinline__ F8 ld_plain8(const float *p, bool w32)
+{
+    F8 r;
+    if (w32) {
+        Z1_LD8("ld.global.v8.f32", p, r);
+    } else {
+        r.lo = reinterpret_cast<const float4 *>(p)[0];
+        r.hi = reinterpret_cast<const float4 *>(p)[1];
+    }
+    return r;
+}
+
+// Which kernels store fp32 in 32-byte accesses (each passes w32 && its
+// policy as st_stream8's flag).  Measured on GB300 with CUDA events, every
+// other choice equal: 32-byte loads never lost, but 32-byte stores pay only
+// where the writes go to a separate buffer (ping-pong copies, reduce-scatter
+// and all-reduce outputs) or make up about half of an in-place update's
+// traffic (the dynamic step's update from sums; the fused step at M <= 2,
+// +2.5 %); an in-place update that reads far more than it writes ran 1-7 %
+// slower with them (the fused step from M = 4, 7 % at M = 64).
+__host__ __device__ constexpr bool wide_stores_in_place(int MT) { return MT >= 1 && MT <= 2; }
+
+// Streaming (.cs) store of 8 floats: one 32-byte access if w32, else two
+// 16-byte ones.
+__device__ __forceinline__ void st_stream8(float *p, const float x[kVec], bool w32)
+{
+    if (w32) {
+        asm volatile("st.global.cs.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                     :
+                     : "l"(p), "f"(x[0]), "f"(x[1]), "f"(x[2]), "f"(x[3]), "f"(x[4]), "f"(x[5]), "f"(x[6]),
+                       "f"(x[7])
+                     : "memory");
+    } else {
+        st_stream(p, x[0], x[1], x[2], x[3]);
+        st_stream(p + 4, x[4], x[5], x[6], x[7]);
+    }
+}
+
+__device__ __forceinline__ void unpack_f8(const F8 &x, float a[kVec])
+{
+    a[0] = x.lo.x; a[1] = x.lo.y; a[2] = x.lo.z; a[3] = x.lo.w;
+    a[4] = x.hi.x; a[5] = x.hi.y; a[6] = x.hi.z; a[7] = x.hi.w;
+}
+
+// AdamW on one 8-element vector whose replica sums are in s, then the
+// streaming stores of master/m/v (32-byte accesses if ws) and the bf16
+// parameters.
+__device__ __forceinline__ void store_vec(const float s[kVec], const F8 &w, const F8 &m, const F8 &v, float *pw,
+                                          float *pm, float *pv, uint16_t *pp, const Z1Consts &c, bool &bad,
+                                          bool ws)
+{
+    float ww[kVec], mm[kVec], vv[kVec];
+    unpack_f8(w, ww);
+    unpack_f8(m, mm);
+    unpack_f8(v, vv);
 #pragma unroll
     for (int k = 0; k < kVec; ++k) {
         bad |= !finite(s[k]);
         adamw1(__fmul_rn(s[k], c.inv), c, ww[k], mm[k], vv[k]);
     }
-    st_stream(pw, ww[0], ww[1], ww[2], ww[3]);
-    st_stream(pw + 4, ww[4], ww[5], ww[6], ww[7]);
-    st_stream(pm, mm[0], mm[1], mm[2], mm[3]);
-    st_stream(pm + 4, mm[4], mm[5], mm[6], mm[7]);
-    st_stream(pv, vv[0], vv[1], vv[2], vv[3]);
-    st_stream(pv + 4, vv[4], vv[5], vv[6], vv[7]);
+    st_stream8(pw, ww, ws);
+    st_stream8(pm, mm, ws);
+    st_stream8(pv, vv, ws);
     __stcs(reinterpret_cast<uint4 *>(pp),
            make_uint4(pack_bf16x2(ww[0], ww[1]), pack_bf16x2(ww[2], ww[3]), pack_bf16x2(ww[4], ww[5]),
                       pack_bf16x2(ww[6], ww[7])));
@@ -230,18 +350,15 @@ __device__ __forceinline__ void store_vec(const float s[kVec], float4 w0, float4
 template <int MT>
 struct VecLoads {
     uint4 q[MT];
-    float4 w0, w1, m0, m1, v0, v1;
+    F8 w, m, v;
     __device__ __forceinline__ void load(const GradPtrs &g, const float *master, const float *mom,
-                                         const float *var, int64_t j)
+                                         const float *var, int64_t j, bool w32)
     {
 #pragma unroll
         for (int r = 0; r < MT; ++r) q[r] = ld_stream_u4(g.p[r] + j);
-        w0 = ld_state(master + j);
-        w1 = ld_state(master + j + 4);
-        m0 = ld_state(mom + j);
-        m1 = ld_state(mom + j + 4);
-        v0 = ld_state(var + j);
-        v1 = ld_state(var + j + 4);
+        w = ld_state8(master + j, w32);
+        m = ld_state8(mom + j, w32);
+        v = ld_state8(var + j, w32);
     }
 };
 
@@ -270,25 +387,21 @@ __device__ __forceinline__ void fused_scalar_rest(const GradPtrs &g, int M, floa
 
 // AdamW on fp32 state given the scaled fp32 gradient.
 struct StateLoads {
-    float4 g0, g1, w0, w1, m0, m1, v0, v1;
+    F8 g, w, m, v;
 };
 
 __device__ __forceinline__ void load_state_vec(StateLoads &x, const float *gin, const float *master,
-                                               const float *mom, const float *var, int64_t j)
+                                               const float *mom, const float *var, int64_t j, bool w32)
 {
-    x.g0 = __ldcs(reinterpret_cast<const float4 *>(gin + j));
-    x.g1 = __ldcs(reinterpret_cast<const float4 *>(gin + j + 4));
-    x.w0 = ld_state(master + j);
-    x.w1 = ld_state(master + j + 4);
-    x.m0 = ld_state(mom + j);
-    x.m1 = ld_state(mom + j + 4);
-    x.v0 = ld_state(var + j);
-    x.v1 = ld_state(var + j + 4);
+    x.g = ld_cs8(gin + j, w32);
+    x.w = ld_state8(master + j, w32);
+    x.m = ld_state8(mom + j, w32);
+    x.v = ld_state8(var + j, w32);
 }
 
 // Reduce-scatter: out[j] = sum * scale (fp32 or bf16), +0 on padding.
 template <bool BF16>
-__device__ __forceinline__ void rs_store(void *out, int64_t j, float s[kVec], float scale)
+__device__ __forceinline__ void rs_store(void *out, int64_t j, float s[kVec], float scale, bool w32)
 {
 #pragma unroll
     for (int k = 0; k < kVec; ++k) s[k] = __fmul_rn(s[k], scale);
@@ -297,8 +410,7 @@ __device__ __forceinline__ void rs_store(void *out, int64_t j, float s[kVec], fl
                make_uint4(pack_bf16x2(s[0], s[1]), pack_bf16x2(s[2], s[3]), pack_bf16x2(s[4], s[5]),
                           pack_bf16x2(s[6], s[7])));
     } else {
-        st_stream(static_cast<float *>(out) + j, s[0], s[1], s[2], s[3]);
-        st_stream(static_cast<float *>(out) + j + 4, s[4], s[5], s[6], s[7]);
+        st_stream8(static_cast<float *>(out) + j, s, w32);
     }
 }
 
@@ -325,7 +437,7 @@ k_reduce_scatter(const __grid_constant__ GradPtrs g, int M, const Walk w, float 
                 for (int r = 1; r < MT; ++r) add8(x.q[r], s);
 #pragma unroll
                 for (int k = 0; k < kVec; ++k) bad |= !finite(s[k]);
-                rs_store<BF16>(out, w.head + i * kVec, s, scale);
+                rs_store<BF16>(out, w.head + i * kVec, s, scale, w.w32);
             });
     } else {
         for (int64_t i = tid; i < w.nvec; i += nthr) {
@@ -334,7 +446,7 @@ k_reduce_scatter(const __grid_constant__ GradPtrs g, int M, const Walk w, float 
             sum8<0>(g, M, j, s);
 #pragma unroll
             for (int k = 0; k < kVec; ++k) bad |= !finite(s[k]);
-            rs_store<BF16>(out, j, s, scale);
+            rs_store<BF16>(out, j, s, scale, w.w32);
         }
     }
     const int64_t ns = w.L - w.nvec * kVec;
@@ -360,18 +472,25 @@ struct ArrayRef {
 };
 
 // Choose the per-element head h in [0, 8) at which every array is 16-byte
-// aligned; if there is none, the whole range runs per element.
+// aligned; if there is none, the whole range runs per element.  An h at
+// which the 4-byte arrays are 32-byte aligned as well is preferred: it sets
+// w32 (8 floats per 32-byte access).
 Walk make_walk(int64_t L, int64_t nv, const ArrayRef *a, int count)
 {
-    Walk w{L, nv, 0, 0};
-    for (int h = 0; h < kVec; ++h) {
-        bool ok = true;
-        for (int k = 0; k < count && ok; ++k)
-            ok = (((uintptr_t)a[k].p + (uintptr_t)h * a[k].esize) & 15u) == 0;
-        if (ok) {
-            w.head = h < nv ? h : nv;
-            w.nvec = nv > h ? (nv - h) / kVec : 0;
-            return w;
+    Walk w{L, nv, 0, 0, 0};
+    for (int pass = 0; pass < 2; ++pass) {
+        for (int h = 0; h < kVec; ++h) {
+            bool ok = true;
+            for (int k = 0; k < count && ok; ++k) {
+                const uintptr_t mask = (pass == 0 && a[k].esize == 4) ? 31u : 15u;
+                ok = (((uintptr_t)a[k].p + (uintptr_t)h * a[k].esize) & mask) == 0;
+            }
+            if (ok) {
+                w.head = h < nv ? h : nv;
+                w.nvec = nv > h ? (nv - h) / kVec : 0;
+                w.w32 = pass == 0 ? 1 : 0;
+                return w;
+            }
         }
     }
     return w;
@@ -399,25 +518,56 @@ int sm_count()
     return n;
 }
 
-// One resident wave: SMs x resident blocks of this kernel (cached per kernel
-// and device), capped by the work.
-template <class K>
-int grid_for(K kernel, int64_t work_items)
+int64_t work_of(const Walk &w)
 {
-    static std::atomic<int> cache[64];
+    const int64_t ns = w.L - w.nvec * kVec;
+    return w.nvec > ns ? w.nvec : ns;
+}
+
+// Resident blocks per SM of one kernel on the current device, from the
+// occupancy API on first use and then from a small table keyed by the
+// kernel's address and the device (kernels of the same signature each get
+// their own entry).
+int blocks_per_sm(const void *kernel)
+{
+    struct Entry {
+        const void *kernel;
+        int dev, per_sm;
+    };
+    static std::mutex mu;
+    static Entry table[256];
+    static int used = 0;
     int dev = 0;
-    cudaGetDevice(&dev);
-    int per_sm = dev < 64 ? cache[dev].load(std::memory_order_relaxed) : 0;
-    if (per_sm <= 0) {
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kBlock, 0) != cudaSuccess ||
-            per_sm <= 0)
-            per_sm = 1;
-        if (dev < 64) cache[dev].store(per_sm, std::memory_order_relaxed);
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int k = 0; k < used; ++k)
+            if (table[k].kernel == kernel && table[k].dev == dev) return table[k].per_sm;
     }
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kBlock, 0) != cudaSuccess || per_sm <= 0) {
+        cudaGetLastError();
+        per_sm = 1;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (used < 256) table[used++] = {kernel, dev, per_sm};
+    return per_sm;
+}
+
+// One resident wave for a walk: SMs x this kernel's resident blocks, capped
+// by the work.  The launch is noted for zero1_debug_last_launch.
+template <class K>
+int grid_for(K kernel, const Walk &w)
+{
+    const void *k = reinterpret_cast<const void *>(kernel);
+    const int per_sm = blocks_per_sm(k);
     const int64_t wave = (int64_t)sm_count() * per_sm;
-    int64_t need = (work_items + kBlock - 1) / kBlock;
+    const int64_t work = work_of(w);
+    int64_t need = (work + kBlock - 1) / kBlock;
     if (need < 1) need = 1;
-    return (int)(need < wave ? need : (wave > 0 ? wave : 1));
+    const int grid = (int)(need < wave ? need : (wave > 0 ? wave : 1));
+    z1_note_launch(k, grid, per_sm, w.w32);
+    return grid;
 }
 
 // True if p is host memory the device reaches over the host link (pinned,
@@ -437,12 +587,6 @@ int launch_status(const char *what)
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return z1_fail(ZERO1_ECUDA, "%s: %s", what, cudaGetErrorString(e));
     return ZERO1_OK;
-}
-
-int64_t work_of(const Walk &w)
-{
-    const int64_t ns = w.L - w.nvec * kVec;
-    return w.nvec > ns ? w.nvec : ns;
 }
 
 int load_grads(const zero1_plan_t *plan, const void *const *grads, GradPtrs *g, const char *what)

@@ -3,6 +3,8 @@
 // loss_scale_window, hysteresis, min_loss_scale; 3.2 trap 3), and the same
 // step for callers that cannot allocate device memory.
 
+#include <mutex>
+
 #include "zero1_device.cuh"
 
 namespace {
@@ -104,13 +106,15 @@ k_apply_sums(const float *__restrict__ sums, float *__restrict__ master, float *
     const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
     const int64_t nthr = (int64_t)gridDim.x * kBlock;
     bool bad = false;  // the flag was already taken by the reduce-scatter
+    const bool w32 = w.w32 != 0;
     pipelined<StateLoads>(
         w.nvec, tid, nthr,
-        [&](StateLoads &x, int64_t i) { load_state_vec(x, sums, master, mom, var, w.head + i * kVec); },
+        [&](StateLoads &x, int64_t i) { load_state_vec(x, sums, master, mom, var, w.head + i * kVec, w32); },
         [&](const StateLoads &x, int64_t i) {
             const int64_t j = w.head + i * kVec;
-            const float s[kVec] = {x.g0.x, x.g0.y, x.g0.z, x.g0.w, x.g1.x, x.g1.y, x.g1.z, x.g1.w};
-            store_vec(s, x.w0, x.w1, x.m0, x.m1, x.v0, x.v1, master + j, mom + j, var + j, params + j, c, bad);
+            float s[kVec];
+            unpack_f8(x.g, s);
+            store_vec(s, x.w, x.m, x.v, master + j, mom + j, var + j, params + j, c, bad, w32);
         });
     const int64_t ns = w.L - w.nvec * kVec;
     for (int64_t q = tid; q < ns; q += nthr) {
@@ -162,27 +166,26 @@ __device__ __forceinline__ void pingpong_body(const GradPtrs &g, int M, const Pi
     const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
     const int64_t nthr = (int64_t)gridDim.x * kBlock;
     bool bad = false;
+    const bool w32 = w.w32 != 0;
     if constexpr (MT > 0) {
         pipelined<VecLoads<MT>>(
-            w.nvec, tid, nthr, [&](VecLoads<MT> &x, int64_t i) { x.load(g, sw, sm, sv, w.head + i * kVec); },
+            w.nvec, tid, nthr,
+            [&](VecLoads<MT> &x, int64_t i) { x.load(g, sw, sm, sv, w.head + i * kVec, w32); },
             [&](const VecLoads<MT> &x, int64_t i) {
                 const int64_t j = w.head + i * kVec;
                 float sum[kVec];
                 unpack8(x.q[0], sum);
 #pragma unroll
                 for (int r = 1; r < MT; ++r) add8(x.q[r], sum);
-                store_vec(sum, x.w0, x.w1, x.m0, x.m1, x.v0, x.v1, dw + j, dm + j, dv + j, params + j, c, bad);
+                store_vec(sum, x.w, x.m, x.v, dw + j, dm + j, dv + j, params + j, c, bad, w32);
             });
     } else {
         for (int64_t i = tid; i < w.nvec; i += nthr) {
             const int64_t j = w.head + i * kVec;
-            const float4 *pw = reinterpret_cast<const float4 *>(sw + j);
-            const float4 *pm = reinterpret_cast<const float4 *>(sm + j);
-            const float4 *pv = reinterpret_cast<const float4 *>(sv + j);
-            const float4 w0 = pw[0], w1 = pw[1], m0 = pm[0], m1 = pm[1], v0 = pv[0], v1 = pv[1];
+            const F8 xw = ld_plain8(sw + j, w32), xm = ld_plain8(sm + j, w32), xv = ld_plain8(sv + j, w32);
             float sum[kVec];
             sum8<0>(g, M, j, sum);
-            store_vec(sum, w0, w1, m0, m1, v0, v1, dw + j, dm + j, dv + j, params + j, c, bad);
+            store_vec(sum, xw, xm, xv, dw + j, dm + j, dv + j, params + j, c, bad, w32);
         }
     }
     const int64_t ns = w.L - w.nvec * kVec;
@@ -238,29 +241,27 @@ k_fused_step_scaled(const __grid_constant__ GradPtrs g, int M, float *__restrict
     const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
     const int64_t nthr = (int64_t)gridDim.x * kBlock;
     bool bad = false;  // the flag is final already; nothing is reported
+    const bool w32 = w.w32 != 0;
     if constexpr (MT > 0) {
         pipelined<VecLoads<MT>>(
             w.nvec, tid, nthr,
-            [&](VecLoads<MT> &x, int64_t i) { x.load(g, master, mom, var, w.head + i * kVec); },
+            [&](VecLoads<MT> &x, int64_t i) { x.load(g, master, mom, var, w.head + i * kVec, w32); },
             [&](const VecLoads<MT> &x, int64_t i) {
                 const int64_t j = w.head + i * kVec;
                 float sum[kVec];
                 unpack8(x.q[0], sum);
 #pragma unroll
                 for (int r = 1; r < MT; ++r) add8(x.q[r], sum);
-                store_vec(sum, x.w0, x.w1, x.m0, x.m1, x.v0, x.v1, master + j, mom + j, var + j, params + j, c,
-                          bad);
+                store_vec(sum, x.w, x.m, x.v, master + j, mom + j, var + j, params + j, c, bad,
+                          w32 && wide_stores_in_place(MT));
             });
     } else {
         for (int64_t i = tid; i < w.nvec; i += nthr) {
             const int64_t j = w.head + i * kVec;
-            const float4 *pw = reinterpret_cast<const float4 *>(master + j);
-            const float4 *pm = reinterpret_cast<const float4 *>(mom + j);
-            const float4 *pv = reinterpret_cast<const float4 *>(var + j);
-            const float4 w0 = pw[0], w1 = pw[1], m0 = pm[0], m1 = pm[1], v0 = pv[0], v1 = pv[1];
+            const F8 xw = ld_plain8(master + j, w32), xm = ld_plain8(mom + j, w32), xv = ld_plain8(var + j, w32);
             float sum[kVec];
             sum8<0>(g, M, j, sum);
-            store_vec(sum, w0, w1, m0, m1, v0, v1, master + j, mom + j, var + j, params + j, c, bad);
+            store_vec(sum, xw, xm, xv, master + j, mom + j, var + j, params + j, c, bad, w32 && wide_stores_in_place(0));
         }
     }
     fused_scalar_rest(g, M, master, mom, var, params, w, c, tid, nthr, bad);
@@ -276,12 +277,13 @@ k_restore_params(const PingPong s, uint16_t *__restrict__ params, const Walk w, 
         (*reinterpret_cast<const volatile uint32_t *>(&sc->current) & 1u) ? s.master[1] : s.master[0];
     const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
     const int64_t nthr = (int64_t)gridDim.x * kBlock;
+    const bool w32 = w.w32 != 0;
     for (int64_t i = tid; i < w.nvec; i += nthr) {
         const int64_t j = w.head + i * kVec;
-        const float4 a = ld_state(master + j), b = ld_state(master + j + 4);
+        const F8 x = ld_state8(master + j, w32);
         __stcs(reinterpret_cast<uint4 *>(params + j),
-               make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y),
-                          pack_bf16x2(b.z, b.w)));
+               make_uint4(pack_bf16x2(x.lo.x, x.lo.y), pack_bf16x2(x.lo.z, x.lo.w), pack_bf16x2(x.hi.x, x.hi.y),
+                          pack_bf16x2(x.hi.z, x.hi.w)));
     }
     const int64_t ns = w.L - w.nvec * kVec;
     for (int64_t q = tid; q < ns; q += nthr) {
@@ -374,13 +376,13 @@ extern "C" int zero1_step_dynamic(const zero1_plan_t *plan, int32_t shard_begin,
     uint32_t *flag = &scaler->overflow;
     dispatch_m(M, [&](auto mt) {
         constexpr int MT = decltype(mt)::value;
-        const int grid = grid_for(k_reduce_scatter<MT, false>, work_of(wr));
+        const int grid = grid_for(k_reduce_scatter<MT, false>, wr);
         k_reduce_scatter<MT, false><<<grid, kBlock, 0, st>>>(g, M, wr, 1.0f, sums, flag);
     });
     // 2. the update from the sums (skipped on overflow)
     const ArrayRef ua[5] = {{sums, 4}, {master, 4}, {m, 4}, {v, 4}, {params, 2}};
     const Walk wu = make_walk(r.L, r.nv, ua, 5);
-    const int grid = grid_for(k_apply_sums, work_of(wu));
+    const int grid = grid_for(k_apply_sums, wu);
     k_apply_sums<<<grid, kBlock, 0, st>>>(sums, master, m, v, static_cast<uint16_t *>(params), wu, c, scaler);
     // 3. the scaler advances
     const ScalePolicy pol{policy->factor, policy->window, policy->hysteresis, policy->min_scale};
@@ -436,7 +438,7 @@ int launch_pingpong_range(const zero1_plan_t *plan, int64_t L, int64_t nv, const
     uint16_t *pp = static_cast<uint16_t *>(params);
     dispatch_m(M, [&](auto mt) {
         constexpr int MT = decltype(mt)::value;
-        const int grid = grid_for(k_fused_step_pingpong<MT>, work_of(w));
+        const int grid = grid_for(k_fused_step_pingpong<MT>, w);
         k_fused_step_pingpong<MT><<<grid, kBlock, 0, st>>>(g, M, s, pp, w, c, scaler);
     });
     return launch_status(what);
@@ -465,7 +467,7 @@ int launch_pingpong_finish(const zero1_plan_t *plan, int64_t L, int64_t nv, floa
     s.master[1] = master[1];
     const ArrayRef arr[3] = {{master[0], 4}, {master[1], 4}, {params, 2}};
     const Walk w = make_walk(L, nv, arr, 3);
-    const int grid = grid_for(k_restore_params, work_of(w));
+    const int grid = grid_for(k_restore_params, w);
     k_restore_params<<<grid, kBlock, 0, st>>>(s, static_cast<uint16_t *>(params), w, scaler);
     const ScalePolicy pol{policy->factor, policy->window, policy->hysteresis, policy->min_scale};
     k_scaler_update<<<1, 32, 0, st>>>(scaler, pol, hp->global_batch, hp->beta1, hp->beta2, 1);
@@ -556,7 +558,7 @@ int z1_scaled_range(const zero1_plan_t *plan, int64_t elem_begin, int64_t elem_e
     uint16_t *pp = static_cast<uint16_t *>(params);
     dispatch_m(M, [&](auto mt) {
         constexpr int MT = decltype(mt)::value;
-        const int grid = grid_for(k_fused_step_scaled<MT>, work_of(w));
+        const int grid = grid_for(k_fused_step_scaled<MT>, w);
         k_fused_step_scaled<MT><<<grid, kBlock, 0, st>>>(g, M, master, m, v, pp, w, c, scaler);
     });
     return launch_status("scaled range launch");
@@ -592,31 +594,70 @@ int z1_check_scaler_and_policy(const zero1_scaler_t *scaler, const zero1_loss_sc
 // workspace of zero1_step_dynamic is this file-scope array, which exists on
 // every device that loads the library until the process exits.  Its name is a
 // host-side stand-in in host code; the device address comes from
-// cudaGetSymbolAddress, looked up once per device with that device current.
+// cudaGetSymbolAddress, looked up with the device current on the first call
+// on each device, and again whenever the device's current context is not
+// the one the address was looked up in (after cudaDeviceReset the array
+// lives in a new context).
 static __device__ __align__(256) float g_noalloc_sums[ZERO1_NOALLOC_MAX_ELEMS];
 
 namespace {
 
-std::atomic<float *> g_noalloc_addr[64];
+// cuCtxGetCurrent, reached through the runtime (no link to the driver
+// library); NULL if the runtime cannot provide it.
+typedef int (*CtxGetCurrentFn)(void **ctx);
 
-// Device address of g_noalloc_sums on the current device (looked up on the
-// first call on each device).
+CtxGetCurrentFn ctx_get_current()
+{
+    static std::once_flag once;
+    static CtxGetCurrentFn fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(p);
+        cudaGetLastError();
+    });
+    return fn;
+}
+
+void *current_context()
+{
+    void *ctx = nullptr;
+    const CtxGetCurrentFn fn = ctx_get_current();
+    if (fn && fn(&ctx) != 0) ctx = nullptr;
+    return ctx;
+}
+
+struct NoallocAddr {
+    void *ctx;
+    float *addr;
+};
+std::mutex g_noalloc_mu;
+NoallocAddr g_noalloc_addr[64];
+
+// Device address of g_noalloc_sums in the current device's current context.
 int noalloc_sums(float **out)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return z1_fail(ZERO1_ECUDA, "no-alloc step: cudaGetDevice: %s", cudaGetErrorString(e));
     if (dev < 0 || dev >= 64) return z1_fail(ZERO1_ERANGE, "no-alloc step: device %d beyond 64 devices", dev);
-    float *p = g_noalloc_addr[dev].load(std::memory_order_acquire);
-    if (!p) {
-        void *addr = nullptr;
-        e = cudaGetSymbolAddress(&addr, g_noalloc_sums);
-        if (e != cudaSuccess || !addr)
-            return z1_fail(ZERO1_ECUDA, "no-alloc step: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
-        p = static_cast<float *>(addr);
-        g_noalloc_addr[dev].store(p, std::memory_order_release);
+    void *ctx = current_context();
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    NoallocAddr &c = g_noalloc_addr[dev];
+    if (ctx && c.addr && c.ctx == ctx) {
+        *out = c.addr;
+        return ZERO1_OK;
     }
-    *out = p;
+    void *addr = nullptr;
+    e = cudaGetSymbolAddress(&addr, g_noalloc_sums);
+    if (e != cudaSuccess || !addr)
+        return z1_fail(ZERO1_ECUDA, "no-alloc step: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+    // the lookup makes the device's primary context current if none was
+    c.ctx = ctx ? ctx : current_context();
+    c.addr = static_cast<float *>(addr);
+    *out = c.addr;
     return ZERO1_OK;
 }
 
@@ -634,11 +675,11 @@ extern "C" int zero1_step_dynamic_noalloc(const zero1_plan_t *plan, int32_t shar
     if (r.L > (int64_t)ZERO1_NOALLOC_MAX_ELEMS)
         return z1_fail(ZERO1_ERANGE,
                        "no-alloc step: range of %lld elements exceeds the built-in workspace of %d elements "
-                       "(64 MiB); split the call by shards",
+                       "(64 MiB); one call is one whole attempt, so a longer range needs zero1_step_dynamic "
+                       "with a caller-provided workspace",
                        (long long)r.L, ZERO1_NOALLOC_MAX_ELEMS);
     float *sums = nullptr;
     if ((rc = noalloc_sums(&sums)) != ZERO1_OK) return rc;
     return zero1_step_dynamic(plan, shard_begin, shard_end, grads, master, m, v, params, hp, scaler, policy,
                               sums, stream);
 }
-

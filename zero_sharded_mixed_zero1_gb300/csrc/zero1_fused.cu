@@ -23,15 +23,14 @@ namespace {
 // One 8-element vector of the fused step for M = MT <= 8 whose loads are in q
 // and the six state registers.
 template <int MT>
-__device__ __forceinline__ void fused_vec(int64_t j, const uint4 *q, float4 w0, float4 w1, float4 m0, float4 m1,
-                                          float4 v0, float4 v1, float *master, float *mom, float *var,
-                                          uint16_t *params, const Z1Consts &c, bool &bad)
+__device__ __forceinline__ void fused_vec(int64_t j, const VecLoads<MT> &x, float *master, float *mom, float *var,
+                                          uint16_t *params, const Z1Consts &c, bool &bad, bool w32)
 {
     float s[kVec];
-    unpack8(q[0], s);
+    unpack8(x.q[0], s);
 #pragma unroll
-    for (int r = 1; r < MT; ++r) add8(q[r], s);
-    store_vec(s, w0, w1, m0, m1, v0, v1, master + j, mom + j, var + j, params + j, c, bad);
+    for (int r = 1; r < MT; ++r) add8(x.q[r], s);
+    store_vec(s, x.w, x.m, x.v, master + j, mom + j, var + j, params + j, c, bad, w32 && wide_stores_in_place(MT));
 }
 
 // The fused reduce-scatter + AdamW + all-gather for M <= 8 (M = MT known at
@@ -53,15 +52,15 @@ k_fused_step(const __grid_constant__ GradPtrs g, int M, float *__restrict__ mast
     const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
     const int64_t nthr = (int64_t)gridDim.x * kBlock;
     bool bad = false;
+    const bool w32 = w.w32 != 0;
     VecLoads<MT> cur, nxt;
     int64_t i = tid;
-    if (i < w.nvec) cur.load(g, master, mom, var, w.head + i * kVec);
+    if (i < w.nvec) cur.load(g, master, mom, var, w.head + i * kVec, w32);
     for (; i < w.nvec; i += nthr) {
         const int64_t j = w.head + i * kVec;
         const bool more = i + nthr < w.nvec;
-        if (more) nxt.load(g, master, mom, var, j + nthr * kVec);
-        fused_vec<MT>(j, cur.q, cur.w0, cur.w1, cur.m0, cur.m1, cur.v0, cur.v1, master, mom, var,
-                      params, c, bad);
+        if (more) nxt.load(g, master, mom, var, j + nthr * kVec, w32);
+        fused_vec<MT>(j, cur, master, mom, var, params, c, bad, w32);
         if (more) cur = nxt;
     }
     fused_scalar_rest(g, M, master, mom, var, params, w, c, tid, nthr, bad);
@@ -85,11 +84,12 @@ k_fused_step_wide(const __grid_constant__ GradPtrs g, int M, float *__restrict__
     const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
     const int64_t nthr = (int64_t)gridDim.x * kBlock;
     bool bad = false;
+    const bool w32 = w.w32 != 0;
     for (int64_t i = tid; i < w.nvec; i += nthr) {
         const int64_t j = w.head + i * kVec;
         VecLoads<MT> x;
-        x.load(g, master, mom, var, j);
-        fused_vec<MT>(j, x.q, x.w0, x.w1, x.m0, x.m1, x.v0, x.v1, master, mom, var, params, c, bad);
+        x.load(g, master, mom, var, j, w32);
+        fused_vec<MT>(j, x, master, mom, var, params, c, bad, w32);
     }
     fused_scalar_rest(g, M, master, mom, var, params, w, c, tid, nthr, bad);
     if (flag && !skip) warp_flag(flag, bad);
@@ -109,12 +109,10 @@ k_fused_step_grouped(const __grid_constant__ GradPtrs g, int M, float *__restric
     const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
     const int64_t nthr = (int64_t)gridDim.x * kBlock;
     bool bad = false;
+    const bool w32 = w.w32 != 0;
     for (int64_t i = tid; i < w.nvec; i += nthr) {
         const int64_t j = w.head + i * kVec;
-        const float4 *pw = reinterpret_cast<const float4 *>(master + j);
-        const float4 *pm = reinterpret_cast<const float4 *>(mom + j);
-        const float4 *pv = reinterpret_cast<const float4 *>(var + j);
-        const float4 w0 = pw[0], w1 = pw[1], m0 = pm[0], m1 = pm[1], v0 = pv[0], v1 = pv[1];
+        const F8 sw = ld_plain8(master + j, w32), sm = ld_plain8(mom + j, w32), sv = ld_plain8(var + j, w32);
         float s[kVec];
         uint4 q[8];
 #pragma unroll
@@ -130,7 +128,7 @@ k_fused_step_grouped(const __grid_constant__ GradPtrs g, int M, float *__restric
             for (int k = 0; k < 8; ++k)
                 if (r0 + k < M) add8(q[k], s);
         }
-        store_vec(s, w0, w1, m0, m1, v0, v1, master + j, mom + j, var + j, params + j, c, bad);
+        store_vec(s, sw, sm, sv, master + j, mom + j, var + j, params + j, c, bad, w32 && wide_stores_in_place(0));
     }
     fused_scalar_rest(g, M, master, mom, var, params, w, c, tid, nthr, bad);
     if (flag && !skip) warp_flag(flag, bad);
@@ -157,19 +155,17 @@ k_fused_step_offload(const __grid_constant__ GradPtrs g, int M, float *__restric
     const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
     const int64_t nthr = (int64_t)gridDim.x * kBlock;
     bool bad = false;
+    const bool w32 = w.w32 != 0;
     for (int64_t i0 = tid; i0 < w.nvec; i0 += kOffloadDepth * nthr) {
-        float4 st[kOffloadDepth][6];
+        F8 st[kOffloadDepth][3];
 #pragma unroll
         for (int u = 0; u < kOffloadDepth; ++u) {
             const int64_t i = i0 + u * nthr;
             if (i < w.nvec) {
                 const int64_t j = w.head + i * kVec;
-                st[u][0] = ld_state(master + j);
-                st[u][1] = ld_state(master + j + 4);
-                st[u][2] = ld_state(mom + j);
-                st[u][3] = ld_state(mom + j + 4);
-                st[u][4] = ld_state(var + j);
-                st[u][5] = ld_state(var + j + 4);
+                st[u][0] = ld_state8(master + j, w32);
+                st[u][1] = ld_state8(mom + j, w32);
+                st[u][2] = ld_state8(var + j, w32);
             }
         }
 #pragma unroll
@@ -179,8 +175,8 @@ k_fused_step_offload(const __grid_constant__ GradPtrs g, int M, float *__restric
                 const int64_t j = w.head + i * kVec;
                 float s[kVec];
                 sum8<MT>(g, M, j, s);
-                store_vec(s, st[u][0], st[u][1], st[u][2], st[u][3], st[u][4], st[u][5], master + j, mom + j,
-                          var + j, params + j, c, bad);
+                store_vec(s, st[u][0], st[u][1], st[u][2], master + j, mom + j, var + j, params + j, c, bad,
+                          w32 && wide_stores_in_place(MT));
             }
         }
     }
@@ -225,22 +221,22 @@ int launch_fused_range(const zero1_plan_t *plan, int64_t L, int64_t nv, const vo
     if (in_host_memory(master)) {
         dispatch_m(M, [&](auto mt) {
             constexpr int MT = decltype(mt)::value;
-            const int grid = grid_for(k_fused_step_offload<MT>, work_of(w));
+            const int grid = grid_for(k_fused_step_offload<MT>, w);
             k_fused_step_offload<MT><<<grid, kBlock, 0, st>>>(g, M, master, m, v, pp, w, c, overflow_flag, skip);
         });
     } else if (M > 8) {
-        const int grid = grid_for(k_fused_step_grouped, work_of(w));
+        const int grid = grid_for(k_fused_step_grouped, w);
         k_fused_step_grouped<<<grid, kBlock, 0, st>>>(g, M, master, m, v, pp, w, c, overflow_flag, skip);
     } else {
         dispatch_m(M, [&](auto mt) {
             constexpr int MT = decltype(mt)::value;
             if constexpr (MT > 0) {
                 if (w.nvec <= kWideMaxVec) {
-                    const int grid = grid_for(k_fused_step_wide<MT>, work_of(w));
+                    const int grid = grid_for(k_fused_step_wide<MT>, w);
                     k_fused_step_wide<MT><<<grid, kBlock, 0, st>>>(g, M, master, m, v, pp, w, c, overflow_flag,
                                                                    skip);
                 } else {
-                    const int grid = grid_for(k_fused_step<MT>, work_of(w));
+                    const int grid = grid_for(k_fused_step<MT>, w);
                     k_fused_step<MT><<<grid, kBlock, 0, st>>>(g, M, master, m, v, pp, w, c, overflow_flag, skip);
                 }
             }

@@ -10,6 +10,8 @@
 #include <cstdio>
 #include <cstring>
 
+#include <cuda_runtime.h>
+
 #include "zero1.h"
 #include "zero1_internal.h"
 
@@ -26,7 +28,37 @@ int z1_fail(int code, const char *fmt, ...)
 
 extern "C" const char *zero1_last_error(void) { return g_last_error; }
 
-extern "C" int zero1_abi_version(void) { return 1; }
+namespace {
+struct LastLaunch {
+    const void *kernel;
+    int grid, blocks_per_sm, w32;
+};
+thread_local LastLaunch g_last_launch = {nullptr, 0, 0, 0};
+}  // namespace
+
+void z1_note_launch(const void *kernel, int grid, int blocks_per_sm, int w32)
+{
+    g_last_launch = {kernel, grid, blocks_per_sm, w32};
+}
+
+extern "C" int zero1_debug_last_launch(const char **kernel_name, int32_t *grid, int32_t *blocks_per_sm,
+                                       int32_t *w32)
+{
+    if (!g_last_launch.kernel) return z1_fail(ZERO1_EINVAL, "no kernel launched on this thread yet");
+    if (kernel_name) {
+        const char *name = nullptr;
+        const cudaError_t e = cudaFuncGetName(&name, g_last_launch.kernel);
+        if (e != cudaSuccess || !name)
+            return z1_fail(ZERO1_ECUDA, "cudaFuncGetName: %s", cudaGetErrorString(e));
+        *kernel_name = name;
+    }
+    if (grid) *grid = g_last_launch.grid;
+    if (blocks_per_sm) *blocks_per_sm = g_last_launch.blocks_per_sm;
+    if (w32) *w32 = g_last_launch.w32;
+    return ZERO1_OK;
+}
+
+extern "C" int zero1_abi_version(void) { return 2; }
 
 extern "C" const char *zero1_strerror(int code)
 {
@@ -40,7 +72,8 @@ extern "C" const char *zero1_strerror(int code)
     }
 }
 
-extern "C" int zero1_plan(int64_t n, int32_t M, int32_t align, zero1_plan_t *out)
+extern "C" int zero1_plan(int64_t n, int32_t M, int32_t align, const int64_t *tensor_numels, int32_t n_tensors,
+                          zero1_plan_t *out)
 {
     if (!out) return z1_fail(ZERO1_EINVAL, "zero1_plan: out is NULL");
     if (n < 1) return z1_fail(ZERO1_EINVAL, "zero1_plan: n = %lld < 1", (long long)n);
@@ -48,6 +81,20 @@ extern "C" int zero1_plan(int64_t n, int32_t M, int32_t align, zero1_plan_t *out
     if (align < 1) return z1_fail(ZERO1_EINVAL, "zero1_plan: align = %d < 1", align);
     if (M > ZERO1_MAX_REPLICAS)
         return z1_fail(ZERO1_ERANGE, "zero1_plan: M = %d > %d", M, ZERO1_MAX_REPLICAS);
+    if (tensor_numels ? n_tensors < 1 : n_tensors != 0)
+        return z1_fail(ZERO1_EINVAL, "zero1_plan: n_tensors = %d with a %s tensor list", n_tensors,
+                       tensor_numels ? "non-NULL" : "NULL");
+    if (tensor_numels) {
+        int64_t total = 0;
+        for (int32_t k = 0; k < n_tensors; ++k) {
+            if (tensor_numels[k] < 0 || tensor_numels[k] > n - total)
+                return z1_fail(ZERO1_EINVAL, "zero1_plan: tensor sizes do not sum to n = %lld", (long long)n);
+            total += tensor_numels[k];
+        }
+        if (total != n)
+            return z1_fail(ZERO1_EINVAL, "zero1_plan: tensor sizes sum to %lld, not n = %lld", (long long)total,
+                           (long long)n);
+    }
     const int64_t unit = (int64_t)M * (int64_t)align;
     const int64_t units = n / unit + (n % unit != 0);
     if (units > INT64_MAX / unit) return z1_fail(ZERO1_ERANGE, "zero1_plan: padded length overflows");
@@ -56,6 +103,7 @@ extern "C" int zero1_plan(int64_t n, int32_t M, int32_t align, zero1_plan_t *out
     out->shard = out->padded_n / M;
     out->M = M;
     out->align = align;
+    out->n_tensors = n_tensors;
     return ZERO1_OK;
 }
 
@@ -63,9 +111,9 @@ int z1_check_plan(const zero1_plan_t *p)
 {
     if (!p) return z1_fail(ZERO1_EINVAL, "plan is NULL");
     zero1_plan_t q;
-    int rc = zero1_plan(p->n, p->M, p->align, &q);
+    int rc = zero1_plan(p->n, p->M, p->align, nullptr, 0, &q);
     if (rc != ZERO1_OK) return rc;
-    if (q.padded_n != p->padded_n || q.shard != p->shard)
+    if (q.padded_n != p->padded_n || q.shard != p->shard || p->n_tensors < 0)
         return z1_fail(ZERO1_EINVAL, "plan fields are inconsistent (not built by zero1_plan)");
     return ZERO1_OK;
 }
@@ -83,16 +131,16 @@ int z1_range(const zero1_plan_t *p, int32_t sb, int32_t se, Z1Range *out)
     return ZERO1_OK;
 }
 
-extern "C" int zero1_plan_segments(const zero1_plan_t *plan, const int64_t *numels, int32_t n_tensors,
-                                   int32_t shard_index, int32_t cap, int64_t *seg_tensor,
-                                   int64_t *seg_tensor_offset, int64_t *seg_shard_offset,
-                                   int64_t *seg_len, int32_t *count)
+extern "C" int zero1_plan_segments(const zero1_plan_t *plan, const int64_t *numels, int32_t shard_index,
+                                   int64_t *seg_tensor, int64_t *seg_begin, int64_t *seg_len, int32_t cap,
+                                   int32_t *count)
 {
     int rc = z1_check_plan(plan);
     if (rc != ZERO1_OK) return rc;
-    if (!numels || n_tensors < 1 || !count || cap < 0 ||
-        (cap > 0 && (!seg_tensor || !seg_tensor_offset || !seg_shard_offset || !seg_len)))
-        return z1_fail(ZERO1_EINVAL, "zero1_plan_segments: NULL or empty argument");
+    const int32_t n_tensors = plan->n_tensors;
+    if (n_tensors < 1) return z1_fail(ZERO1_EINVAL, "zero1_plan_segments: the plan was built without tensors");
+    if (!numels || !count || cap < 0 || (cap > 0 && (!seg_tensor || !seg_begin || !seg_len)))
+        return z1_fail(ZERO1_EINVAL, "zero1_plan_segments: NULL argument");
     if (shard_index < 0 || shard_index >= plan->M)
         return z1_fail(ZERO1_EINVAL, "zero1_plan_segments: shard %d not in [0, %d)", shard_index, plan->M);
     int64_t total = 0;
@@ -113,8 +161,7 @@ extern "C" int zero1_plan_segments(const zero1_plan_t *plan, const int64_t *nume
         if (b > a) {
             if (c >= cap) return z1_fail(ZERO1_ERANGE, "zero1_plan_segments: more than %d pieces", cap);
             seg_tensor[c] = k;
-            seg_tensor_offset[c] = a - start;
-            seg_shard_offset[c] = a - lo;
+            seg_begin[c] = a - start;
             seg_len[c] = b - a;
             ++c;
         }

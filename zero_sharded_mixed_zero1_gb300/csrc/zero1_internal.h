@@ -70,3 +70,8 @@ int z1_scaler_advance(zero1_scaler_t *scaler, const zero1_loss_scale_policy_t *p
                       int32_t M, zero1_stream_t stream);
 int z1_check_scaler_and_policy(const zero1_scaler_t *scaler, const zero1_loss_scale_policy_t *policy,
                                const zero1_adamw_t *hp, int32_t M);
+
+// Record a kernel launch for zero1_debug_last_launch (per host thread): the
+// kernel, its grid, the resident blocks per SM the grid was sized from, and
+// whether the vector body moved fp32 in 32-byte accesses.
+void z1_note_launch(const void *kernel, int grid, int blocks_per_sm, int w32);

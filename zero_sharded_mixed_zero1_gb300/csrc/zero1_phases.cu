@@ -42,23 +42,22 @@ k_adamw(const float *__restrict__ gin, float *__restrict__ master, float *__rest
 {
     const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
     const int64_t nthr = (int64_t)gridDim.x * kBlock;
+    const bool w32 = w.w32 != 0;
     pipelined<StateLoads>(
         w.nvec, tid, nthr,
-        [&](StateLoads &x, int64_t i) { load_state_vec(x, gin, master, mom, var, w.head + i * kVec); },
+        [&](StateLoads &x, int64_t i) { load_state_vec(x, gin, master, mom, var, w.head + i * kVec, w32); },
         [&](const StateLoads &x, int64_t i) {
             const int64_t j = w.head + i * kVec;
-            float gg[kVec] = {x.g0.x, x.g0.y, x.g0.z, x.g0.w, x.g1.x, x.g1.y, x.g1.z, x.g1.w};
-            float ww[kVec] = {x.w0.x, x.w0.y, x.w0.z, x.w0.w, x.w1.x, x.w1.y, x.w1.z, x.w1.w};
-            float mm[kVec] = {x.m0.x, x.m0.y, x.m0.z, x.m0.w, x.m1.x, x.m1.y, x.m1.z, x.m1.w};
-            float vv[kVec] = {x.v0.x, x.v0.y, x.v0.z, x.v0.w, x.v1.x, x.v1.y, x.v1.z, x.v1.w};
+            float gg[kVec], ww[kVec], mm[kVec], vv[kVec];
+            unpack_f8(x.g, gg);
+            unpack_f8(x.w, ww);
+            unpack_f8(x.m, mm);
+            unpack_f8(x.v, vv);
 #pragma unroll
             for (int k = 0; k < kVec; ++k) adamw1(gg[k], c, ww[k], mm[k], vv[k]);
-            st_stream(master + j, ww[0], ww[1], ww[2], ww[3]);
-            st_stream(master + j + 4, ww[4], ww[5], ww[6], ww[7]);
-            st_stream(mom + j, mm[0], mm[1], mm[2], mm[3]);
-            st_stream(mom + j + 4, mm[4], mm[5], mm[6], mm[7]);
-            st_stream(var + j, vv[0], vv[1], vv[2], vv[3]);
-            st_stream(var + j + 4, vv[4], vv[5], vv[6], vv[7]);
+            st_stream8(master + j, ww, w32);
+            st_stream8(mom + j, mm, w32);
+            st_stream8(var + j, vv, w32);
         });
     const int64_t ns = w.L - w.nvec * kVec;
     for (int64_t q = tid; q < ns; q += nthr) {
@@ -72,26 +71,18 @@ k_adamw(const float *__restrict__ gin, float *__restrict__ master, float *__rest
 }
 
 // All-gather of the updated shard: params[j] = bf16(master[j]), real only.
-struct MasterLoads {
-    float4 a, b;
-};
-
 __global__ void __launch_bounds__(kBlock, 1)
 k_all_gather(const float *__restrict__ master, uint16_t *__restrict__ params, const Walk w)
 {
     const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
     const int64_t nthr = (int64_t)gridDim.x * kBlock;
-    pipelined<MasterLoads>(
-        w.nvec, tid, nthr,
-        [&](MasterLoads &x, int64_t i) {
-            const float4 *pw = reinterpret_cast<const float4 *>(master + w.head + i * kVec);
-            x.a = __ldcs(pw);
-            x.b = __ldcs(pw + 1);
-        },
-        [&](const MasterLoads &x, int64_t i) {
+    const bool w32 = w.w32 != 0;
+    pipelined<F8>(
+        w.nvec, tid, nthr, [&](F8 &x, int64_t i) { x = ld_cs8(master + w.head + i * kVec, w32); },
+        [&](const F8 &x, int64_t i) {
             __stcs(reinterpret_cast<uint4 *>(params + w.head + i * kVec),
-                   make_uint4(pack_bf16x2(x.a.x, x.a.y), pack_bf16x2(x.a.z, x.a.w), pack_bf16x2(x.b.x, x.b.y),
-                              pack_bf16x2(x.b.z, x.b.w)));
+                   make_uint4(pack_bf16x2(x.lo.x, x.lo.y), pack_bf16x2(x.lo.z, x.lo.w),
+                              pack_bf16x2(x.hi.x, x.hi.y), pack_bf16x2(x.hi.z, x.hi.w)));
         });
     const int64_t ns = w.L - w.nvec * kVec;
     for (int64_t q = tid; q < ns; q += nthr) {
@@ -125,7 +116,7 @@ k_all_gather_shards(const uint16_t *__restrict__ shards, const __grid_constant__
 // Naive All-Reduce: every output gets sum * scale.  Element j's inputs are
 // all read before any output of j is written (outputs may alias inputs).
 template <bool BF16>
-__device__ __forceinline__ void ar_store(const OutPtrs &o, int M, int64_t j, float s[kVec], float scale)
+__device__ __forceinline__ void ar_store(const OutPtrs &o, int M, int64_t j, float s[kVec], float scale, bool w32)
 {
 #pragma unroll
     for (int k = 0; k < kVec; ++k) s[k] = __fmul_rn(s[k], scale);
@@ -134,20 +125,21 @@ __device__ __forceinline__ void ar_store(const OutPtrs &o, int M, int64_t j, flo
                                    pack_bf16x2(s[6], s[7]));
         for (int r = 0; r < M; ++r) __stcs(reinterpret_cast<uint4 *>(static_cast<uint16_t *>(o.p[r]) + j), q);
     } else {
-        for (int r = 0; r < M; ++r) {
-            st_stream(static_cast<float *>(o.p[r]) + j, s[0], s[1], s[2], s[3]);
-            st_stream(static_cast<float *>(o.p[r]) + j + 4, s[4], s[5], s[6], s[7]);
-        }
+        for (int r = 0; r < M; ++r) st_stream8(static_cast<float *>(o.p[r]) + j, s, w32);
     }
 }
 
-template <int MT, bool BF16>
-__global__ void Z1_BOUNDS(MT)
-k_allreduce(const __grid_constant__ GradPtrs g, const __grid_constant__ OutPtrs o, int M,
-            const Walk w, float scale)
+// The all-reduce body.  NC: the gradients are read through the read-only
+// (non-coherent) path, which is allowed only while no buffer this kernel
+// writes overlaps them; an in-place call (an output aliasing an input) runs
+// the coherent instance, which reads them with ordinary global loads.
+template <int MT, bool BF16, bool NC>
+__device__ __forceinline__ void allreduce_body(const GradPtrs &g, const OutPtrs &o, int M, const Walk &w,
+                                               float scale)
 {
     const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
     const int64_t nthr = (int64_t)gridDim.x * kBlock;
+    const bool w32 = w.w32 != 0;
     if constexpr (MT > 0) {
         // in place, the next vector's loads touch other elements than the
         // current vector's stores, so prefetching them stays correct
@@ -156,32 +148,50 @@ k_allreduce(const __grid_constant__ GradPtrs g, const __grid_constant__ OutPtrs 
             [&](GradLoads<MT> &x, int64_t i) {
                 const int64_t j = w.head + i * kVec;
 #pragma unroll
-                for (int r = 0; r < MT; ++r) x.q[r] = ld_stream_u4(g.p[r] + j);
+                for (int r = 0; r < MT; ++r) x.q[r] = ld_grad_u4<NC>(g.p[r] + j);
             },
             [&](const GradLoads<MT> &x, int64_t i) {
                 float s[kVec];
                 unpack8(x.q[0], s);
 #pragma unroll
                 for (int r = 1; r < MT; ++r) add8(x.q[r], s);
-                ar_store<BF16>(o, MT, w.head + i * kVec, s, scale);
+                ar_store<BF16>(o, MT, w.head + i * kVec, s, scale, w32);
             });
     } else {
         for (int64_t i = tid; i < w.nvec; i += nthr) {
             const int64_t j = w.head + i * kVec;
             float s[kVec];
-            sum8<0>(g, M, j, s);
-            ar_store<BF16>(o, M, j, s, scale);
+            sum8<0, NC>(g, M, j, s);
+            ar_store<BF16>(o, M, j, s, scale, w32);
         }
     }
     const int64_t ns = w.L - w.nvec * kVec;
     for (int64_t q = tid; q < ns; q += nthr) {
         const int64_t j = scalar_index(w, q);
-        const float s = __fmul_rn(sum1(g, M, j), scale);
+        const float s = __fmul_rn(sum1<NC>(g, M, j), scale);
         for (int r = 0; r < M; ++r) {
             if constexpr (BF16) static_cast<uint16_t *>(o.p[r])[j] = to_bf16(s);
             else static_cast<float *>(o.p[r])[j] = s;
         }
     }
+}
+
+// Separate outputs: gradients through the read-only path.
+template <int MT, bool BF16>
+__global__ void Z1_BOUNDS(MT)
+k_allreduce(const __grid_constant__ GradPtrs g, const __grid_constant__ OutPtrs o, int M,
+            const Walk w, float scale)
+{
+    allreduce_body<MT, BF16, true>(g, o, M, w, scale);
+}
+
+// In place (bf16 outputs overlapping the inputs): coherent loads.
+template <int MT>
+__global__ void Z1_BOUNDS(MT)
+k_allreduce_inplace(const __grid_constant__ GradPtrs g, const __grid_constant__ OutPtrs o, int M,
+                    const Walk w, float scale)
+{
+    allreduce_body<MT, true, false>(g, o, M, w, scale);
 }
 
 }  // namespace
@@ -205,7 +215,7 @@ extern "C" int zero1_overflow_check(const zero1_plan_t *plan, int32_t shard_begi
     const int M = plan->M;
     dispatch_m(M, [&](auto mt) {
         constexpr int MT = decltype(mt)::value;
-        const int grid = grid_for(k_overflow<MT>, work_of(w));
+        const int grid = grid_for(k_overflow<MT>, w);
         k_overflow<MT><<<grid, kBlock, 0, st>>>(g, M, w, flag);
     });
     return launch_status("overflow check launch");
@@ -227,15 +237,16 @@ extern "C" int dp_allreduce(const zero1_plan_t *plan, const void *const *grads_i
     const int osz = out_dtype == ZERO1_DTYPE_BF16 ? 2 : 4;
     OutPtrs o{};
     ArrayRef arr[2 * ZERO1_MAX_REPLICAS];
+    bool overlap = false;  // some output overlaps some input
     for (int k = 0; k < M; ++k) {
         if (!outs[k]) return z1_fail(ZERO1_EINVAL, "all-reduce: outs[%d] is NULL", k);
         if ((rc = check_natural(outs[k], osz, "an all-reduce output")) != ZERO1_OK) return rc;
-        if (osz == 4) {
-            const uintptr_t a = (uintptr_t)outs[k], b = a + (uintptr_t)plan->n * 4;
-            for (int q = 0; q < M; ++q) {
-                const uintptr_t c0 = (uintptr_t)grads_in[q], c1 = c0 + (uintptr_t)plan->n * 2;
-                if (a < c1 && c0 < b)
-                    return z1_fail(ZERO1_EINVAL, "all-reduce: fp32 output %d overlaps input %d", k, q);
+        const uintptr_t a = (uintptr_t)outs[k], b = a + (uintptr_t)plan->n * osz;
+        for (int q = 0; q < M; ++q) {
+            const uintptr_t c0 = (uintptr_t)grads_in[q], c1 = c0 + (uintptr_t)plan->n * 2;
+            if (a < c1 && c0 < b) {
+                if (osz == 4) return z1_fail(ZERO1_EINVAL, "all-reduce: fp32 output %d overlaps input %d", k, q);
+                overlap = true;
             }
         }
         o.p[k] = outs[k];
@@ -246,11 +257,14 @@ extern "C" int dp_allreduce(const zero1_plan_t *plan, const void *const *grads_i
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     dispatch_m(M, [&](auto mt) {
         constexpr int MT = decltype(mt)::value;
-        if (osz == 2) {
-            const int grid = grid_for(k_allreduce<MT, true>, work_of(w));
+        if (osz == 2 && overlap) {
+            const int grid = grid_for(k_allreduce_inplace<MT>, w);
+            k_allreduce_inplace<MT><<<grid, kBlock, 0, st>>>(g, o, M, w, scale);
+        } else if (osz == 2) {
+            const int grid = grid_for(k_allreduce<MT, true>, w);
             k_allreduce<MT, true><<<grid, kBlock, 0, st>>>(g, o, M, w, scale);
         } else {
-            const int grid = grid_for(k_allreduce<MT, false>, work_of(w));
+            const int grid = grid_for(k_allreduce<MT, false>, w);
             k_allreduce<MT, false><<<grid, kBlock, 0, st>>>(g, o, M, w, scale);
         }
     });
@@ -282,10 +296,10 @@ extern "C" int zero1_reduce_scatter(const zero1_plan_t *plan, int32_t shard_begi
     dispatch_m(M, [&](auto mt) {
         constexpr int MT = decltype(mt)::value;
         if (osz == 2) {
-            const int grid = grid_for(k_reduce_scatter<MT, true>, work_of(w));
+            const int grid = grid_for(k_reduce_scatter<MT, true>, w);
             k_reduce_scatter<MT, true><<<grid, kBlock, 0, st>>>(g, M, w, scale, out, flag);
         } else {
-            const int grid = grid_for(k_reduce_scatter<MT, false>, work_of(w));
+            const int grid = grid_for(k_reduce_scatter<MT, false>, w);
             k_reduce_scatter<MT, false><<<grid, kBlock, 0, st>>>(g, M, w, scale, out, flag);
         }
     });
@@ -310,7 +324,7 @@ extern "C" int zero1_adamw_update(const zero1_plan_t *plan, int32_t shard_begin,
     // every element of the range is updated: walk it as if all were real
     const Walk w = make_walk(r.L, r.L, arr, 4);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const int grid = grid_for(k_adamw, work_of(w));
+    const int grid = grid_for(k_adamw, w);
     k_adamw<<<grid, kBlock, 0, st>>>(gin, master, m, v, w, c);
     return launch_status("adamw launch");
 }
@@ -328,7 +342,7 @@ extern "C" int zero1_all_gather(const zero1_plan_t *plan, int32_t shard_begin, i
     const ArrayRef arr[2] = {{master, 4}, {params, 2}};
     const Walk w = make_walk(r.nv, r.nv, arr, 2);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const int grid = grid_for(k_all_gather, work_of(w));
+    const int grid = grid_for(k_all_gather, w);
     k_all_gather<<<grid, kBlock, 0, st>>>(master, static_cast<uint16_t *>(params), w);
     return launch_status("all-gather launch");
 }
@@ -351,7 +365,7 @@ extern "C" int zero1_all_gather_shards(const zero1_plan_t *plan, const void *sha
     }
     const Walk w = make_walk(plan->n, plan->n, arr, 1 + plan->M);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const int grid = grid_for(k_all_gather_shards, work_of(w));
+    const int grid = grid_for(k_all_gather_shards, w);
     k_all_gather_shards<<<grid, kBlock, 0, st>>>(static_cast<const uint16_t *>(shards), o, plan->M, w);
     return launch_status("all-gather shards launch");
 }

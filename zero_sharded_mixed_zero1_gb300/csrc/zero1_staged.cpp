@@ -30,6 +30,7 @@ constexpr int kSlots = 3;
 // two streams were no faster for staged gradients and 3 % slower for staged
 // state than one.
 constexpr int kIn = 1;
+constexpr int kTimes = 6;
 
 enum class Kind { kNull, kDevice, kPinnedHost, kOther };
 
@@ -80,6 +81,12 @@ struct zero1_staged {
     cudaEvent_t entry, done, last;
     bool last_recorded;
     std::vector<int64_t> cuts;   // chunk boundaries, 0 = cuts[0] < ... < cuts.back() = L
+    // ZERO1_STAGE_TIMELINE: timing events of the last step, kTimes per chunk
+    // (inbound copies start/end, kernel start/end, outbound copies start/end)
+    // after t0, recorded on the caller's stream at the step's start
+    bool timeline, timed_step, timed_out;
+    cudaEvent_t t0;
+    std::vector<cudaEvent_t> tev;
 };
 
 namespace {
@@ -114,6 +121,9 @@ void release(zero1_staged_t *h)
         for (cudaEvent_t e : {h->computed[s], h->copied_out[s]})
             if (e) cudaEventDestroy(e);
     }
+    if (h->t0) cudaEventDestroy(h->t0);
+    for (cudaEvent_t e : h->tev)
+        if (e) cudaEventDestroy(e);
     for (cudaStream_t q : h->in)
         if (q) cudaStreamDestroy(q);
     if (h->out) cudaStreamDestroy(h->out);
@@ -132,7 +142,8 @@ extern "C" int zero1_staged_create(const zero1_plan_t *plan, int32_t shard_begin
     int rc;
     Z1Range r;
     if ((rc = z1_range(plan, shard_begin, shard_end, &r)) != ZERO1_OK) return rc;
-    if (what <= 0 || what > (ZERO1_STAGE_GRADS | ZERO1_STAGE_STATE | ZERO1_STAGE_PARAMS))
+    const int32_t staging = ZERO1_STAGE_GRADS | ZERO1_STAGE_STATE | ZERO1_STAGE_PARAMS;
+    if ((what & staging) == 0 || (what & ~(staging | ZERO1_STAGE_TIMELINE)) != 0)
         return z1_fail(ZERO1_EINVAL, "staged create: what = %d is not a non-empty set of ZERO1_STAGE_* bits", what);
     if (chunk_elems < 1) return z1_fail(ZERO1_EINVAL, "staged create: chunk_elems = %lld", (long long)chunk_elems);
     zero1_staged_t *h = new (std::nothrow) zero1_staged_t{};
@@ -140,7 +151,8 @@ extern "C" int zero1_staged_create(const zero1_plan_t *plan, int32_t shard_begin
     h->plan = *plan;
     h->shard_begin = shard_begin;
     h->shard_end = shard_end;
-    h->what = what;
+    h->what = what & staging;
+    h->timeline = (what & ZERO1_STAGE_TIMELINE) != 0;
     h->base = r.base;
     h->L = r.L;
     h->nv = r.nv;
@@ -175,6 +187,17 @@ extern "C" int zero1_staged_create(const zero1_plan_t *plan, int32_t shard_begin
             if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
         for (cudaEvent_t *ev : {&h->computed[s], &h->copied_out[s]})
             if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+    }
+    if (e == cudaSuccess && h->timeline) {
+        try {
+            h->tev.assign((h->cuts.size() - 1) * kTimes, nullptr);
+        } catch (...) {
+            release(h);
+            return z1_fail(ZERO1_ECUDA, "staged create: out of host memory");
+        }
+        e = cudaEventCreate(&h->t0);
+        for (cudaEvent_t &ev : h->tev)
+            if (e == cudaSuccess) e = cudaEventCreate(&ev);
     }
     if (e != cudaSuccess) {
         release(h);
@@ -252,6 +275,8 @@ int staged_run(zero1_staged_t *h, const void *const *grads, float *master, float
         if ((e = (call)) != cudaSuccess) return cuda_fail(e, #call); \
     } while (0)
     Z1_CUDA(cudaEventRecord(h->entry, st));
+    if (h->timeline) Z1_CUDA(cudaEventRecord(h->t0, st));
+    cudaEvent_t *tk = nullptr;  // this chunk's timing events, or NULL
     // and once this handle's outbound copies are done, including those of a
     // call that failed part way (it did not reach its own join)
     Z1_CUDA(cudaEventRecord(h->done, h->out));
@@ -273,6 +298,8 @@ int staged_run(zero1_staged_t *h, const void *const *grads, float *master, float
         if (k >= (size_t)kSlots)
             for (cudaStream_t q : h->in)
                 Z1_CUDA(cudaStreamWaitEvent(q, has_out ? h->copied_out[slot] : h->computed[slot], 0));
+        tk = h->timeline ? &h->tev[k * kTimes] : nullptr;
+        if (tk) Z1_CUDA(cudaEventRecord(tk[0], h->in[0]));
         int next = 0;  // the inbound copies take the inbound streams in turn
         const void *gp[ZERO1_MAX_REPLICAS] = {};
         for (int r = 0; r < M && real > 0; ++r) {
@@ -297,10 +324,12 @@ int staged_run(zero1_staged_t *h, const void *const *grads, float *master, float
                 sp3[a] = state[a] + e0;
             }
         }
+        if (tk) Z1_CUDA(cudaEventRecord(tk[1], h->in[0]));
         for (int q = 0; q < kIn; ++q) {
             Z1_CUDA(cudaEventRecord(h->copied_in[slot][q], h->in[q]));
             Z1_CUDA(cudaStreamWaitEvent(st, h->copied_in[slot][q], 0));
         }
+        if (tk) Z1_CUDA(cudaEventRecord(tk[2], st));
         void *pp = real > 0 ? static_cast<uint16_t *>(params) + e0 : nullptr;
         rc = scaler ? z1_scaled_range(&h->plan, h->base + e0, h->base + e1, real > 0 ? gp : nullptr, sp3[0], sp3[1],
                                       sp3[2], pp, hp, scaler, stream)
@@ -308,8 +337,10 @@ int staged_run(zero1_staged_t *h, const void *const *grads, float *master, float
                                         sp3[1], sp3[2], pp, hp, overflow_flag, stream);
         if (rc != ZERO1_OK) return rc;
         Z1_CUDA(cudaEventRecord(h->computed[slot], st));
+        if (tk) Z1_CUDA(cudaEventRecord(tk[3], st));
         if (has_out) {
             Z1_CUDA(cudaStreamWaitEvent(h->out, h->computed[slot], 0));
+            if (tk) Z1_CUDA(cudaEventRecord(tk[4], h->out));
             for (int a = 0; a < 3 && ss; ++a)
                 Z1_CUDA(cudaMemcpyAsync(state[a] + e0, sp3[a], sizeof(float) * len, cudaMemcpyDeviceToHost,
                                         h->out));
@@ -317,6 +348,7 @@ int staged_run(zero1_staged_t *h, const void *const *grads, float *master, float
                 Z1_CUDA(cudaMemcpyAsync(static_cast<uint16_t *>(params_host) + e0,
                                         static_cast<const uint16_t *>(params) + e0, sizeof(uint16_t) * real,
                                         cudaMemcpyDeviceToHost, h->out));
+            if (tk) Z1_CUDA(cudaEventRecord(tk[5], h->out));
             Z1_CUDA(cudaEventRecord(h->copied_out[slot], h->out));
         }
     }
@@ -329,6 +361,8 @@ int staged_run(zero1_staged_t *h, const void *const *grads, float *master, float
     Z1_CUDA(cudaEventRecord(h->last, st));
 #undef Z1_CUDA
     h->last_recorded = true;
+    h->timed_step = h->timeline;
+    h->timed_out = has_out;
     return ZERO1_OK;
 }
 
@@ -361,5 +395,29 @@ extern "C" int zero1_staged_chunks(const zero1_staged_t *h, int64_t *cuts, int32
         if (cap < n) return z1_fail(ZERO1_ERANGE, "staged chunks: %d boundaries, room for %d", n, cap);
         for (int32_t i = 0; i < n; ++i) cuts[i] = h->cuts[i];
     }
+    return ZERO1_OK;
+}
+
+extern "C" int zero1_staged_timeline(zero1_staged_t *h, float *ms, int32_t cap, int32_t *count)
+{
+    if (!h || !count) return z1_fail(ZERO1_EINVAL, "staged timeline: handle or count is NULL");
+    if (!h->timeline) return z1_fail(ZERO1_EINVAL, "staged timeline: the handle was created without ZERO1_STAGE_TIMELINE");
+    if (!h->timed_step) return z1_fail(ZERO1_EINVAL, "staged timeline: no step has been enqueued on the handle");
+    const int32_t chunks = (int32_t)(h->cuts.size() - 1);
+    *count = chunks;
+    if (!ms) return ZERO1_OK;
+    if (cap < chunks * kTimes)
+        return z1_fail(ZERO1_ERANGE, "staged timeline: %d values needed, room for %d", chunks * kTimes, cap);
+    cudaError_t e = cudaEventSynchronize(h->last);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize");
+    for (int32_t k = 0; k < chunks; ++k)
+        for (int q = 0; q < kTimes; ++q) {
+            float t = -1.0f;
+            if (q < 4 || h->timed_out) {
+                e = cudaEventElapsedTime(&t, h->t0, h->tev[(size_t)k * kTimes + q]);
+                if (e != cudaSuccess) return cuda_fail(e, "cudaEventElapsedTime");
+            }
+            ms[(size_t)k * kTimes + q] = t;
+        }
     return ZERO1_OK;
 }

@@ -44,7 +44,8 @@ class HostStreamedStep:
     step and its copies back to host memory are complete."""
 
     def __init__(self, plan: _lib.Plan, shard_begin: int, shard_end: int, grads, master, m, v, params,
-                 chunk_elems: int = 1 << 24, params_host=None, overflow_flag=None, stream=None):
+                 chunk_elems: int = 1 << 24, params_host=None, overflow_flag=None, stream=None,
+                 timeline: bool = False):
         _lib._replicas(plan, grads, "grads")
         base, L, nv = _lib._range(plan, shard_begin, shard_end)
         if L == 0:
@@ -65,6 +66,8 @@ class HostStreamedStep:
                 (_lib.ZERO1_STAGE_PARAMS if params_host is not None else 0))
         if what == 0:
             raise ValueError("no buffer in host memory: call the fused step directly")
+        if timeline:
+            what |= _lib.ZERO1_STAGE_TIMELINE
         self.plan, self.nv, self.L = plan, nv, L
         self.chunk = max(8, (int(chunk_elems) + 7) // 8 * 8)
         # keep the tensors alive for as long as the handle holds their addresses
@@ -110,6 +113,20 @@ class HostStreamedStep:
                 self._handle, self._grads, *self._state, self._params, self._params_host,
                 ctypes.byref(hp.c_struct()), _lib._scaler_ptr(scaler), ctypes.byref(policy.c_struct()),
                 _lib._stream(self._stream)))
+
+    def timeline(self):
+        """Per-chunk timeline of the last step (created with timeline=True):
+        a (chunks, 6) float32 array of milliseconds since the step started -
+        inbound copies start/end, kernel start/end, outbound copies start/end
+        (-1 when nothing is copied back).  Waits for the step to finish."""
+        import numpy as np
+        if self._handle is None:
+            raise ValueError("the staged step has been closed")
+        count = ctypes.c_int32()
+        _lib._check_rc(self._lib.zero1_staged_timeline(self._handle, None, 0, ctypes.byref(count)))
+        out = np.zeros((count.value, 6), np.float32)
+        _lib._check_rc(self._lib.zero1_staged_timeline(self._handle, out.ctypes.data, out.size, ctypes.byref(count)))
+        return out
 
     def close(self) -> None:
         """Wait for the handle's queued work and free its staging memory."""

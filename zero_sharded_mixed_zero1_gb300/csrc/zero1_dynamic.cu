@@ -63,6 +63,7 @@ __global__ void k_scaler_init(zero1_scaler_t *sc, float initial_scale, int32_t h
 __global__ void k_scaler_update(zero1_scaler_t *sc, const ScalePolicy pol, int64_t B, float beta1, float beta2,
                                 int pingpong)
 {
+    wait_prior_grid();
     if (threadIdx.x != 0 || blockIdx.x != 0) return;
     sc->attempts += 1;
     const bool overflow = *reinterpret_cast<volatile uint32_t *>(&sc->overflow) != 0u;
@@ -93,12 +94,15 @@ __global__ void k_scaler_update(zero1_scaler_t *sc, const ScalePolicy pol, int64
 // AdamW + all-gather from fp32 replica sums (written by the reduce-scatter
 // kernel just before on the same stream), with 1/(B*S) and the bias
 // corrections read from the scaler; nothing is written if the attempt's flag
-// is set.  The arithmetic is the fused step's, operation for operation.
-__global__ void __launch_bounds__(kBlock, 1)
+// is set.  The arithmetic is the fused step's, operation for operation.  Two
+// resident blocks per SM (at most 128 registers): measured 0.8-1.4 % faster
+// for the whole dynamic step than one block with 144 registers.
+__global__ void __launch_bounds__(kBlock, 2)
 k_apply_sums(const float *__restrict__ sums, float *__restrict__ master, float *__restrict__ mom,
              float *__restrict__ var, uint16_t *__restrict__ params, const Walk w, Z1Consts c,
              const zero1_scaler_t *sc)
 {
+    wait_prior_grid();
     if (*reinterpret_cast<const volatile uint32_t *>(&sc->overflow) != 0u) return;
     c.inv = sc->inv;
     c.bc1 = sc->bc1;
@@ -272,6 +276,7 @@ k_fused_step_scaled(const __grid_constant__ GradPtrs g, int M, float *__restrict
 __global__ void __launch_bounds__(kBlock)
 k_restore_params(const PingPong s, uint16_t *__restrict__ params, const Walk w, const zero1_scaler_t *sc)
 {
+    wait_prior_grid();
     if (*reinterpret_cast<const volatile uint32_t *>(&sc->overflow) == 0u) return;
     const float *__restrict__ master =
         (*reinterpret_cast<const volatile uint32_t *>(&sc->current) & 1u) ? s.master[1] : s.master[0];
@@ -383,10 +388,11 @@ extern "C" int zero1_step_dynamic(const zero1_plan_t *plan, int32_t shard_begin,
     const ArrayRef ua[5] = {{sums, 4}, {master, 4}, {m, 4}, {v, 4}, {params, 2}};
     const Walk wu = make_walk(r.L, r.nv, ua, 5);
     const int grid = grid_for(k_apply_sums, wu);
-    k_apply_sums<<<grid, kBlock, 0, st>>>(sums, master, m, v, static_cast<uint16_t *>(params), wu, c, scaler);
+    launch_pdl(k_apply_sums, grid, kBlock, st, (const float *)sums, master, m, v, static_cast<uint16_t *>(params), wu,
+               c, (const zero1_scaler_t *)scaler);
     // 3. the scaler advances
     const ScalePolicy pol{policy->factor, policy->window, policy->hysteresis, policy->min_scale};
-    k_scaler_update<<<1, 32, 0, st>>>(scaler, pol, hp->global_batch, hp->beta1, hp->beta2, 0);
+    launch_pdl(k_scaler_update, 1, 32, st, scaler, pol, (int64_t)hp->global_batch, hp->beta1, hp->beta2, 0);
     return launch_status("dynamic step launch");
 }
 
@@ -468,9 +474,9 @@ int launch_pingpong_finish(const zero1_plan_t *plan, int64_t L, int64_t nv, floa
     const ArrayRef arr[3] = {{master[0], 4}, {master[1], 4}, {params, 2}};
     const Walk w = make_walk(L, nv, arr, 3);
     const int grid = grid_for(k_restore_params, w);
-    k_restore_params<<<grid, kBlock, 0, st>>>(s, static_cast<uint16_t *>(params), w, scaler);
+    launch_pdl(k_restore_params, grid, kBlock, st, s, static_cast<uint16_t *>(params), w, (const zero1_scaler_t *)scaler);
     const ScalePolicy pol{policy->factor, policy->window, policy->hysteresis, policy->min_scale};
-    k_scaler_update<<<1, 32, 0, st>>>(scaler, pol, hp->global_batch, hp->beta1, hp->beta2, 1);
+    launch_pdl(k_scaler_update, 1, 32, st, scaler, pol, (int64_t)hp->global_batch, hp->beta1, hp->beta2, 1);
     return launch_status(what);
 }
 

@@ -36,10 +36,13 @@ k_overflow(const __grid_constant__ GradPtrs g, int M, const Walk w, uint32_t *fl
     warp_flag(flag, bad);
 }
 
-__global__ void __launch_bounds__(kBlock, 1)
+// Two resident blocks per SM (at most 128 registers): the unfused chain
+// measured 1.5 % faster than with one block of 138 registers.
+__global__ void __launch_bounds__(kBlock, 2)
 k_adamw(const float *__restrict__ gin, float *__restrict__ master, float *__restrict__ mom,
         float *__restrict__ var, const Walk w, const Z1Consts c)
 {
+    wait_prior_grid();
     const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
     const int64_t nthr = (int64_t)gridDim.x * kBlock;
     const bool w32 = w.w32 != 0;
@@ -74,6 +77,7 @@ k_adamw(const float *__restrict__ gin, float *__restrict__ master, float *__rest
 __global__ void __launch_bounds__(kBlock, 1)
 k_all_gather(const float *__restrict__ master, uint16_t *__restrict__ params, const Walk w)
 {
+    wait_prior_grid();
     const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
     const int64_t nthr = (int64_t)gridDim.x * kBlock;
     const bool w32 = w.w32 != 0;
@@ -325,7 +329,7 @@ extern "C" int zero1_adamw_update(const zero1_plan_t *plan, int32_t shard_begin,
     const Walk w = make_walk(r.L, r.L, arr, 4);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const int grid = grid_for(k_adamw, w);
-    k_adamw<<<grid, kBlock, 0, st>>>(gin, master, m, v, w, c);
+    launch_pdl(k_adamw, grid, kBlock, st, gin, master, m, v, w, c);
     return launch_status("adamw launch");
 }
 
@@ -343,7 +347,7 @@ extern "C" int zero1_all_gather(const zero1_plan_t *plan, int32_t shard_begin, i
     const Walk w = make_walk(r.nv, r.nv, arr, 2);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const int grid = grid_for(k_all_gather, w);
-    k_all_gather<<<grid, kBlock, 0, st>>>(master, static_cast<uint16_t *>(params), w);
+    launch_pdl(k_all_gather, grid, kBlock, st, master, static_cast<uint16_t *>(params), w);
     return launch_status("all-gather launch");
 }
 

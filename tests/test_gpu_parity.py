@@ -379,3 +379,72 @@ def test_pages_deepspeed_optimizer_block(cuda_device, M, n, align, S):
         for x, y, what in zip(state, o, ("master", "m", "v")):
             assert_f32_bits(f32(x), y, f"{what} t={t}")
         assert_bf16_bits(u16(params), want_p, f"params t={t}")
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 8, 13])
+def test_state_at_16_byte_phase_matches_oracle(cuda_device, M):
+    """fp32 buffers 16 bytes past a 32-byte boundary (the gradients at one):
+    every vector kernel moves the state in 16-byte accesses instead of 32,
+    with the same bits - the fused step (both store widths), the dynamic
+    step, the ping-pong step and the unfused chain."""
+    dev = cuda_device
+    n = 3 * 4096 + 37
+    plan = z.zero1_plan(n, M, 8)
+    P = plan.padded_n
+
+    def shifted(t):
+        """t's values in a fresh buffer that starts 4 floats into its allocation."""
+        out = torch.zeros(t.numel() + 4, dtype=t.dtype, device=dev)[4:]
+        out.copy_(t)
+        return out
+
+    grads = make_grads(M, n, 1e-2, 70 + M, 1, dev)
+    g_np = [u16(g) for g in grads]
+    hp = z.AdamW(global_batch=max(M, 64), step=3)
+    base_state = make_state(n, P, 71 + M, dev, nonzero_moments=True)
+
+    # the oracle, once
+    o = [f32(t).copy() for t in base_state]
+    want_p = oracle_step(plan, g_np, *o, oracle_hp(hp))
+
+    # fused step
+    st = [shifted(t) for t in base_state]
+    params = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+    z.zero1_reduce_scatter_adamw_allgather(plan, 0, M, grads, *st, params, hp)
+    assert z.debug_last_launch()["w32"] is False
+    torch.cuda.synchronize()
+    for x, want, what in zip(st, o, ("master", "m", "v")):
+        assert_f32_bits(f32(x), want, f"fused {what} M={M}")
+    assert_bf16_bits(u16(params), want_p, f"fused params M={M}")
+
+    # dynamic step and ping-pong step with the scaler at S = 1 and t = 3
+    policy = z.LossScalePolicy(initial_scale=1.0, window=1000, hysteresis=2)
+    for design in ("dynamic", "pingpong"):
+        st = [shifted(t) for t in base_state]
+        params = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+        scaler = z.new_scaler(dev)
+        z.zero1_scaler_init(scaler, policy, hp)
+        if design == "dynamic":
+            sums = shifted(torch.zeros(P, dtype=torch.float32, device=dev))
+            z.zero1_step_dynamic(plan, 0, M, grads, *st, params, hp, scaler, policy, sums)
+        else:
+            pairs = [[t, shifted(torch.full_like(t, float("nan")))] for t in st]
+            z.zero1_step_dynamic_pingpong(plan, 0, M, grads, *pairs, params, hp, scaler, policy)
+            st = list(z.current_state(scaler, *pairs))
+        torch.cuda.synchronize()
+        for x, want, what in zip(st, o, ("master", "m", "v")):
+            assert_f32_bits(f32(x), want, f"{design} {what} M={M}")
+        assert_bf16_bits(u16(params), want_p, f"{design} params M={M}")
+
+    # unfused chain: reduce-scatter to fp32, AdamW, all-gather
+    st = [shifted(t) for t in base_state]
+    params = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+    g = shifted(torch.zeros(P, dtype=torch.float32, device=dev))
+    inv = float(oracle.adamw_constants(oracle_hp(hp))["inv"])
+    z.zero1_reduce_scatter(plan, 0, M, grads, inv, g)
+    z.zero1_adamw_update(plan, 0, M, g, *st, hp)
+    z.zero1_all_gather(plan, 0, M, st[0], params)
+    torch.cuda.synchronize()
+    for x, want, what in zip(st, o, ("master", "m", "v")):
+        assert_f32_bits(f32(x), want, f"unfused {what} M={M}")
+    assert_bf16_bits(u16(params), want_p, f"unfused params M={M}")

@@ -1,7 +1,7 @@
 """Seeded random configurations against the oracle, bit for bit: replica
 count, size, alignment unit, shard sub-range, the element phase of every
-buffer (so the vector head, the per-element fallback and the ragged tail all
-occur), hyperparameters and step, and every entry point that computes the
+buffer (so the vector head, 32- and 16-byte fp32 accesses, the per-element
+fallback and the ragged tail all occur), hyperparameters and step, and every entry point that computes the
 step (one-shot, prepared, bucketed, shared-memory staged, dynamic, ping-pong
 whole and in buckets, and the copy-engine staged step with state or
 gradients in pinned host memory, with and without dynamic loss scaling)."""
@@ -48,8 +48,15 @@ def test_random_configuration(cuda_device, case):
     se = int(rng.integers(sb + 1, M + 1))
     base, L, nv = plan.shard_range(sb, se)
     entry = ENTRIES[case % len(ENTRIES)]
-    same_phase = bool(rng.random() < 0.6)
-    ph = (lambda: 0) if same_phase else (lambda: int(rng.integers(0, 8)))
+    # buffer phases: all at the allocation's start (32-byte accesses); fp32
+    # buffers 16 bytes in (the vector body moves fp32 in 16-byte accesses);
+    # or every buffer at a random element phase (mostly the per-element path)
+    mode = str(rng.choice(["same", "state16", "mixed"], p=[0.45, 0.2, 0.35]))
+    if mode == "mixed":
+        ph = ph32 = lambda: int(rng.integers(0, 8))
+    else:
+        ph = lambda: 0
+        ph32 = (lambda: 4) if mode == "state16" else ph
     g_np = [(rng.standard_normal(nv) * 10 ** rng.uniform(-4, -1)).astype(np.float32) for _ in range(M)]
     g_np = [oracle.f32_to_bf16(x) for x in g_np]
     grads = []
@@ -65,7 +72,7 @@ def test_random_configuration(cuda_device, case):
     v_np[nv:] = 0
     state = []
     for a in (w_np, m_np, v_np):
-        t = _buf(L, torch.float32, ph(), dev)
+        t = _buf(L, torch.float32, ph32(), dev)
         t.copy_(torch.from_numpy(a))
         state.append(t)
     params = _buf(nv, torch.bfloat16, ph(), dev)
@@ -84,13 +91,13 @@ def test_random_configuration(cuda_device, case):
         policy = z.LossScalePolicy(initial_scale=S, window=1000, hysteresis=2)
         scaler = z.new_scaler(dev)
         z.zero1_scaler_init(scaler, policy, hp)
-        sums = _buf(L, torch.float32, ph(), dev)
+        sums = _buf(L, torch.float32, ph32(), dev)
         z.zero1_step_dynamic(plan, sb, se, grads, *state, params, hp, scaler, policy, sums)
     elif entry in ("pingpong", "pingpong_buckets"):
         policy = z.LossScalePolicy(initial_scale=S, window=1000, hysteresis=2)
         scaler = z.new_scaler(dev)
         z.zero1_scaler_init(scaler, policy, hp)
-        pairs = [[t, _buf(L, torch.float32, ph(), dev).fill_(float("nan"))] for t in state]
+        pairs = [[t, _buf(L, torch.float32, ph32(), dev).fill_(float("nan"))] for t in state]
         if entry == "pingpong":
             z.zero1_step_dynamic_pingpong(plan, sb, se, grads, *pairs, params, hp, scaler, policy)
         else:
@@ -103,7 +110,7 @@ def test_random_configuration(cuda_device, case):
             attempt.finish(hp)
         state = list(z.current_state(scaler, *pairs))
     elif entry in ("staged_state", "staged_dynamic"):
-        state = [_pinned_like(t, ph()) for t in state]
+        state = [_pinned_like(t, ph32()) for t in state]
         step = z.HostStreamedStep(plan, sb, se, grads, *state, params, chunk_elems=int(rng.integers(1, 6000)))
         if entry == "staged_dynamic":
             policy = z.LossScalePolicy(initial_scale=S, window=1000, hysteresis=2)
@@ -128,7 +135,7 @@ def test_random_configuration(cuda_device, case):
     torch.cuda.synchronize()
     want_p = np.zeros(nv, np.uint16)
     oracle.zero1_step(g_np, nv, w_np, m_np, v_np, want_p, oracle_hp(hp))
-    what = f"case {case}: {entry} M={M} n={n} align={align} shards=[{sb},{se}) phases={'same' if same_phase else 'mixed'}"
+    what = f"case {case}: {entry} M={M} n={n} align={align} shards=[{sb},{se}) phases={mode}"
     assert_f32_bits(f32(state[0]), w_np, "master " + what)
     assert_f32_bits(f32(state[1]), m_np, "m " + what)
     assert_f32_bits(f32(state[2]), v_np, "v " + what)

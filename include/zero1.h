@@ -543,7 +543,9 @@ const char *zero1_last_error(void);
 int zero1_abi_version(void);
 
 /* Introspection for tests and tuning (no counterpart in the pages): the last
- * kernel that a library call launched on this host thread.  *kernel_name
+ * streaming kernel that a library call launched on this host thread (every
+ * kernel whose grid is sized as one resident wave; not the one-thread scaler
+ * kernels, the shared-memory staged kernel or the wait self-test).  *kernel_name
  * gets its (mangled) name, owned by the CUDA runtime; *grid the blocks it was
  * launched with; *blocks_per_sm the resident blocks per SM the grid was
  * sized from (one wave = SMs x blocks_per_sm, each kernel's own occupancy);

@@ -168,7 +168,7 @@ int zero1_plan_memory(const zero1_plan_t *plan, int64_t *naive_bytes_per_rank,
  * range holds no real parameter (nv == 0: all padding) grads and params are
  * not touched and may be NULL.
  * EINVAL: NULL pointers, bad range, bad hyperparameters, skip_if_flag with a
- * NULL flag. */
+ * NULL flag, master/m/v/params overlapping one another or a gradient buffer. */
 int zero1_reduce_scatter_adamw_allgather(const zero1_plan_t *plan, int32_t shard_begin,
                                          int32_t shard_end, const void *const *grads,
                                          float *master, float *m, float *v, void *params,
@@ -237,8 +237,8 @@ int zero1_step_bucket(const zero1_plan_t *plan, int64_t elem_begin, int64_t elem
  * zero1_staged_destroy waits for the handle's queued work, then frees it
  * (NULL is accepted).
  * EINVAL: bad range, `what` or chunk size, a NULL or misplaced buffer (host
- * where device memory is required or the reverse), the wrong current device,
- * a capturing stream.  All arguments are checked before anything is
+ * where device memory is required or the reverse), overlapping buffers, the
+ * wrong current device, a capturing stream.  All arguments are checked before anything is
  * enqueued; on ZERO1_ECUDA part of the step may have been enqueued. */
 #define ZERO1_STAGE_GRADS 1
 #define ZERO1_STAGE_STATE 2
@@ -410,7 +410,9 @@ int zero1_scaler_init(zero1_scaler_t *scaler, const zero1_loss_scale_policy_t *p
  *           step are ignored: the scaler's are used);
  *  scaler:  device pointer, started with zero1_scaler_init;
  *  sums:    device fp32 workspace of at least L elements (scratch; its
- *           contents on return are the last attempt's sums). */
+ *           contents on return are the last attempt's sums).
+ * EINVAL as the fused step, also if sums or the scaler overlaps another
+ * buffer. */
 int zero1_step_dynamic(const zero1_plan_t *plan, int32_t shard_begin, int32_t shard_end,
                        const void *const *grads, float *master, float *m, float *v, void *params,
                        const zero1_adamw_t *hp, zero1_scaler_t *scaler,
@@ -436,7 +438,8 @@ int zero1_step_dynamic(const zero1_plan_t *plan, int32_t shard_begin, int32_t sh
  * at the same 16-byte phase for the 128-bit path (else the whole range runs
  * per element).  No workspace is needed; the call can be captured in a CUDA
  * graph (the copy to read is decided on the device).  EINVAL: as
- * zero1_step_dynamic, or the two copies of an array are the same buffer. */
+ * zero1_step_dynamic, or any two of the six state buffers, params, the
+ * scaler and the gradients overlap (the gradients may alias one another). */
 int zero1_step_dynamic_pingpong(const zero1_plan_t *plan, int32_t shard_begin, int32_t shard_end,
                                 const void *const *grads, float *const *master, float *const *m,
                                 float *const *v, void *params, const zero1_adamw_t *hp, zero1_scaler_t *scaler,

@@ -133,6 +133,16 @@ def test_fused_step_rejects_bad_arguments(lib):
     assert _fused(lib, plan, sb=-1, se=2) == -1
     assert _fused(lib, plan, grads=_ptr_array([A, A, None, A])) == -1
     assert _fused(lib, plan, master=None) == -1
+    # buffers the step writes must not overlap each other or the gradients
+    assert _fused(lib, plan, m=A) == -1                             # m is master
+    assert _fused(lib, plan, v=A + 4096 + 2048) == -1               # v starts inside m
+    assert _fused(lib, plan, params=A + 8192 + 4000) == -1          # params runs into v's end
+    assert _fused(lib, plan, grads=_ptr_array([A + 65536] * 3 + [A + 12288 + 1000])) == -1  # a gradient inside params
+    assert "overlap" in lib.zero1_last_error().decode()
+    # gradient buffers may alias one another, and neighbours may touch: this
+    # call passes the host checks (it fails later only because the addresses
+    # are fake, when the pointer kind is looked up or the launch is made)
+    assert _fused(lib, plan, grads=_ptr_array([A + 65536] * 4)) in (-4, 0)
     assert _fused(lib, plan, master=A + 2) == -2          # fp32 not 4-byte aligned
     assert _fused(lib, plan, params=A + 1) == -2          # bf16 odd address
     assert _fused(lib, plan, grads=_ptr_array([A, A + 3, A, A])) == -2
@@ -214,6 +224,14 @@ def test_pingpong_entries_reject_bad_arguments(lib):
     w, m, v = two(A, A + 8192), two(A + 16384, A + 24576), two(A + 32768, A + 40960)
     step = lambda *a: lib.zero1_step_dynamic_pingpong(P, 0, 2, g, *a)
     assert step(two(A, A), m, v, A + 49152, hp, sc, pol, None) == -1             # one buffer for both copies
+    assert step(two(A, A + 2048), m, v, A + 49152, hp, sc, pol, None) == -1      # copy 1 inside copy 0
+    assert step(w, m, v, A + 65536 + 1024, hp, sc, pol, None) == -1             # params inside grads[0]
+    assert step(w, m, v, A + 49152, hp, A + 40960 + 512, pol, None) == -1       # scaler inside v[1]
+    assert b"overlap" in lib.zero1_last_error()
+    dyn = lambda sums, mm=A + 16384: lib.zero1_step_dynamic(P, 0, 2, g, A, mm, A + 32768, A + 49152, hp, sc, pol,
+                                                            sums, None)
+    assert dyn(A) == -1                                                         # sums is master
+    assert dyn(A + 24576, mm=A + 2048) == -1                                    # m inside master
     assert step(two(A, A + 8194), m, v, A + 49152, hp, sc, pol, None) == -2      # copy 1 misaligned
     assert step(None, m, v, A + 49152, hp, sc, pol, None) == -1
     assert step(w, m, v, A + 49152, hp, sc + 4, pol, None) == -2                # scaler not 8-byte aligned

@@ -524,6 +524,38 @@ Walk make_walk(int64_t L, int64_t nv, const ArrayRef *a, int count)
     return w;
 }
 
+// A buffer's byte extent, for the overlap checks.
+struct Extent {
+    const void *p;
+    int64_t bytes;
+    const char *what;
+};
+
+bool overlap(const Extent &a, const Extent &b)
+{
+    if (a.bytes <= 0 || b.bytes <= 0 || !a.p || !b.p) return false;
+    const uintptr_t a0 = (uintptr_t)a.p, a1 = a0 + (uintptr_t)a.bytes;
+    const uintptr_t b0 = (uintptr_t)b.p, b1 = b0 + (uintptr_t)b.bytes;
+    return a0 < b1 && b0 < a1;
+}
+
+// EINVAL unless the `nout` buffers a call writes are pairwise disjoint and
+// none of the M gradient buffers (`nv` bf16 elements each, read through the
+// read-only path; they may alias one another) overlaps one of them.
+int check_disjoint(const Extent *out, int nout, const GradPtrs &g, int M, int64_t nv, const char *call)
+{
+    for (int a = 0; a < nout; ++a)
+        for (int b = a + 1; b < nout; ++b)
+            if (overlap(out[a], out[b]))
+                return z1_fail(ZERO1_EINVAL, "%s: %s and %s overlap", call, out[a].what, out[b].what);
+    for (int r = 0; r < M && nv > 0; ++r) {
+        const Extent gr{g.p[r], nv * 2, "a gradient buffer"};
+        for (int a = 0; a < nout; ++a)
+            if (overlap(gr, out[a])) return z1_fail(ZERO1_EINVAL, "%s: grads[%d] overlaps %s", call, r, out[a].what);
+    }
+    return ZERO1_OK;
+}
+
 int check_natural(const void *p, int esize, const char *what)
 {
     if (((uintptr_t)p & (uintptr_t)(esize - 1)) != 0)

@@ -372,6 +372,9 @@ extern "C" int zero1_step_dynamic(const zero1_plan_t *plan, int32_t shard_begin,
         (rc = check_natural(v, 4, "v")) || (rc = check_natural(params, 2, "params")) ||
         (rc = check_natural(sums, 4, "sums")))
         return rc;
+    const Extent out[6] = {{master, r.L * 4, "master"}, {m, r.L * 4, "m"},   {v, r.L * 4, "v"},
+                           {params, r.nv * 2, "params"},  {sums, r.L * 4, "sums"}, {scaler, (int64_t)sizeof(zero1_scaler_t), "the scaler"}};
+    if ((rc = check_disjoint(out, 6, g, plan->M, r.nv, "dynamic step")) != ZERO1_OK) return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const int M = plan->M;
     // 1. reduce-scatter into the fp32 sums, flag into the scaler
@@ -435,6 +438,10 @@ int launch_pingpong_range(const zero1_plan_t *plan, int64_t L, int64_t nv, const
     if ((rc = check_natural(params, 2, "params")) != ZERO1_OK) return rc;
     GradPtrs g{};
     if (nv > 0 && (rc = load_grads(plan, grads, &g, what)) != ZERO1_OK) return rc;
+    const Extent out[8] = {{s.master[0], L * 4, "master[0]"}, {s.mom[0], L * 4, "m[0]"}, {s.var[0], L * 4, "v[0]"},
+                           {s.master[1], L * 4, "master[1]"}, {s.mom[1], L * 4, "m[1]"}, {s.var[1], L * 4, "v[1]"},
+                           {params, nv * 2, "params"},        {scaler, (int64_t)sizeof(zero1_scaler_t), "the scaler"}};
+    if ((rc = check_disjoint(out, 8, g, plan->M, nv, what)) != ZERO1_OK) return rc;
     // one walk serves both copies: they must share the 16-byte phase
     ArrayRef arr[ZERO1_MAX_REPLICAS + 7] = {{s.master[0], 4}, {s.mom[0], 4}, {s.var[0], 4}, {s.master[1], 4},
                                             {s.mom[1], 4},    {s.var[1], 4}, {params, 2}};
@@ -556,6 +563,8 @@ int z1_scaled_range(const zero1_plan_t *plan, int64_t elem_begin, int64_t elem_e
     if ((rc = check_natural(master, 4, "master")) || (rc = check_natural(m, 4, "m")) ||
         (rc = check_natural(v, 4, "v")) || (rc = check_natural(params, 2, "params")))
         return rc;
+    const Extent out[4] = {{master, L * 4, "master"}, {m, L * 4, "m"}, {v, L * 4, "v"}, {params, nv * 2, "params"}};
+    if ((rc = check_disjoint(out, 4, g, plan->M, nv, "scaled range")) != ZERO1_OK) return rc;
     ArrayRef arr[ZERO1_MAX_REPLICAS + 4] = {{master, 4}, {m, 4}, {v, 4}, {params, 2}};
     const int M = plan->M;
     for (int k = 0; k < M; ++k) arr[4 + k] = {g.p[k], 2};

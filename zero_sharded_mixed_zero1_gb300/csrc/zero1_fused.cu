@@ -211,6 +211,8 @@ int launch_fused_range(const zero1_plan_t *plan, int64_t L, int64_t nv, const vo
         (rc = check_natural(v, 4, "v")) || (rc = check_natural(params, 2, "params")) ||
         (overflow_flag && (rc = check_natural(overflow_flag, 4, "overflow_flag"))))
         return rc;
+    const Extent out[4] = {{master, L * 4, "master"}, {m, L * 4, "m"}, {v, L * 4, "v"}, {params, nv * 2, "params"}};
+    if ((rc = check_disjoint(out, 4, g, plan->M, nv, what)) != ZERO1_OK) return rc;
     ArrayRef arr[ZERO1_MAX_REPLICAS + 4] = {{master, 4}, {m, 4}, {v, 4}, {params, 2}};
     for (int k = 0; k < plan->M; ++k) arr[4 + k] = {g.p[k], 2};
     const Walk w = make_walk(L, nv, arr, 4 + plan->M);

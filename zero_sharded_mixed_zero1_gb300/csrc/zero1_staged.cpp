@@ -62,6 +62,11 @@ int check_buffer(const void *p, bool staged, int elem, const char *what)
     return ZERO1_OK;
 }
 
+// EINVAL if buffers the step writes overlap one another or the gradients
+// (the gradients may alias one another).
+int check_staged_disjoint(const zero1_staged_t *h, const void *const *grads, const float *master, const float *m,
+                          const float *v, const void *params, const void *params_host);
+
 int cuda_fail(cudaError_t e, const char *what)
 {
     return z1_fail(ZERO1_ECUDA, "staged step: %s: %s", what, cudaGetErrorString(e));
@@ -90,6 +95,37 @@ struct zero1_staged {
 };
 
 namespace {
+
+bool spans_overlap(const void *a, int64_t abytes, const void *b, int64_t bbytes)
+{
+    if (!a || !b || abytes <= 0 || bbytes <= 0) return false;
+    const uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
+    return a0 < b0 + (uintptr_t)bbytes && b0 < a0 + (uintptr_t)abytes;
+}
+
+int check_staged_disjoint(const zero1_staged_t *h, const void *const *grads, const float *master, const float *m,
+                          const float *v, const void *params, const void *params_host)
+{
+    struct Span {
+        const void *p;
+        int64_t bytes;
+        const char *what;
+    };
+    const Span out[5] = {{master, h->L * 4, "master"},
+                         {m, h->L * 4, "m"},
+                         {v, h->L * 4, "v"},
+                         {params, h->nv * 2, "params"},
+                         {params_host, h->nv * 2, "params_host"}};
+    for (int a = 0; a < 5; ++a)
+        for (int b = a + 1; b < 5; ++b)
+            if (spans_overlap(out[a].p, out[a].bytes, out[b].p, out[b].bytes))
+                return z1_fail(ZERO1_EINVAL, "staged step: %s and %s overlap", out[a].what, out[b].what);
+    for (int r = 0; r < h->plan.M && h->nv > 0 && grads; ++r)
+        for (int a = 0; a < 5; ++a)
+            if (spans_overlap(grads[r], h->nv * 2, out[a].p, out[a].bytes))
+                return z1_fail(ZERO1_EINVAL, "staged step: grads[%d] overlaps %s", r, out[a].what);
+    return ZERO1_OK;
+}
 
 int64_t round8(int64_t x) { return (x + 7) / 8 * 8; }
 
@@ -260,6 +296,8 @@ int staged_run(zero1_staged_t *h, const void *const *grads, float *master, float
         (rc = check_buffer(v, ss, 4, "v")))
         return rc;
     if (overflow_flag && (rc = check_buffer(overflow_flag, false, 4, "overflow_flag")) != ZERO1_OK) return rc;
+    if ((rc = check_staged_disjoint(h, grads, master, m, v, params, sp ? params_host : nullptr)) != ZERO1_OK)
+        return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
     if ((e = cudaStreamIsCapturing(st, &cap)) != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");

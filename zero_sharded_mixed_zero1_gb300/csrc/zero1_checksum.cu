@@ -2,6 +2,7 @@
 // silent-data-corruption guard for the replicated parameters.
 
 #include "zero1_device.cuh"
+#include "zero1_checks.h"
 
 namespace {
 

@@ -6,6 +6,7 @@
 #include <mutex>
 
 #include "zero1_device.cuh"
+#include "zero1_checks.h"
 
 namespace {
 
@@ -391,11 +392,15 @@ extern "C" int zero1_step_dynamic(const zero1_plan_t *plan, int32_t shard_begin,
     const ArrayRef ua[5] = {{sums, 4}, {master, 4}, {m, 4}, {v, 4}, {params, 2}};
     const Walk wu = make_walk(r.L, r.nv, ua, 5);
     const int grid = grid_for(k_apply_sums, wu);
-    launch_pdl(k_apply_sums, grid, kBlock, st, (const float *)sums, master, m, v, static_cast<uint16_t *>(params), wu,
-               c, (const zero1_scaler_t *)scaler);
-    // 3. the scaler advances
+    if ((rc = launch_status("dynamic step: reduce-scatter launch")) != ZERO1_OK) return rc;
+    const cudaError_t e = launch_pdl(k_apply_sums, grid, kBlock, st, (const float *)sums, master, m, v,
+                                     static_cast<uint16_t *>(params), wu, c, (const zero1_scaler_t *)scaler);
+    if (e != cudaSuccess) return pdl_fail(e, "dynamic step: update launch");
+    // 3. the scaler advances (only once the update is enqueued)
     const ScalePolicy pol{policy->factor, policy->window, policy->hysteresis, policy->min_scale};
-    launch_pdl(k_scaler_update, 1, 32, st, scaler, pol, (int64_t)hp->global_batch, hp->beta1, hp->beta2, 0);
+    const cudaError_t e2 =
+        launch_pdl(k_scaler_update, 1, 32, st, scaler, pol, (int64_t)hp->global_batch, hp->beta1, hp->beta2, 0);
+    if (e2 != cudaSuccess) return pdl_fail(e2, "dynamic step: scaler launch");
     return launch_status("dynamic step launch");
 }
 
@@ -481,9 +486,13 @@ int launch_pingpong_finish(const zero1_plan_t *plan, int64_t L, int64_t nv, floa
     const ArrayRef arr[3] = {{master[0], 4}, {master[1], 4}, {params, 2}};
     const Walk w = make_walk(L, nv, arr, 3);
     const int grid = grid_for(k_restore_params, w);
-    launch_pdl(k_restore_params, grid, kBlock, st, s, static_cast<uint16_t *>(params), w, (const zero1_scaler_t *)scaler);
+    const cudaError_t e =
+        launch_pdl(k_restore_params, grid, kBlock, st, s, static_cast<uint16_t *>(params), w, (const zero1_scaler_t *)scaler);
+    if (e != cudaSuccess) return pdl_fail(e, what);
     const ScalePolicy pol{policy->factor, policy->window, policy->hysteresis, policy->min_scale};
-    launch_pdl(k_scaler_update, 1, 32, st, scaler, pol, (int64_t)hp->global_batch, hp->beta1, hp->beta2, 1);
+    const cudaError_t e2 =
+        launch_pdl(k_scaler_update, 1, 32, st, scaler, pol, (int64_t)hp->global_batch, hp->beta1, hp->beta2, 1);
+    if (e2 != cudaSuccess) return pdl_fail(e2, what);
     return launch_status(what);
 }
 

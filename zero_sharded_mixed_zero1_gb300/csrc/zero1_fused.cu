@@ -17,6 +17,7 @@
 // are reproducible bit for bit.
 
 #include "zero1_device.cuh"
+#include "zero1_checks.h"
 
 namespace {
 

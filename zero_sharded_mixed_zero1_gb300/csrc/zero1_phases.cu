@@ -7,6 +7,7 @@
 // uses it too.)
 
 #include "zero1_device.cuh"
+#include "zero1_checks.h"
 
 namespace {
 
@@ -329,7 +330,8 @@ extern "C" int zero1_adamw_update(const zero1_plan_t *plan, int32_t shard_begin,
     const Walk w = make_walk(r.L, r.L, arr, 4);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const int grid = grid_for(k_adamw, w);
-    launch_pdl(k_adamw, grid, kBlock, st, gin, master, m, v, w, c);
+    const cudaError_t e = launch_pdl(k_adamw, grid, kBlock, st, gin, master, m, v, w, c);
+    if (e != cudaSuccess) return pdl_fail(e, "adamw launch");
     return launch_status("adamw launch");
 }
 
@@ -347,7 +349,8 @@ extern "C" int zero1_all_gather(const zero1_plan_t *plan, int32_t shard_begin, i
     const Walk w = make_walk(r.nv, r.nv, arr, 2);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const int grid = grid_for(k_all_gather, w);
-    launch_pdl(k_all_gather, grid, kBlock, st, master, static_cast<uint16_t *>(params), w);
+    const cudaError_t e = launch_pdl(k_all_gather, grid, kBlock, st, master, static_cast<uint16_t *>(params), w);
+    if (e != cudaSuccess) return pdl_fail(e, "all-gather launch");
     return launch_status("all-gather launch");
 }
 

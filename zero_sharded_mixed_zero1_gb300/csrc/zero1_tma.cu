@@ -3,6 +3,7 @@
 // the design comparison with the direct loads of zero1_fused.cu.
 
 #include "zero1_device.cuh"
+#include "zero1_checks.h"
 
 namespace {
 

@@ -322,7 +322,9 @@ int dp_allreduce(const zero1_plan_t *plan, const void *const *grads_in, void *co
  *
  * Reduce-scatter [COLL]: out (device, L elements of out_dtype) gets
  * (rank order fp32 sum) * scale for the nv real elements and +0 for padding;
- * flag (device, may be NULL) as in zero1_overflow_check. */
+ * flag (device, may be NULL) as in zero1_overflow_check.  These calls reject
+ * (EINVAL) a buffer they write that overlaps another buffer of the call (the
+ * gradients may alias one another). */
 int zero1_reduce_scatter(const zero1_plan_t *plan, int32_t shard_begin, int32_t shard_end,
                          const void *const *grads, float scale, int32_t out_dtype, void *out,
                          uint32_t *flag, zero1_stream_t stream);

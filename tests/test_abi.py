@@ -176,6 +176,10 @@ def test_other_entry_points_reject_bad_arguments(lib):
     assert lib.zero1_reduce_scatter(P, 0, 2, g, 1.0, 5, A, None, None) == -1
     assert lib.zero1_reduce_scatter(P, 0, 2, g, 1.0, 1, A + 2, None, None) == -2
     assert lib.zero1_adamw_update(P, 0, 2, None, A, A, A, ctypes.byref(_hp()), None) == -1
+    assert lib.zero1_adamw_update(P, 0, 2, A, A + 8192, A + 8192, A + 16384, ctypes.byref(_hp()), None) == -1
+    assert lib.zero1_reduce_scatter(P, 0, 2, g, 1.0, 1, A + 2048, None, None) == -1     # out inside grads[0]
+    assert lib.zero1_all_gather(P, 0, 2, A, A + 2048, None) == -1                      # params inside master
+    assert lib.zero1_all_gather_shards(P, A, _ptr_array([A + 1024, A + 65536]), None) == -1
     assert lib.zero1_all_gather(P, 1, 1, A, A, None) == -1
     assert lib.zero1_all_gather_shards(P, A + 1, o, None) == -2
     assert lib.zero1_strerror(-2) == b"misaligned device pointer"

@@ -293,6 +293,8 @@ extern "C" int zero1_reduce_scatter(const zero1_plan_t *plan, int32_t shard_begi
     if (flag && (rc = check_natural(flag, 4, "flag")) != ZERO1_OK) return rc;
     GradPtrs g{};
     if (r.nv > 0 && (rc = load_grads(plan, grads, &g, "reduce-scatter")) != ZERO1_OK) return rc;
+    const Extent outs[2] = {{out, r.L * osz, "out"}, {flag, 4, "flag"}};
+    if ((rc = check_disjoint(outs, 2, g, plan->M, r.nv, "reduce-scatter")) != ZERO1_OK) return rc;
     ArrayRef arr[ZERO1_MAX_REPLICAS + 1] = {{out, osz}};
     for (int k = 0; k < plan->M; ++k) arr[1 + k] = {g.p[k], 2};
     const Walk w = make_walk(r.L, r.nv, arr, 1 + plan->M);
@@ -325,6 +327,8 @@ extern "C" int zero1_adamw_update(const zero1_plan_t *plan, int32_t shard_begin,
     if ((rc = check_natural(gin, 4, "g")) || (rc = check_natural(master, 4, "master")) ||
         (rc = check_natural(m, 4, "m")) || (rc = check_natural(v, 4, "v")))
         return rc;
+    const Extent bufs[4] = {{gin, r.L * 4, "g"}, {master, r.L * 4, "master"}, {m, r.L * 4, "m"}, {v, r.L * 4, "v"}};
+    if ((rc = check_disjoint(bufs, 4, GradPtrs{}, 0, 0, "adamw")) != ZERO1_OK) return rc;
     const ArrayRef arr[4] = {{gin, 4}, {master, 4}, {m, 4}, {v, 4}};
     // every element of the range is updated: walk it as if all were real
     const Walk w = make_walk(r.L, r.L, arr, 4);
@@ -345,6 +349,8 @@ extern "C" int zero1_all_gather(const zero1_plan_t *plan, int32_t shard_begin, i
     if (r.nv == 0) return ZERO1_OK;
     if (!master || !params) return z1_fail(ZERO1_EINVAL, "all-gather: NULL array");
     if ((rc = check_natural(master, 4, "master")) || (rc = check_natural(params, 2, "params"))) return rc;
+    const Extent bufs[2] = {{master, r.nv * 4, "master"}, {params, r.nv * 2, "params"}};
+    if ((rc = check_disjoint(bufs, 2, GradPtrs{}, 0, 0, "all-gather")) != ZERO1_OK) return rc;
     const ArrayRef arr[2] = {{master, 4}, {params, 2}};
     const Walk w = make_walk(r.nv, r.nv, arr, 2);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -367,6 +373,8 @@ extern "C" int zero1_all_gather_shards(const zero1_plan_t *plan, const void *sha
     for (int k = 0; k < plan->M; ++k) {
         if (!outs[k]) return z1_fail(ZERO1_EINVAL, "all-gather shards: outs[%d] is NULL", k);
         if ((rc = check_natural(outs[k], 2, "an all-gather output")) != ZERO1_OK) return rc;
+        if (overlap({shards, plan->padded_n * 2, "shards"}, {outs[k], plan->n * 2, "an output"}))
+            return z1_fail(ZERO1_EINVAL, "all-gather shards: outs[%d] overlaps the shards", k);
         o.p[k] = outs[k];
         arr[1 + k] = {outs[k], 2};
     }

@@ -719,9 +719,10 @@ def main(argv=None) -> int:
                          "with the fp16 block's policy instead of the fused step")
     ap.add_argument("--state-on-host", action="store_true",
                     help="keep fp32 master/m/v in pinned host memory (optimizer-state offload)")
-    ap.add_argument("--offload-transfer", choices=["zero_copy", "copy_engines"], default="copy_engines",
+    ap.add_argument("--offload-transfer", choices=["zero_copy", "copy_engines"], default="zero_copy",
                     help="with --state-on-host: the kernel reads and writes the host state over the link "
-                         "(zero_copy), or chunks are staged through HBM by the copy engines (copy_engines)")
+                         "(zero_copy, the faster one), or chunks are staged through HBM by the copy engines "
+                         "(copy_engines)")
     ap.add_argument("--chunk-elems", type=int, default=1 << 23,
                     help="chunk size of the staged (copy-engine) paths")
     args = ap.parse_args(argv)

@@ -389,6 +389,10 @@ def run_ours(args, w) -> None:
         return z.AdamW(lr=w.lr, beta1=w.beta1, beta2=w.beta2, eps=w.eps, weight_decay=w.weight_decay,
                        loss_scale=w.S, global_batch=w.B, step=t)
 
+    def second_copy(x):
+        """The ping-pong state's other copy, where x lives (pinned host or HBM)."""
+        return torch.empty(x.shape, dtype=x.dtype, pin_memory=True) if x.device.type == "cpu" else torch.empty_like(x)
+
     op = args.op if "pingpong" in args.op else ("dynamic" if args.dynamic_loss_scale else args.op)
     if op in ("dynamic", "dynamic_pingpong", "bucketed_pingpong"):
         policy = z.LossScalePolicy(initial_scale=w.S if w.S > 1 else 2.0 ** 12, factor=2.0, window=1000,
@@ -416,7 +420,7 @@ def run_ours(args, w) -> None:
             op_kernel = "dynamic step: k_reduce_scatter + k_apply_sums + k_scaler_update"
             launches_per_step, op_bytes = 3, algorithmic_bytes(nv, L - nv, w.M) + 8 * L
         elif op == "dynamic_pingpong":
-            pairs = [[x, torch.empty_like(x)] for x in (master, m, v)]
+            pairs = [[x, second_copy(x)] for x in (master, m, v)]
 
             def launch(gr, tt, st=None):
                 z.zero1_step_dynamic_pingpong(plan, sb, se, gr, *pairs, params, hp(tt), scaler, policy, stream=st)
@@ -426,7 +430,7 @@ def run_ours(args, w) -> None:
         else:
             # gradient buckets of reduce_bucket_size elements updated as they
             # arrive, the skip decided once all have run
-            pairs = [[x, torch.empty_like(x)] for x in (master, m, v)]
+            pairs = [[x, second_copy(x)] for x in (master, m, v)]
             buckets = z.PingPongBuckets(plan, sb, se, *pairs, params, scaler, policy, stream=stream)
             bucket = args.bucket_elems
             cuts = list(range(0, L, bucket)) + [L]
@@ -644,7 +648,7 @@ def run_ours(args, w) -> None:
     # with the state in host memory the step is bound by the host link: 12 B
     # of master/m/v in and 12 B out per element, measured against the link
     offload_link = None
-    if args.state_on_host and op in ("step", "dynamic"):
+    if args.state_on_host and op in ("step", "dynamic", "dynamic_pingpong", "bucketed_pingpong"):
         offload_link = link_roofline(host_link_rates(dev), 12 * L, 12 * L, ms_total * 1e-3 / args.steps)
         # host-link steps see occasional stalls from other work on the shared
         # host: the median step against the same bound

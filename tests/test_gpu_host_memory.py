@@ -353,3 +353,39 @@ def test_staged_timeline_is_ordered_and_changes_no_bit(cuda_device, where):
         plain.timeline()                             # created without tracing
     plain.close()
     traced.close()
+
+
+@pytest.mark.parametrize("M,n,align", [(8, 100_003, 128), (2, 30_001, 1), (13, 9_999, 8)])
+def test_pingpong_with_host_state_matches_oracle(cuda_device, M, n, align):
+    """The dynamically scaled ping-pong step with both copies of master/m/v in
+    pinned host memory (offload with one pass over the data): every attempt
+    bit for bit the oracle's, overflowing ones included."""
+    dev = cuda_device
+    plan = z.zero1_plan(n, M, align)
+    P = plan.padded_n
+    policy = z.LossScalePolicy(initial_scale=1024.0, factor=2.0, window=2, hysteresis=1, min_scale=1.0)
+    hp = z.AdamW(global_batch=max(M, 64), step=1)
+    state = [pinned(t) for t in make_state(n, P, 150 + M, dev, nonzero_moments=True)]
+    o = [f32(t).copy() for t in state]
+    pairs = [[t, torch.full((P,), float("nan"), dtype=torch.float32).pin_memory()] for t in state]
+    params = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+    o_p = np.zeros(n, np.uint16)
+    scaler = z.new_scaler(dev)
+    z.zero1_scaler_init(scaler, policy, hp)
+    o_policy = oracle.LossScalePolicy(initial_scale=policy.initial_scale, factor=policy.factor,
+                                      window=policy.window, hysteresis=policy.hysteresis, min_scale=policy.min_scale)
+    o_sc = oracle.Scaler.start(o_policy, hp.step)
+    for k in range(5):
+        grads = make_grads(M, n, 1e-3 * o_sc.scale, 160 + M, k, dev)
+        if k in (1, 2):
+            grads[k % M][(31 * k) % n] = float("inf")
+        z.zero1_step_dynamic_pingpong(plan, 0, M, grads, *pairs, params, hp, scaler, policy)
+        torch.cuda.synchronize()
+        flag = oracle.zero1_dynamic_attempt([u16(g) for g in grads], n, *o, o_p, oracle_hp(hp), o_sc, o_policy)
+        assert flag == (1 if k in (1, 2) else 0)
+        cur = z.current_state(scaler, *pairs)
+        for x, want, what in zip(cur, o, ("master", "m", "v")):
+            assert_f32_bits(f32(x), want, f"{what} attempt {k}")
+        assert_bf16_bits(u16(params), o_p, f"params attempt {k}")
+    st = z.scaler_state(scaler)
+    assert (st["step"], st["skipped"]) == (o_sc.step, o_sc.skipped) == (4, 2)

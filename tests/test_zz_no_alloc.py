@@ -118,3 +118,46 @@ def test_no_alloc_step_rejects_ranges_beyond_its_workspace(cuda_device):
     g16 = torch.zeros(8, dtype=torch.bfloat16, device=dev)
     with pytest.raises(ValueError):
         z.zero1_step_dynamic_noalloc(plan, 0, 1, [g16] * M, one, one, one, g16, hp, scaler, policy)
+
+
+def test_no_alloc_step_at_its_maximum_range(cuda_device):
+    """A range of exactly ZERO1_NOALLOC_MAX_ELEMS elements fills the built-in
+    array and is accepted; the result is the workspace step's and the
+    oracle's, bit for bit."""
+    dev = cuda_device
+    lib = z.load()
+    fn = _c_noalloc(lib)
+    M, n = 2, lib_max() - 5
+    plan = z.zero1_plan(n, M, 8)
+    P = plan.padded_n
+    assert P == lib_max()
+    policy = z.LossScalePolicy(initial_scale=64.0, factor=2.0, window=1000, hysteresis=2, min_scale=1.0)
+    hp = z.AdamW(global_batch=64, step=1)
+    a = _state(n, P, dev, 8)
+    b = [t.clone() for t in a]
+    o = [f32(t).copy() for t in a]
+    pa = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+    pb = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+    sa, sb = z.new_scaler(dev), z.new_scaler(dev)
+    z.zero1_scaler_init(sa, policy, hp)
+    z.zero1_scaler_init(sb, policy, hp)
+    grads = [synth.normal_bf16(n, 1e-3 * 64, synth.seed_of(9, r), dev) for r in range(M)]
+    z.zero1_step_dynamic(plan, 0, M, grads, *a, pa, hp, sa, policy, torch.empty(P, dtype=torch.float32, device=dev))
+    gp = (ctypes.c_void_p * M)(*[g.data_ptr() for g in grads])
+    rc = fn(ctypes.byref(plan), 0, M, gp, b[0].data_ptr(), b[1].data_ptr(), b[2].data_ptr(), pb.data_ptr(),
+            ctypes.byref(hp.c_struct()), sb.data_ptr(), ctypes.byref(policy.c_struct()),
+            torch.cuda.current_stream().cuda_stream)
+    assert rc == 0, lib.zero1_last_error()
+    torch.cuda.synchronize()
+    o_policy = oracle.LossScalePolicy(initial_scale=64.0, factor=2.0, window=1000, hysteresis=2, min_scale=1.0)
+    o_sc = oracle.Scaler.start(o_policy, 1)
+    o_p = np.zeros(n, np.uint16)
+    o_hp = oracle.AdamW(lr=hp.lr, beta1=hp.beta1, beta2=hp.beta2, eps=hp.eps, weight_decay=hp.weight_decay,
+                        global_batch=hp.global_batch)
+    assert oracle.zero1_dynamic_attempt([u16(g) for g in grads], n, *o, o_p, o_hp, o_sc, o_policy) == 0
+    for x, y, want, what in zip(a, b, o, ("master", "m", "v")):
+        assert_f32_bits(f32(y), f32(x), what)
+        assert_f32_bits(f32(y), want, what + " against the oracle")
+    assert_bf16_bits(u16(pb), u16(pa), "params")
+    assert_bf16_bits(u16(pb), o_p, "params against the oracle")
+    assert z.scaler_state(sb) == z.scaler_state(sa)

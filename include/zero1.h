@@ -166,7 +166,10 @@ int zero1_plan_memory(const zero1_plan_t *plan, int64_t *naive_bytes_per_rank,
  *                      on the same stream to skip a step globally).
  * Buffers must not overlap, except grads may alias one another.  When the
  * range holds no real parameter (nv == 0: all padding) grads and params are
- * not touched and may be NULL.
+ * not touched and may be NULL.  Keep master, m and v in the same kind of
+ * memory: the kernel is chosen from where master lives (pinned host memory
+ * selects the offload kernel, which keeps more state loads in flight and
+ * writes whole lines of host memory).
  * EINVAL: NULL pointers, bad range, bad hyperparameters, skip_if_flag with a
  * NULL flag, master/m/v/params overlapping one another or a gradient buffer. */
 int zero1_reduce_scatter_adamw_allgather(const zero1_plan_t *plan, int32_t shard_begin,

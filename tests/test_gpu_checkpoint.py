@@ -2,12 +2,16 @@
 master/m/v, the step counter and (for the dynamic path) the scaler.  Ten
 steps in a row must equal five steps, a save to disk, a load into fresh
 buffers and five more steps, bit for bit ("CS336 Lecture 7: Parallelism 1"
-case studies: long runs are interrupted and resumed)."""
+case studies: long runs are interrupted and resumed), and both must be the
+oracle's run."""
+import numpy as np
 import pytest
 import torch
 
+import oracle
 import zero_sharded_mixed_zero1_gb300 as z
-from test_gpu_parity import make_grads, make_state
+from gpu_helpers import assert_bf16_bits, assert_f32_bits, f32, oracle_hp, u16
+from test_gpu_parity import make_grads, make_state, oracle_step
 
 pytestmark = pytest.mark.gpu
 
@@ -20,6 +24,7 @@ def test_ten_steps_equal_five_save_load_five(cuda_device, tmp_path):
     grads = [make_grads(M, n, 1e-3, 41, t, dev) for t in range(1, 11)]
     run = make_state(n, P, 40, dev)
     ref = [t.clone() for t in run]
+    o = [f32(t).copy() for t in run]
     p_ref = torch.zeros(n, dtype=torch.bfloat16, device=dev)
     for t in range(1, 11):
         z.zero1_reduce_scatter_adamw_allgather(plan, 0, M, grads[t - 1], *ref, p_ref, z.AdamW(global_batch=512, step=t))
@@ -39,6 +44,12 @@ def test_ten_steps_equal_five_save_load_five(cuda_device, tmp_path):
     for a, b in zip(state, ref):
         assert torch.equal(a.view(torch.int32), b.view(torch.int32))
     assert torch.equal(p2.view(torch.int16), p_ref.view(torch.int16))
+    # and both are the oracle's ten steps
+    for t in range(1, 11):
+        o_p = oracle_step(plan, [u16(g) for g in grads[t - 1]], *o, oracle_hp(z.AdamW(global_batch=512, step=t)))
+    for a, want, what in zip(state, o, ("master", "m", "v")):
+        assert_f32_bits(f32(a), want, f"resumed {what} against the oracle")
+    assert_bf16_bits(u16(p2), o_p, "resumed params against the oracle")
 
 
 def test_dynamic_scaler_resumes(cuda_device, tmp_path):
@@ -78,6 +89,19 @@ def test_dynamic_scaler_resumes(cuda_device, tmp_path):
     assert torch.equal(p.view(torch.int16), pref.view(torch.int16))
     assert z.scaler_state(sc) == z.scaler_state(sref)
     assert z.scaler_state(sc)["skipped"] == 2
+    # and the oracle's eight attempts give the same state, parameters and scaler
+    o = [f32(t).copy() for t in make_state(n, P, 50, dev)]
+    o_p = np.zeros(n, np.uint16)
+    o_pol = oracle.LossScalePolicy(initial_scale=policy.initial_scale, factor=policy.factor, window=policy.window,
+                                   hysteresis=policy.hysteresis, min_scale=policy.min_scale)
+    o_sc = oracle.Scaler.start(o_pol, 1)
+    for k in range(8):
+        oracle.zero1_dynamic_attempt([u16(g) for g in grads[k]], n, *o, o_p, oracle_hp(hp), o_sc, o_pol)
+    for a, want, what in zip(state, o, ("master", "m", "v")):
+        assert_f32_bits(f32(a), want, f"resumed {what} against the oracle")
+    assert_bf16_bits(u16(p), o_p, "resumed params against the oracle")
+    st = z.scaler_state(sc)
+    assert (st["scale"], st["step"], st["skipped"]) == (o_sc.scale, o_sc.step, o_sc.skipped)
 
 
 def test_pingpong_resumes_from_the_current_copy(cuda_device, tmp_path):

@@ -241,8 +241,9 @@ int zero1_step_bucket(const zero1_plan_t *plan, int64_t elem_begin, int64_t elem
  * (NULL is accepted).
  * EINVAL: bad range, `what` or chunk size, a NULL or misplaced buffer (host
  * where device memory is required or the reverse), overlapping buffers, the
- * wrong current device, a capturing stream.  All arguments are checked before anything is
- * enqueued; on ZERO1_ECUDA part of the step may have been enqueued. */
+ * wrong current device, a capturing stream.  All arguments are checked before
+ * anything is enqueued; on ZERO1_ECUDA part of the step may have been
+ * enqueued. */
 #define ZERO1_STAGE_GRADS 1
 #define ZERO1_STAGE_STATE 2
 #define ZERO1_STAGE_PARAMS 4

@@ -16,7 +16,7 @@ from gpu_helpers import assert_bf16_bits, assert_f32_bits, f32, oracle_hp, u16
 pytestmark = pytest.mark.gpu
 
 ENTRIES = ["fused", "prepared", "bucket", "tma", "dynamic", "pingpong", "pingpong_buckets", "staged_state",
-           "staged_grads", "staged_dynamic"]
+           "staged_grads", "staged_dynamic", "offload", "pingpong_host"]
 
 
 def _buf(numel, dtype, phase, dev):
@@ -36,7 +36,7 @@ def _cuts(rng, L):
     return sorted({0, L, *[int(x) for x in rng.integers(0, L + 1, int(rng.integers(1, 6)))]})
 
 
-@pytest.mark.parametrize("case", range(140))
+@pytest.mark.parametrize("case", range(168))
 def test_random_configuration(cuda_device, case):
     dev = cuda_device
     rng = np.random.default_rng(20_000 + case)
@@ -93,12 +93,22 @@ def test_random_configuration(cuda_device, case):
         z.zero1_scaler_init(scaler, policy, hp)
         sums = _buf(L, torch.float32, ph32(), dev)
         z.zero1_step_dynamic(plan, sb, se, grads, *state, params, hp, scaler, policy, sums)
-    elif entry in ("pingpong", "pingpong_buckets"):
+    elif entry == "offload":
+        # master/m/v in pinned host memory, read and written by the offload kernel
+        state = [_pinned_like(t, ph32()) for t in state]
+        z.zero1_reduce_scatter_adamw_allgather(plan, sb, se, grads, *state, params, hp)
+    elif entry in ("pingpong", "pingpong_buckets", "pingpong_host"):
         policy = z.LossScalePolicy(initial_scale=S, window=1000, hysteresis=2)
         scaler = z.new_scaler(dev)
         z.zero1_scaler_init(scaler, policy, hp)
-        pairs = [[t, _buf(L, torch.float32, ph32(), dev).fill_(float("nan"))] for t in state]
-        if entry == "pingpong":
+        if entry == "pingpong_host":
+            # both copies in pinned host memory, at one phase
+            p32 = ph32()
+            state = [_pinned_like(t, p32) for t in state]
+            pairs = [[t, _pinned_like(torch.full((L,), float("nan")), p32)] for t in state]
+        else:
+            pairs = [[t, _buf(L, torch.float32, ph32(), dev).fill_(float("nan"))] for t in state]
+        if entry in ("pingpong", "pingpong_host"):
             z.zero1_step_dynamic_pingpong(plan, sb, se, grads, *pairs, params, hp, scaler, policy)
         else:
             attempt = z.PingPongBuckets(plan, sb, se, *pairs, params, scaler, policy)

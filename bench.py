@@ -37,6 +37,7 @@ import torch
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 METRIC = "params/s and achieved HBM GB/s (% of GB300 peak) per fused ZeRO-1 step"
+NOMINAL_HBM_GBS = 7900.0   # GB300 HBM3e, nominal
 # The fused kernel's sources, hashed in this order (concatenated) to tell
 # whether recorded ncu traffic was taken on the kernel as it stands.
 KERNEL_SOURCES = [os.path.join(ROOT, "zero_sharded_mixed_zero1_gb300", "csrc", f)
@@ -693,7 +694,9 @@ def run_ours(args, w) -> None:
                      "traffic": traffic, "traffic_source": traffic_note,
                      "kernel": op_kernel,
                      "bytes_per_launch": bytes_launch, "kernel_ms": kernel_ms,
-                     "kernel_ms_median": float(np.median(launch_ms)), "kernel_ms_min": float(launch_ms.min())},
+                     "kernel_ms_median": float(np.median(launch_ms)), "kernel_ms_min": float(launch_ms.min()),
+                     # context: the part's nominal HBM3e bandwidth (7.9 TB/s), not the roofline
+                     "nominal_gbs": NOMINAL_HBM_GBS, "frac_of_nominal": achieved / NOMINAL_HBM_GBS},
         "cpu_baseline": cpu_baseline,
         "offload_link_roofline": offload_link,
         "e2e": e2e if e2e is not None else ({"skipped": e2e_note} if e2e_note else None),

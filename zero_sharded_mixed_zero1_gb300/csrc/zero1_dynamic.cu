@@ -216,6 +216,7 @@ __global__ void __launch_bounds__(kBlock, MT == 0 ? 2 : (MT <= 2 ? 2 : 1))
 k_fused_step_pingpong(const __grid_constant__ GradPtrs g, int M, const __grid_constant__ PingPong s,
                       uint16_t *__restrict__ params, const Walk w, Z1Consts c, zero1_scaler_t *sc)
 {
+    wait_prior_grid();
     const uint32_t cur = *reinterpret_cast<const volatile uint32_t *>(&sc->current) & 1u;
     c.inv = sc->inv;
     c.bc1 = sc->bc1;
@@ -454,11 +455,13 @@ int launch_pingpong_range(const zero1_plan_t *plan, int64_t L, int64_t nv, const
     for (int k = 0; k < M; ++k) arr[7 + k] = {g.p[k], 2};
     const Walk w = make_walk(L, nv, arr, 7 + M);
     uint16_t *pp = static_cast<uint16_t *>(params);
+    cudaError_t e = cudaSuccess;
     dispatch_m(M, [&](auto mt) {
         constexpr int MT = decltype(mt)::value;
         const int grid = grid_for(k_fused_step_pingpong<MT>, w);
-        k_fused_step_pingpong<MT><<<grid, kBlock, 0, st>>>(g, M, s, pp, w, c, scaler);
+        e = launch_pdl(k_fused_step_pingpong<MT>, grid, kBlock, st, g, M, s, pp, w, c, scaler);
     });
+    if (e != cudaSuccess) return pdl_fail(e, what);
     return launch_status(what);
 }
 

@@ -49,6 +49,7 @@ k_fused_step(const __grid_constant__ GradPtrs g, int M, float *__restrict__ mast
              float *__restrict__ mom, float *__restrict__ var, uint16_t *__restrict__ params,
              const Walk w, const Z1Consts c, uint32_t *flag, int skip)
 {
+    wait_prior_grid();
     if (skip && *reinterpret_cast<volatile uint32_t *>(flag) != 0u) return;
     const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
     const int64_t nthr = (int64_t)gridDim.x * kBlock;
@@ -81,6 +82,7 @@ k_fused_step_wide(const __grid_constant__ GradPtrs g, int M, float *__restrict__
                   float *__restrict__ mom, float *__restrict__ var, uint16_t *__restrict__ params,
                   const Walk w, const Z1Consts c, uint32_t *flag, int skip)
 {
+    wait_prior_grid();
     if (skip && *reinterpret_cast<volatile uint32_t *>(flag) != 0u) return;
     const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
     const int64_t nthr = (int64_t)gridDim.x * kBlock;
@@ -106,6 +108,7 @@ k_fused_step_grouped(const __grid_constant__ GradPtrs g, int M, float *__restric
                      float *__restrict__ mom, float *__restrict__ var, uint16_t *__restrict__ params,
                      const Walk w, const Z1Consts c, uint32_t *flag, int skip)
 {
+    wait_prior_grid();
     if (skip && *reinterpret_cast<volatile uint32_t *>(flag) != 0u) return;
     const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
     const int64_t nthr = (int64_t)gridDim.x * kBlock;
@@ -153,6 +156,7 @@ k_fused_step_offload(const __grid_constant__ GradPtrs g, int M, float *__restric
                      float *__restrict__ mom, float *__restrict__ var, uint16_t *__restrict__ params,
                      const Walk w, const Z1Consts c, uint32_t *flag, int skip)
 {
+    wait_prior_grid();
     if (skip && *reinterpret_cast<volatile uint32_t *>(flag) != 0u) return;
     const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
     const int64_t nthr = (int64_t)gridDim.x * kBlock;
@@ -221,30 +225,36 @@ int launch_fused_range(const zero1_plan_t *plan, int64_t L, int64_t nv, const vo
     uint16_t *pp = static_cast<uint16_t *>(params);
     const int M = plan->M;
     const int skip = skip_if_flag ? 1 : 0;
+    // programmatic dependent launch: consecutive calls (buckets, chunks)
+    // overlap each launch with the end of the kernel before it
+    cudaError_t e = cudaSuccess;
     if (in_host_memory(master)) {
         dispatch_m(M, [&](auto mt) {
             constexpr int MT = decltype(mt)::value;
             const int grid = grid_for(k_fused_step_offload<MT>, w);
-            k_fused_step_offload<MT><<<grid, kBlock, 0, st>>>(g, M, master, m, v, pp, w, c, overflow_flag, skip);
+            e = launch_pdl(k_fused_step_offload<MT>, grid, kBlock, st, g, M, master, m, v, pp, w, c, overflow_flag,
+                           skip);
         });
     } else if (M > 8) {
         const int grid = grid_for(k_fused_step_grouped, w);
-        k_fused_step_grouped<<<grid, kBlock, 0, st>>>(g, M, master, m, v, pp, w, c, overflow_flag, skip);
+        e = launch_pdl(k_fused_step_grouped, grid, kBlock, st, g, M, master, m, v, pp, w, c, overflow_flag, skip);
     } else {
         dispatch_m(M, [&](auto mt) {
             constexpr int MT = decltype(mt)::value;
             if constexpr (MT > 0) {
                 if (w.nvec <= kWideMaxVec) {
                     const int grid = grid_for(k_fused_step_wide<MT>, w);
-                    k_fused_step_wide<MT><<<grid, kBlock, 0, st>>>(g, M, master, m, v, pp, w, c, overflow_flag,
-                                                                   skip);
+                    e = launch_pdl(k_fused_step_wide<MT>, grid, kBlock, st, g, M, master, m, v, pp, w, c,
+                                   overflow_flag, skip);
                 } else {
                     const int grid = grid_for(k_fused_step<MT>, w);
-                    k_fused_step<MT><<<grid, kBlock, 0, st>>>(g, M, master, m, v, pp, w, c, overflow_flag, skip);
+                    e = launch_pdl(k_fused_step<MT>, grid, kBlock, st, g, M, master, m, v, pp, w, c, overflow_flag,
+                                   skip);
                 }
             }
         });
     }
+    if (e != cudaSuccess) return pdl_fail(e, what);
     return launch_status(what);
 }
 

@@ -586,13 +586,22 @@ def run_ours(args, w) -> None:
         # the e2e gradients: drawn on the device (fast even at 1.3B x 8), then
         # placed in pinned host memory before anything is timed
         host_g = []
-        for r in range(w.M):
-            h = torch.empty(nv, dtype=torch.bfloat16, pin_memory=True)
-            h.copy_(synth.normal_bf16(nv, w.grad_std * w.S, synth.seed_of(w.seed, 7, r, rank), dev))
-            host_g.append(h)
+        refused = None
+        try:
+            for r in range(w.M):
+                h = torch.empty(nv, dtype=torch.bfloat16, pin_memory=True)
+                h.copy_(synth.normal_bf16(nv, w.grad_std * w.S, synth.seed_of(w.seed, 7, r, rank), dev))
+                host_g.append(h)
+            host_p = torch.empty(nv, dtype=torch.bfloat16, pin_memory=True)
+            host_f = torch.empty(1, dtype=torch.int32, pin_memory=True)
+        except RuntimeError as e:          # the host refused to pin this much memory
+            refused = str(e).splitlines()[0] if str(e) else type(e).__name__
+        # one decision for all ranks (they meet in barriers inside the leg)
+        if max_over_ranks(1.0 if refused else 0.0, world) > 0:
+            host_g = host_p = host_f = None
+            e2e_note = f"end-to-end leg skipped: pinning the host buffers failed ({refused or 'on another rank'})"
+    if not args.no_e2e and op == "step" and e2e_note is None:
         del gsets
-        host_p = torch.empty(nv, dtype=torch.bfloat16, pin_memory=True)
-        host_f = torch.empty(1, dtype=torch.int32, pin_memory=True)
         streamed = z.HostStreamedStep(plan, sb, se, host_g, master, m, v, params, chunk_elems=args.chunk_elems,
                                       params_host=host_p, overflow_flag=flag, stream=stream)
 

@@ -33,8 +33,8 @@ def check_scaler(dev_state: dict, sc: oracle.Scaler, hp: z.AdamW):
         assert np.float32(dev_state[k]).view(np.uint32) == np.float32(c[k]).view(np.uint32), k
 
 
-@pytest.mark.parametrize("M,n,align", [(1, 1000, 1), (4, 2048 * 3 + 37, 128), (8, 100_003, 1),
-                                       (9, 5000, 8), (64, 3001, 1)])
+@pytest.mark.parametrize("M,n,align", [(1, 1000, 1), (2, 40_001, 8), (4, 2048 * 3 + 37, 128), (5, 30_011, 1),
+                                       (7, 20_003, 128), (8, 100_003, 1), (9, 5000, 8), (64, 3001, 1)])
 def test_dynamic_attempts_match_oracle(cuda_device, M, n, align):
     dev = cuda_device
     plan = z.zero1_plan(n, M, align)

@@ -29,12 +29,12 @@ def _fused(dev, n, M, state_offset=0):
 
 
 def test_each_kernel_gets_its_own_occupancy(cuda_device):
-    """The small-range kernel (up to four blocks per SM) and the pipelined
+    """The small-range kernel (up to four blocks per SM) and the two-deep
     large-range kernel (one block per SM at M = 8) share a signature; a call
     of one must not fix the grid of the other."""
     dev = cuda_device
     sms = _sms()
-    big, small = 8 << 20, 1 << 16            # 8M elements: pipelined kernel; 64K: small-range kernel
+    big, small = 8 << 20, 1 << 16            # 8M elements: large-range shape; 64K: small-range kernel
     first_big = _fused(dev, big, 8)
     first_small = _fused(dev, small, 8)
     again_big = _fused(dev, big, 8)
@@ -45,6 +45,61 @@ def test_each_kernel_gets_its_own_occupancy(cuda_device):
     assert first_big["grid"] == sms * first_big["blocks_per_sm"]
     # the small range needs fewer blocks than a wave: one vector of 8 per thread
     assert first_small["grid"] == min(sms * first_small["blocks_per_sm"], -(-small // 8 // 256))
+
+
+def test_large_range_shapes_per_replica_count(cuda_device):
+    """On a large range the fused step runs the one-vector kernel at two
+    blocks per SM for M <= 5 and the two-deep kernel at one block per SM for
+    M = 6..8 (the measured faster shape for each M); the grid is one wave."""
+    dev = cuda_device
+    sms = _sms()
+    big = 8 << 20
+    for M in (1, 3, 5):
+        d = _fused(dev, big, M)
+        assert "k_fused_step_wide" in d["kernel"], (M, d)
+        assert d["blocks_per_sm"] == 2 and d["grid"] == 2 * sms, (M, d)
+    for M in (6, 8):
+        d = _fused(dev, big, M)
+        assert "k_fused_step_wide" not in d["kernel"] and "k_fused_step" in d["kernel"], (M, d)
+        assert d["blocks_per_sm"] == 1 and d["grid"] == sms, (M, d)
+    # the same one-vector kernel on a small range keeps its full occupancy
+    d = _fused(dev, 1 << 16, 3)
+    assert "k_fused_step_wide" in d["kernel"] and d["blocks_per_sm"] >= 3, d
+
+
+def test_allreduce_and_update_shapes(cuda_device):
+    """All-reduce grids follow their per-M table (one-vector kernels at two or
+    three blocks per SM, two-deep at M = 8); the dynamic step's update from
+    the sums runs one vector per thread at two blocks per SM."""
+    dev = cuda_device
+    sms = _sms()
+    n = 4 << 20
+    for M, per_sm, one_vector in ((1, 3, True), (3, 2, True), (4, 3, True), (6, 2, True), (8, None, False)):
+        plan = z.zero1_plan(n, M, 1)
+        grads = make_grads(M, n, 1e-3, 5, 1, dev)
+        outs = [torch.empty(n, dtype=torch.bfloat16, device=dev) for _ in range(M)]
+        z.dp_allreduce(plan, grads, outs, 1.0)
+        d = z.debug_last_launch()
+        assert "k_allreduce" in d["kernel"], d
+        # the depth is the kernel's last template argument (mangled: ...ELi<D>EEE)
+        assert ("Li1EEE" if one_vector else "Li2EEE") in d["kernel"], (M, d)
+        if per_sm is not None:
+            assert d["blocks_per_sm"] == per_sm and d["grid"] == per_sm * sms, (M, d)
+    M = 8
+    plan = z.zero1_plan(n, M, 1)
+    P = plan.padded_n
+    grads = make_grads(M, n, 1e-3, 6, 1, dev)
+    master, m, v = make_state(n, P, 9, dev)
+    params = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+    policy = z.LossScalePolicy()
+    hp = z.AdamW(global_batch=64)
+    scaler = z.new_scaler(dev)
+    z.zero1_scaler_init(scaler, policy, hp)
+    sums = torch.empty(P, dtype=torch.float32, device=dev)
+    z.zero1_step_dynamic(plan, 0, M, grads, master, m, v, params, hp, scaler, policy, sums)
+    torch.cuda.synchronize()
+    d = z.debug_last_launch()
+    assert "k_apply_sums" in d["kernel"] and d["blocks_per_sm"] == 2 and d["grid"] == 2 * sms, d
 
 
 def test_fp32_arrays_move_in_32_byte_accesses_when_aligned(cuda_device):

@@ -238,7 +238,8 @@ def test_skip_if_flag_writes_nothing(cuda_device):
     assert_bf16_bits(u16(params), want, "params")
 
 
-@pytest.mark.parametrize("M,n", [(1, 17), (4, 10_000), (8, 2048 * 3 + 5), (9, 4099), (64, 3000)])
+@pytest.mark.parametrize("M,n", [(1, 17), (1, 70_001), (2, 9_999), (3, 20_003), (4, 10_000), (5, 12_345), (6, 8_191),
+                                 (7, 30_001), (8, 2048 * 3 + 5), (9, 4099), (64, 3000)])
 def test_allreduce_matches_oracle_and_equals_rs_plus_ag(cuda_device, M, n):
     """Naive All-Reduce vs the oracle, and All-Reduce == Reduce-Scatter +
     All-Gather on the GPU, bitwise."""

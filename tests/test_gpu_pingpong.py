@@ -35,8 +35,8 @@ def two_copies(n, P, seed, dev, nonzero_moments=False):
     return [[a, b] for a, b in zip(cur, other)]
 
 
-@pytest.mark.parametrize("M,n,align", [(1, 1000, 1), (4, 2048 * 3 + 37, 128), (8, 100_003, 1),
-                                       (9, 5000, 8), (64, 3001, 1), (8, 7, 1)])
+@pytest.mark.parametrize("M,n,align", [(1, 1000, 1), (3, 40_001, 8), (4, 2048 * 3 + 37, 128), (5, 30_011, 1),
+                                       (6, 20_003, 128), (8, 100_003, 1), (9, 5000, 8), (64, 3001, 1), (8, 7, 1)])
 def test_pingpong_attempts_match_oracle(cuda_device, M, n, align):
     dev = cuda_device
     plan = z.zero1_plan(n, M, align)

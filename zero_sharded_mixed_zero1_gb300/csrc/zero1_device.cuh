@@ -220,21 +220,31 @@ __device__ __forceinline__ int64_t scalar_index(const Walk &w, int64_t q)
     return q < w.head ? q : q + w.nvec * kVec;
 }
 
-// Two-deep software pipeline over the vector body [0, nvec) with a grid
-// stride: the loads of vector i + nthr are issued before vector i is
-// computed, so each thread keeps two vectors of loads in flight.  (Measured
-// on the fused step: this beat higher occupancy with one vector in flight.)
-template <class Loads, class LoadF, class ComputeF>
+// The vector body [0, nvec) with a grid stride, D vectors of loads in
+// flight per thread.  D = 2: the loads of vector i + nthr are issued before
+// vector i is computed.  D = 1: one vector at a time, for grids with more
+// resident warps instead.  Which is faster depends on the kernel and on M
+// (measured; each launch site names its shape table).
+template <class Loads, int D = 2, class LoadF, class ComputeF>
 __device__ __forceinline__ void pipelined(int64_t nvec, int64_t tid, int64_t nthr, LoadF &&load, ComputeF &&compute)
 {
-    Loads cur, nxt;
-    int64_t i = tid;
-    if (i < nvec) load(cur, i);
-    for (; i < nvec; i += nthr) {
-        const bool more = i + nthr < nvec;
-        if (more) load(nxt, i + nthr);
-        compute(cur, i);
-        if (more) cur = nxt;
+    static_assert(D == 1 || D == 2, "one or two vectors in flight");
+    if constexpr (D == 1) {
+        for (int64_t i = tid; i < nvec; i += nthr) {
+            Loads cur;
+            load(cur, i);
+            compute(cur, i);
+        }
+    } else {
+        Loads cur, nxt;
+        int64_t i = tid;
+        if (i < nvec) load(cur, i);
+        for (; i < nvec; i += nthr) {
+            const bool more = i + nthr < nvec;
+            if (more) load(nxt, i + nthr);
+            compute(cur, i);
+            if (more) cur = nxt;
+        }
     }
 }
 
@@ -243,10 +253,32 @@ struct GradLoads {
     uint4 q[MT > 0 ? MT : 1];
 };
 
-// Resident blocks per SM requested from the compiler: one for the pipelined
-// M <= 8 paths (room for two vectors of loads per thread), three for the
-// grouped M > 8 paths.
-#define Z1_BOUNDS(MT) __launch_bounds__(kBlock, (MT) > 0 ? 1 : 3)
+// Resident blocks per SM requested from the compiler: one for the two-deep
+// M <= 8 paths (room for two vectors of loads per thread), four for the
+// one-vector paths (at most 64 registers; the grid may use fewer), three for
+// the grouped M > 8 paths.
+#define Z1_BOUNDS(MT, D) __launch_bounds__(kBlock, (MT) == 0 ? 3 : ((D) == 1 ? 4 : 1))
+
+// How a streaming kernel is launched over a large range: D vectors of loads
+// in flight per thread (1 or 2), and a grid of at most per_sm resident blocks
+// per SM (0: as many as fit).
+struct Shape {
+    int D, per_sm;
+};
+
+// Launch shape of the in-place fused update for M = MT on a large range
+// (k_fused_step_scaled, and the fused step: D = 2 is k_fused_step, D = 1
+// k_fused_step_wide with at most per_sm blocks per SM; MT = 0: M > 8,
+// replicas in groups of 8, where D is not used).  Measured on GB300, fused
+// step on 124M elements, fraction of the measured copy bandwidth (two-deep
+// against one vector at two blocks per SM): M = 1..5 0.925 0.925 0.931 0.958
+// 0.979 against 0.948 0.969 0.998 1.016 1.017; M = 6..8 0.997 1.010 1.022
+// against 0.969 0.960 0.984.  One vector at three or four blocks per SM was
+// slower for every M (0.85-0.97), so the fastest grid is not the fullest one.
+constexpr Shape fused_shape(int MT)
+{
+    return MT >= 1 && MT <= 5 ? Shape{1, 2} : Shape{2, 0};
+}
 
 // fp32 state loads that do not allocate in L1 (each line is read once) and
 // streaming stores (.cs: the written lines are not read again by this kernel).
@@ -445,8 +477,8 @@ __device__ __forceinline__ void rs_store(void *out, int64_t j, float s[kVec], fl
     }
 }
 
-template <int MT, bool BF16>
-__global__ void Z1_BOUNDS(MT)
+template <int MT, bool BF16, int D>
+__global__ void Z1_BOUNDS(MT, D)
 k_reduce_scatter(const __grid_constant__ GradPtrs g, int M, const Walk w, float scale, void *out,
                  uint32_t *flag)
 {
@@ -454,7 +486,7 @@ k_reduce_scatter(const __grid_constant__ GradPtrs g, int M, const Walk w, float 
     const int64_t nthr = (int64_t)gridDim.x * kBlock;
     bool bad = false;
     if constexpr (MT > 0) {
-        pipelined<GradLoads<MT>>(
+        pipelined<GradLoads<MT>, D>(
             w.nvec, tid, nthr,
             [&](GradLoads<MT> &x, int64_t i) {
                 const int64_t j = w.head + i * kVec;
@@ -493,6 +525,18 @@ k_reduce_scatter(const __grid_constant__ GradPtrs g, int M, const Walk w, float 
         else static_cast<float *>(out)[j] = s;
     }
     if (flag) warp_flag(flag, bad);
+}
+
+// Launch shape of k_reduce_scatter for M = MT (MT = 0: M > 8, replicas in
+// groups of 8, where D is not used).  Measured on GB300, fp32 output, 124M
+// elements: for M = 4..7 one vector at three blocks per SM reached 0.987
+// 1.001 1.011 1.010 of the measured copy bandwidth against 0.979 1.000 1.010
+// 0.990 two-deep; for the other M the two were within 0.3 %.  In the dynamic
+// step (followed by k_apply_sums) this table measured within 0.1 % of the
+// best of the uniform shapes for every M.
+constexpr Shape rs_shape(int MT)
+{
+    return MT >= 4 && MT <= 7 ? Shape{1, 3} : Shape{2, 0};
 }
 
 // ------------------------------------------------------------ host side ----
@@ -578,13 +622,15 @@ int blocks_per_sm(const void *kernel)
     return per_sm;
 }
 
-// One resident wave for a walk: SMs x this kernel's resident blocks, capped
-// by the work.  The launch is noted for zero1_debug_last_launch.
+// One resident wave for a walk: SMs x this kernel's resident blocks (at most
+// max_per_sm of them when that is positive), capped by the work.  The launch
+// is noted for zero1_debug_last_launch.
 template <class K>
-int grid_for(K kernel, const Walk &w)
+int grid_for(K kernel, const Walk &w, int max_per_sm = 0)
 {
     const void *k = reinterpret_cast<const void *>(kernel);
-    const int per_sm = blocks_per_sm(k);
+    int per_sm = blocks_per_sm(k);
+    if (max_per_sm > 0 && max_per_sm < per_sm) per_sm = max_per_sm;
     const int64_t wave = (int64_t)sm_count() * per_sm;
     const int64_t work = work_of(w);
     int64_t need = (work + kBlock - 1) / kBlock;

@@ -95,10 +95,12 @@ __global__ void k_scaler_update(zero1_scaler_t *sc, const ScalePolicy pol, int64
 // AdamW + all-gather from fp32 replica sums (written by the reduce-scatter
 // kernel just before on the same stream), with 1/(B*S) and the bias
 // corrections read from the scaler; nothing is written if the attempt's flag
-// is set.  The arithmetic is the fused step's, operation for operation.  Two
-// resident blocks per SM (at most 128 registers): measured 0.8-1.4 % faster
-// for the whole dynamic step than one block with 144 registers.
-__global__ void __launch_bounds__(kBlock, 2)
+// is set.  The arithmetic is the fused step's, operation for operation.
+// D = 2: two resident blocks per SM (at most 128 registers), measured
+// 0.8-1.4 % faster for the whole dynamic step than one block with 144
+// registers; D = 1: one vector per thread at most 64 registers.
+template <int D>
+__global__ void __launch_bounds__(kBlock, D == 1 ? 4 : 2)
 k_apply_sums(const float *__restrict__ sums, float *__restrict__ master, float *__restrict__ mom,
              float *__restrict__ var, uint16_t *__restrict__ params, const Walk w, Z1Consts c,
              const zero1_scaler_t *sc)
@@ -112,7 +114,7 @@ k_apply_sums(const float *__restrict__ sums, float *__restrict__ master, float *
     const int64_t nthr = (int64_t)gridDim.x * kBlock;
     bool bad = false;  // the flag was already taken by the reduce-scatter
     const bool w32 = w.w32 != 0;
-    pipelined<StateLoads>(
+    pipelined<StateLoads, D>(
         w.nvec, tid, nthr,
         [&](StateLoads &x, int64_t i) { load_state_vec(x, sums, master, mom, var, w.head + i * kVec, w32); },
         [&](const StateLoads &x, int64_t i) {
@@ -133,6 +135,13 @@ k_apply_sums(const float *__restrict__ sums, float *__restrict__ master, float *
     }
 }
 
+// Launch shape of k_apply_sums (which reads no gradients).  Measured on
+// GB300, the whole dynamic step on 124M elements, M = 1..8, fraction of the
+// measured copy bandwidth: 0.928-0.953 with both of its kernels two-deep,
+// 0.982-0.998 with this shape (and rs_shape's), 0.915-0.952 with both one
+// vector per thread at three or four blocks per SM.
+constexpr Shape kApplyShape{1, 2};
+
 // --------------------------------------------------- ping-pong state ------
 //
 // The dynamic step in one pass over the data: master/m/v exist twice, and
@@ -148,8 +157,8 @@ struct PingPong {
     float *master[2], *mom[2], *var[2];
 };
 
-// One attempt for M <= 8 (MT = M, two vectors of loads in flight per thread)
-// or M > 8 (MT = 0, replicas in groups of 8).  For M > 8, measured on the
+// One attempt for M <= 8 (MT = M, D vectors of loads in flight per thread,
+// pingpong_shape) or M > 8 (MT = 0, replicas in groups of 8).  For M > 8, measured on the
 // 64-replica shard: state read with the default policy at two blocks per SM
 // (107 registers) beat three blocks per SM, whose 85-register cap spilled
 // (2.64 against 2.75-2.85 ms).
@@ -157,7 +166,7 @@ struct PingPong {
 // kernel parameter, which the compiler can reload instead of holding it in a
 // register (169 registers at M = 8 against 179 with the copy picked at run
 // time; the same speed on the same box).
-template <int MT, int CUR>
+template <int MT, int CUR, int D>
 __device__ __forceinline__ void pingpong_body(const GradPtrs &g, int M, const PingPong &s,
                                               uint16_t *__restrict__ params, const Walk &w, const Z1Consts &c,
                                               zero1_scaler_t *sc)
@@ -173,7 +182,7 @@ __device__ __forceinline__ void pingpong_body(const GradPtrs &g, int M, const Pi
     bool bad = false;
     const bool w32 = w.w32 != 0;
     if constexpr (MT > 0) {
-        pipelined<VecLoads<MT>>(
+        pipelined<VecLoads<MT>, D>(
             w.nvec, tid, nthr,
             [&](VecLoads<MT> &x, int64_t i) { x.load(g, sw, sm, sv, w.head + i * kVec, w32); },
             [&](const VecLoads<MT> &x, int64_t i) {
@@ -211,8 +220,8 @@ __device__ __forceinline__ void pingpong_body(const GradPtrs &g, int M, const Pi
     warp_flag(&sc->overflow, bad);
 }
 
-template <int MT>
-__global__ void __launch_bounds__(kBlock, MT == 0 ? 2 : (MT <= 2 ? 2 : 1))
+template <int MT, int D>
+__global__ void __launch_bounds__(kBlock, MT == 0 ? 2 : (D == 1 ? 4 : (MT <= 2 ? 2 : 1)))
 k_fused_step_pingpong(const __grid_constant__ GradPtrs g, int M, const __grid_constant__ PingPong s,
                       uint16_t *__restrict__ params, const Walk w, Z1Consts c, zero1_scaler_t *sc)
 {
@@ -222,9 +231,21 @@ k_fused_step_pingpong(const __grid_constant__ GradPtrs g, int M, const __grid_co
     c.bc1 = sc->bc1;
     c.bc2 = sc->bc2;
     if (cur)
-        pingpong_body<MT, 1>(g, M, s, params, w, c, sc);
+        pingpong_body<MT, 1, D>(g, M, s, params, w, c, sc);
     else
-        pingpong_body<MT, 0>(g, M, s, params, w, c, sc);
+        pingpong_body<MT, 0, D>(g, M, s, params, w, c, sc);
+}
+
+// Launch shape of k_fused_step_pingpong for M = MT (MT = 0: M > 8, replicas
+// in groups of 8, where D is not used).  Measured on GB300, the ping-pong
+// step on 124M elements, fraction of the measured copy bandwidth: M = 1..4
+// two-deep 0.909 0.915 0.932 0.951, one vector at two blocks per SM 0.949
+// 0.975 0.995 1.006; M = 5 two-deep 0.967, one vector at three blocks per SM
+// 0.979 (at two: 0.907); M = 6..8 two-deep 0.981 0.992 1.002, ahead of every
+// one-vector grid.
+constexpr Shape pingpong_shape(int MT)
+{
+    return MT >= 1 && MT <= 4 ? Shape{1, 2} : (MT == 5 ? Shape{1, 3} : Shape{2, 0});
 }
 
 // The fused step in place, with S and t taken from the scaler, for a range
@@ -234,8 +255,8 @@ k_fused_step_pingpong(const __grid_constant__ GradPtrs g, int M, const __grid_co
 // staged step with dynamic loss scaling uses it on its HBM slots: there the
 // state lives in host memory, where a second copy would cost host memory and
 // twice the link traffic.
-template <int MT>
-__global__ void __launch_bounds__(kBlock, MT == 0 ? 2 : (MT <= 2 ? 2 : 1))
+template <int MT, int D>
+__global__ void __launch_bounds__(kBlock, MT == 0 ? 2 : (D == 1 ? 4 : (MT <= 2 ? 2 : 1)))
 k_fused_step_scaled(const __grid_constant__ GradPtrs g, int M, float *__restrict__ master,
                     float *__restrict__ mom, float *__restrict__ var, uint16_t *__restrict__ params, const Walk w,
                     Z1Consts c, const zero1_scaler_t *sc)
@@ -249,7 +270,7 @@ k_fused_step_scaled(const __grid_constant__ GradPtrs g, int M, float *__restrict
     bool bad = false;  // the flag is final already; nothing is reported
     const bool w32 = w.w32 != 0;
     if constexpr (MT > 0) {
-        pipelined<VecLoads<MT>>(
+        pipelined<VecLoads<MT>, D>(
             w.nvec, tid, nthr,
             [&](VecLoads<MT> &x, int64_t i) { x.load(g, master, mom, var, w.head + i * kVec, w32); },
             [&](const VecLoads<MT> &x, int64_t i) {
@@ -386,15 +407,16 @@ extern "C" int zero1_step_dynamic(const zero1_plan_t *plan, int32_t shard_begin,
     uint32_t *flag = &scaler->overflow;
     dispatch_m(M, [&](auto mt) {
         constexpr int MT = decltype(mt)::value;
-        const int grid = grid_for(k_reduce_scatter<MT, false>, wr);
-        k_reduce_scatter<MT, false><<<grid, kBlock, 0, st>>>(g, M, wr, 1.0f, sums, flag);
+        constexpr Shape sh = rs_shape(MT);
+        const int grid = grid_for(k_reduce_scatter<MT, false, sh.D>, wr, sh.per_sm);
+        k_reduce_scatter<MT, false, sh.D><<<grid, kBlock, 0, st>>>(g, M, wr, 1.0f, sums, flag);
     });
     // 2. the update from the sums (skipped on overflow)
     const ArrayRef ua[5] = {{sums, 4}, {master, 4}, {m, 4}, {v, 4}, {params, 2}};
     const Walk wu = make_walk(r.L, r.nv, ua, 5);
-    const int grid = grid_for(k_apply_sums, wu);
+    const int grid = grid_for(k_apply_sums<kApplyShape.D>, wu, kApplyShape.per_sm);
     if ((rc = launch_status("dynamic step: reduce-scatter launch")) != ZERO1_OK) return rc;
-    const cudaError_t e = launch_pdl(k_apply_sums, grid, kBlock, st, (const float *)sums, master, m, v,
+    const cudaError_t e = launch_pdl(k_apply_sums<kApplyShape.D>, grid, kBlock, st, (const float *)sums, master, m, v,
                                      static_cast<uint16_t *>(params), wu, c, (const zero1_scaler_t *)scaler);
     if (e != cudaSuccess) return pdl_fail(e, "dynamic step: update launch");
     // 3. the scaler advances (only once the update is enqueued)
@@ -458,8 +480,9 @@ int launch_pingpong_range(const zero1_plan_t *plan, int64_t L, int64_t nv, const
     cudaError_t e = cudaSuccess;
     dispatch_m(M, [&](auto mt) {
         constexpr int MT = decltype(mt)::value;
-        const int grid = grid_for(k_fused_step_pingpong<MT>, w);
-        e = launch_pdl(k_fused_step_pingpong<MT>, grid, kBlock, st, g, M, s, pp, w, c, scaler);
+        constexpr Shape sh = pingpong_shape(MT);
+        const int grid = grid_for(k_fused_step_pingpong<MT, sh.D>, w, sh.per_sm);
+        e = launch_pdl(k_fused_step_pingpong<MT, sh.D>, grid, kBlock, st, g, M, s, pp, w, c, scaler);
     });
     if (e != cudaSuccess) return pdl_fail(e, what);
     return launch_status(what);
@@ -585,8 +608,9 @@ int z1_scaled_range(const zero1_plan_t *plan, int64_t elem_begin, int64_t elem_e
     uint16_t *pp = static_cast<uint16_t *>(params);
     dispatch_m(M, [&](auto mt) {
         constexpr int MT = decltype(mt)::value;
-        const int grid = grid_for(k_fused_step_scaled<MT>, w);
-        k_fused_step_scaled<MT><<<grid, kBlock, 0, st>>>(g, M, master, m, v, pp, w, c, scaler);
+        constexpr Shape sh = fused_shape(MT);
+        const int grid = grid_for(k_fused_step_scaled<MT, sh.D>, w, sh.per_sm);
+        k_fused_step_scaled<MT, sh.D><<<grid, kBlock, 0, st>>>(g, M, master, m, v, pp, w, c, scaler);
     });
     return launch_status("scaled range launch");
 }

@@ -8,10 +8,12 @@
 //                                ->  bf16 parameter, 2 B written once
 //
 // 2M + 26 bytes per parameter, bound by HBM bandwidth.  Four kernels, chosen
-// per call: two vectors of loads in flight per thread for M <= 8 (the
-// measured fastest on large ranges), one vector per thread at four blocks per
-// SM on small ranges, replicas in groups of 8 for M > 8, and four vectors of
-// state loads in flight when master/m/v live in host memory.  Arithmetic uses
+// per call: for M <= 8 on large ranges, two vectors of loads in flight per
+// thread at one block per SM (M = 6..8) or one vector per thread at two
+// blocks per SM (M <= 5), whichever measured faster (fused_shape); one vector
+// per thread at up to four blocks per SM on small ranges; replicas in groups
+// of 8 for M > 8; and four vectors of state loads in flight when master/m/v
+// live in host memory.  Arithmetic uses
 // the explicit round-to-nearest intrinsics (__fadd_rn, __fmul_rn, __fdiv_rn,
 // __fsqrt_rn): no contraction, IEEE division and square root, so the results
 // are reproducible bit for bit.
@@ -38,11 +40,13 @@ __device__ __forceinline__ void fused_vec(int64_t j, const VecLoads<MT> &x, floa
 // compile time).
 //
 // Shape chosen by measurement on GB300 (CUDA events through this entry point
-// on the 124M-parameter M = 8 workload): each thread issues all loads of its
-// next vector before computing the current one, so two vectors - 2 x
-// (16M + 96) bytes - are in flight per thread; the register budget this needs
-// (launch bounds of one block per SM) beat higher occupancy with one vector
-// in flight.  fp32 state is read with L1::no_allocate and every store is .cs.
+// on the 124M-parameter workload): each thread issues all loads of its next
+// vector before computing the current one, so two vectors - 2 x (16M + 96)
+// bytes - are in flight per thread; the register budget this needs (launch
+// bounds of one block per SM) beat higher occupancy with one vector in flight
+// for M = 6..8.  For M <= 5 k_fused_step_wide at two blocks per SM is faster
+// (fused_shape).  fp32 state is read with L1::no_allocate and every store is
+// .cs.
 template <int MT>
 __global__ void __launch_bounds__(kBlock, MT <= 2 ? 2 : 1)
 k_fused_step(const __grid_constant__ GradPtrs g, int M, float *__restrict__ master,
@@ -73,7 +77,8 @@ k_fused_step(const __grid_constant__ GradPtrs g, int M, float *__restrict__ mast
 // one vector per thread and iteration at up to four blocks per SM.  Few
 // vectors per thread means the two-deep pipeline has nothing to overlap, and
 // the chain of dependent iterations per thread, not bandwidth, sets the time;
-// four times the threads shortens that chain.
+// four times the threads shortens that chain.  The same kernel at two blocks
+// per SM is the large-range shape for M <= 5 (fused_shape).
 constexpr int64_t kWideMaxVec = 1 << 18;  // 2M elements
 
 template <int MT>
@@ -242,12 +247,19 @@ int launch_fused_range(const zero1_plan_t *plan, int64_t L, int64_t nv, const vo
         dispatch_m(M, [&](auto mt) {
             constexpr int MT = decltype(mt)::value;
             if constexpr (MT > 0) {
-                if (w.nvec <= kWideMaxVec) {
+                // small ranges: the one-vector kernel at full occupancy
+                constexpr Shape sh = fused_shape(MT);
+                const bool small = w.nvec <= kWideMaxVec;
+                if constexpr (sh.D == 1) {
+                    const int grid = grid_for(k_fused_step_wide<MT>, w, small ? 0 : sh.per_sm);
+                    e = launch_pdl(k_fused_step_wide<MT>, grid, kBlock, st, g, M, master, m, v, pp, w, c,
+                                   overflow_flag, skip);
+                } else if (small) {
                     const int grid = grid_for(k_fused_step_wide<MT>, w);
                     e = launch_pdl(k_fused_step_wide<MT>, grid, kBlock, st, g, M, master, m, v, pp, w, c,
                                    overflow_flag, skip);
                 } else {
-                    const int grid = grid_for(k_fused_step<MT>, w);
+                    const int grid = grid_for(k_fused_step<MT>, w, sh.per_sm);
                     e = launch_pdl(k_fused_step<MT>, grid, kBlock, st, g, M, master, m, v, pp, w, c, overflow_flag,
                                    skip);
                 }

@@ -138,7 +138,7 @@ __device__ __forceinline__ void ar_store(const OutPtrs &o, int M, int64_t j, flo
 // (non-coherent) path, which is allowed only while no buffer this kernel
 // writes overlaps them; an in-place call (an output aliasing an input) runs
 // the coherent instance, which reads them with ordinary global loads.
-template <int MT, bool BF16, bool NC>
+template <int MT, bool BF16, bool NC, int D>
 __device__ __forceinline__ void allreduce_body(const GradPtrs &g, const OutPtrs &o, int M, const Walk &w,
                                                float scale)
 {
@@ -148,7 +148,7 @@ __device__ __forceinline__ void allreduce_body(const GradPtrs &g, const OutPtrs 
     if constexpr (MT > 0) {
         // in place, the next vector's loads touch other elements than the
         // current vector's stores, so prefetching them stays correct
-        pipelined<GradLoads<MT>>(
+        pipelined<GradLoads<MT>, D>(
             w.nvec, tid, nthr,
             [&](GradLoads<MT> &x, int64_t i) {
                 const int64_t j = w.head + i * kVec;
@@ -182,21 +182,47 @@ __device__ __forceinline__ void allreduce_body(const GradPtrs &g, const OutPtrs 
 }
 
 // Separate outputs: gradients through the read-only path.
-template <int MT, bool BF16>
-__global__ void Z1_BOUNDS(MT)
+template <int MT, bool BF16, int D>
+__global__ void Z1_BOUNDS(MT, D)
 k_allreduce(const __grid_constant__ GradPtrs g, const __grid_constant__ OutPtrs o, int M,
             const Walk w, float scale)
 {
-    allreduce_body<MT, BF16, true>(g, o, M, w, scale);
+    allreduce_body<MT, BF16, true, D>(g, o, M, w, scale);
 }
 
 // In place (bf16 outputs overlapping the inputs): coherent loads.
-template <int MT>
-__global__ void Z1_BOUNDS(MT)
+template <int MT, int D>
+__global__ void Z1_BOUNDS(MT, D)
 k_allreduce_inplace(const __grid_constant__ GradPtrs g, const __grid_constant__ OutPtrs o, int M,
                     const Walk w, float scale)
 {
-    allreduce_body<MT, true, false>(g, o, M, w, scale);
+    allreduce_body<MT, true, false, D>(g, o, M, w, scale);
+}
+
+// Launch shapes of the all-reduce kernels for M = MT (MT = 0: M > 8, where D
+// is not used), with separate outputs and in place.  Measured on GB300, bf16
+// outputs, 124M elements, M = 1..8, fraction of the measured copy bandwidth:
+// separate outputs two-deep 0.761 0.951 0.948 0.940 0.933 0.944 0.941 0.952,
+// this table 0.926 0.952 0.970 0.964 0.969 0.975 0.961 0.952; in place
+// two-deep 0.788 0.963 0.954 0.942 0.939 0.944 0.935 0.956, this table 0.789
+// 0.963 0.968 0.969 0.977 0.981 0.965 0.956.  Two or three blocks per SM: the
+// better of the two differs by M, reproducibly across boxes.
+constexpr Shape allreduce_shape(int MT)
+{
+    switch (MT) {
+    case 1: case 4: return Shape{1, 3};
+    case 3: case 5: case 6: case 7: return Shape{1, 2};
+    default: return Shape{2, 0};
+    }
+}
+
+constexpr Shape allreduce_inplace_shape(int MT)
+{
+    switch (MT) {
+    case 3: case 4: return Shape{1, 3};
+    case 5: case 6: case 7: return Shape{1, 2};
+    default: return Shape{2, 0};
+    }
 }
 
 }  // namespace
@@ -262,15 +288,16 @@ extern "C" int dp_allreduce(const zero1_plan_t *plan, const void *const *grads_i
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     dispatch_m(M, [&](auto mt) {
         constexpr int MT = decltype(mt)::value;
+        constexpr Shape sh = allreduce_shape(MT), ish = allreduce_inplace_shape(MT);
         if (osz == 2 && overlap) {
-            const int grid = grid_for(k_allreduce_inplace<MT>, w);
-            k_allreduce_inplace<MT><<<grid, kBlock, 0, st>>>(g, o, M, w, scale);
+            const int grid = grid_for(k_allreduce_inplace<MT, ish.D>, w, ish.per_sm);
+            k_allreduce_inplace<MT, ish.D><<<grid, kBlock, 0, st>>>(g, o, M, w, scale);
         } else if (osz == 2) {
-            const int grid = grid_for(k_allreduce<MT, true>, w);
-            k_allreduce<MT, true><<<grid, kBlock, 0, st>>>(g, o, M, w, scale);
+            const int grid = grid_for(k_allreduce<MT, true, sh.D>, w, sh.per_sm);
+            k_allreduce<MT, true, sh.D><<<grid, kBlock, 0, st>>>(g, o, M, w, scale);
         } else {
-            const int grid = grid_for(k_allreduce<MT, false>, w);
-            k_allreduce<MT, false><<<grid, kBlock, 0, st>>>(g, o, M, w, scale);
+            const int grid = grid_for(k_allreduce<MT, false, sh.D>, w, sh.per_sm);
+            k_allreduce<MT, false, sh.D><<<grid, kBlock, 0, st>>>(g, o, M, w, scale);
         }
     });
     return launch_status("all-reduce launch");
@@ -302,12 +329,13 @@ extern "C" int zero1_reduce_scatter(const zero1_plan_t *plan, int32_t shard_begi
     const int M = plan->M;
     dispatch_m(M, [&](auto mt) {
         constexpr int MT = decltype(mt)::value;
+        constexpr Shape sh = rs_shape(MT);
         if (osz == 2) {
-            const int grid = grid_for(k_reduce_scatter<MT, true>, w);
-            k_reduce_scatter<MT, true><<<grid, kBlock, 0, st>>>(g, M, w, scale, out, flag);
+            const int grid = grid_for(k_reduce_scatter<MT, true, sh.D>, w, sh.per_sm);
+            k_reduce_scatter<MT, true, sh.D><<<grid, kBlock, 0, st>>>(g, M, w, scale, out, flag);
         } else {
-            const int grid = grid_for(k_reduce_scatter<MT, false>, w);
-            k_reduce_scatter<MT, false><<<grid, kBlock, 0, st>>>(g, M, w, scale, out, flag);
+            const int grid = grid_for(k_reduce_scatter<MT, false, sh.D>, w, sh.per_sm);
+            k_reduce_scatter<MT, false, sh.D><<<grid, kBlock, 0, st>>>(g, M, w, scale, out, flag);
         }
     });
     return launch_status("reduce-scatter launch");

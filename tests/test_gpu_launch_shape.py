@@ -100,6 +100,35 @@ def test_allreduce_and_update_shapes(cuda_device):
     torch.cuda.synchronize()
     d = z.debug_last_launch()
     assert "k_apply_sums" in d["kernel"] and d["blocks_per_sm"] == 2 and d["grid"] == 2 * sms, d
+    # the unfused update: one vector per thread at two blocks per SM
+    z.zero1_adamw_update(plan, 0, M, sums, master, m, v, hp)
+    d = z.debug_last_launch()
+    assert "k_adamw" in d["kernel"] and "Li1E" in d["kernel"] and d["grid"] == 2 * sms, d
+    # the overflow check at M = 8: three blocks per SM
+    flag = torch.zeros(1, dtype=torch.int32, device=dev)
+    z.zero1_overflow_check(plan, 0, M, grads, flag)
+    d = z.debug_last_launch()
+    assert "k_overflow" in d["kernel"] and d["blocks_per_sm"] == 3 and d["grid"] == 3 * sms, d
+    # the ping-pong step ends with the parameter restore at four blocks per SM
+    pairs = [[x, x.clone()] for x in (master, m, v)]
+    z.zero1_step_dynamic_pingpong(plan, 0, M, grads, *pairs, params, hp, scaler, policy)
+    torch.cuda.synchronize()
+    d = z.debug_last_launch()
+    assert "k_restore_params" in d["kernel"] and d["blocks_per_sm"] == 4 and d["grid"] == 4 * sms, d
+
+
+def test_grouped_allreduce_runs_two_blocks_per_sm(cuda_device):
+    """M > 8: the all-reduce's grouped loop runs at two blocks per SM (below
+    its occupancy of three, measured faster)."""
+    dev = cuda_device
+    sms = _sms()
+    n, M = 1 << 20, 16
+    plan = z.zero1_plan(n, M, 1)
+    grads = make_grads(M, n, 1e-3, 8, 1, dev)
+    outs = [torch.empty(n, dtype=torch.bfloat16, device=dev) for _ in range(M)]
+    z.dp_allreduce(plan, grads, outs, 1.0)
+    d = z.debug_last_launch()
+    assert "k_allreduce" in d["kernel"] and d["blocks_per_sm"] == 2 and d["grid"] == 2 * sms, d
 
 
 def test_fp32_arrays_move_in_32_byte_accesses_when_aligned(cuda_device):

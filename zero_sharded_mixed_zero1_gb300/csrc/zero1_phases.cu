@@ -37,9 +37,21 @@ k_overflow(const __grid_constant__ GradPtrs g, int M, const Walk w, uint32_t *fl
     warp_flag(flag, bad);
 }
 
-// Two resident blocks per SM (at most 128 registers): the unfused chain
-// measured 1.5 % faster than with one block of 138 registers.
-__global__ void __launch_bounds__(kBlock, 2)
+// Blocks per SM of k_overflow's grid for M = MT (0: as many as fit, five for
+// M <= 8).  Measured on GB300, 124M elements, fraction of the measured copy
+// bandwidth at the full occupancy against this cap: M = 6 1.066 against 1.080
+// (four), M = 7 1.066 against 1.079 (three), M = 8 1.066 against 1.087
+// (three); for M <= 5 and M > 8 the full occupancy was fastest.
+constexpr int overflow_per_sm(int MT)
+{
+    return MT == 6 ? 4 : (MT == 7 || MT == 8 ? 3 : 0);
+}
+
+// D = 2: two resident blocks per SM (at most 128 registers), measured 1.5 %
+// faster for the unfused chain than one block of 138 registers; D = 1: one
+// vector per thread at most 64 registers.
+template <int D>
+__global__ void __launch_bounds__(kBlock, D == 1 ? 4 : 2)
 k_adamw(const float *__restrict__ gin, float *__restrict__ master, float *__restrict__ mom,
         float *__restrict__ var, const Walk w, const Z1Consts c)
 {
@@ -47,7 +59,7 @@ k_adamw(const float *__restrict__ gin, float *__restrict__ master, float *__rest
     const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
     const int64_t nthr = (int64_t)gridDim.x * kBlock;
     const bool w32 = w.w32 != 0;
-    pipelined<StateLoads>(
+    pipelined<StateLoads, D>(
         w.nvec, tid, nthr,
         [&](StateLoads &x, int64_t i) { load_state_vec(x, gin, master, mom, var, w.head + i * kVec, w32); },
         [&](const StateLoads &x, int64_t i) {
@@ -75,14 +87,15 @@ k_adamw(const float *__restrict__ gin, float *__restrict__ master, float *__rest
 }
 
 // All-gather of the updated shard: params[j] = bf16(master[j]), real only.
-__global__ void __launch_bounds__(kBlock, 1)
+template <int D>
+__global__ void __launch_bounds__(kBlock, D == 1 ? 4 : 1)
 k_all_gather(const float *__restrict__ master, uint16_t *__restrict__ params, const Walk w)
 {
     wait_prior_grid();
     const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
     const int64_t nthr = (int64_t)gridDim.x * kBlock;
     const bool w32 = w.w32 != 0;
-    pipelined<F8>(
+    pipelined<F8, D>(
         w.nvec, tid, nthr, [&](F8 &x, int64_t i) { x = ld_cs8(master + w.head + i * kVec, w32); },
         [&](const F8 &x, int64_t i) {
             __stcs(reinterpret_cast<uint4 *>(params + w.head + i * kVec),
@@ -95,6 +108,14 @@ k_all_gather(const float *__restrict__ master, uint16_t *__restrict__ params, co
         if (j < w.nv) params[j] = to_bf16(master[j]);
     }
 }
+
+// Launch shapes of k_adamw and k_all_gather.  Measured on GB300, 124M
+// elements, fraction of the measured copy bandwidth: k_adamw two-deep at two
+// blocks per SM 0.952, one vector at two blocks per SM 0.982 (three: 0.949,
+// four: 0.921); k_all_gather two-deep at its full occupancy 0.998, one vector
+// at two, three, four blocks per SM 0.748, 0.895, 0.982.
+constexpr Shape kAdamwShape{1, 2};
+constexpr Shape kAllGatherShape{2, 0};
 
 // All-gather of bf16 shards into M outputs (real elements only).
 __global__ void __launch_bounds__(kBlock)
@@ -206,12 +227,15 @@ k_allreduce_inplace(const __grid_constant__ GradPtrs g, const __grid_constant__ 
 // this table 0.926 0.952 0.970 0.964 0.969 0.975 0.961 0.952; in place
 // two-deep 0.788 0.963 0.954 0.942 0.939 0.944 0.935 0.956, this table 0.789
 // 0.963 0.968 0.969 0.977 0.981 0.965 0.956.  Two or three blocks per SM: the
-// better of the two differs by M, reproducibly across boxes.
+// better of the two differs by M, reproducibly across boxes.  M > 8 (16M
+// elements): two blocks per SM 0.942 at M = 16 and 0.948 at M = 64, against
+// 0.922 and 0.929 at the kernel's occupancy of three.
 constexpr Shape allreduce_shape(int MT)
 {
     switch (MT) {
     case 1: case 4: return Shape{1, 3};
     case 3: case 5: case 6: case 7: return Shape{1, 2};
+    case 0: return Shape{2, 2};
     default: return Shape{2, 0};
     }
 }
@@ -221,6 +245,7 @@ constexpr Shape allreduce_inplace_shape(int MT)
     switch (MT) {
     case 3: case 4: return Shape{1, 3};
     case 5: case 6: case 7: return Shape{1, 2};
+    case 0: return Shape{2, 2};
     default: return Shape{2, 0};
     }
 }
@@ -246,7 +271,7 @@ extern "C" int zero1_overflow_check(const zero1_plan_t *plan, int32_t shard_begi
     const int M = plan->M;
     dispatch_m(M, [&](auto mt) {
         constexpr int MT = decltype(mt)::value;
-        const int grid = grid_for(k_overflow<MT>, w);
+        const int grid = grid_for(k_overflow<MT>, w, overflow_per_sm(MT));
         k_overflow<MT><<<grid, kBlock, 0, st>>>(g, M, w, flag);
     });
     return launch_status("overflow check launch");
@@ -361,8 +386,8 @@ extern "C" int zero1_adamw_update(const zero1_plan_t *plan, int32_t shard_begin,
     // every element of the range is updated: walk it as if all were real
     const Walk w = make_walk(r.L, r.L, arr, 4);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const int grid = grid_for(k_adamw, w);
-    const cudaError_t e = launch_pdl(k_adamw, grid, kBlock, st, gin, master, m, v, w, c);
+    const int grid = grid_for(k_adamw<kAdamwShape.D>, w, kAdamwShape.per_sm);
+    const cudaError_t e = launch_pdl(k_adamw<kAdamwShape.D>, grid, kBlock, st, gin, master, m, v, w, c);
     if (e != cudaSuccess) return pdl_fail(e, "adamw launch");
     return launch_status("adamw launch");
 }
@@ -382,8 +407,9 @@ extern "C" int zero1_all_gather(const zero1_plan_t *plan, int32_t shard_begin, i
     const ArrayRef arr[2] = {{master, 4}, {params, 2}};
     const Walk w = make_walk(r.nv, r.nv, arr, 2);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const int grid = grid_for(k_all_gather, w);
-    const cudaError_t e = launch_pdl(k_all_gather, grid, kBlock, st, master, static_cast<uint16_t *>(params), w);
+    const int grid = grid_for(k_all_gather<kAllGatherShape.D>, w, kAllGatherShape.per_sm);
+    const cudaError_t e = launch_pdl(k_all_gather<kAllGatherShape.D>, grid, kBlock, st, master,
+                                     static_cast<uint16_t *>(params), w);
     if (e != cudaSuccess) return pdl_fail(e, "all-gather launch");
     return launch_status("all-gather launch");
 }

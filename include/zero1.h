@@ -271,8 +271,9 @@ int zero1_staged_chunks(const zero1_staged_t *handle, int64_t *cuts, int32_t cap
  * kernel start, kernel end, outbound copies start, outbound copies end (the
  * last two -1 when nothing is copied back).  A start is when that stream
  * reached the chunk, after its waits for the previous stage.  Waits for the
- * last step to finish (synchronous).  EINVAL without the bit or before any
- * step; ERANGE if cap < 6 x chunks. */
+ * last step to finish (synchronous).  EINVAL without the bit, before any
+ * step, or after a step call that returned an error; ERANGE if cap < 6 x
+ * chunks. */
 int zero1_staged_timeline(zero1_staged_t *handle, float *ms, int32_t cap, int32_t *count);
 
 /* The fused step with its vector body staged through shared memory by the

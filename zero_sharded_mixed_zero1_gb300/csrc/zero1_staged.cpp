@@ -312,6 +312,8 @@ int staged_run(zero1_staged_t *h, const void *const *grads, float *master, float
     do {                                                 \
         if ((e = (call)) != cudaSuccess) return cuda_fail(e, #call); \
     } while (0)
+    // a call that fails part way leaves no timeline to read
+    h->timed_step = false;
     Z1_CUDA(cudaEventRecord(h->entry, st));
     if (h->timeline) Z1_CUDA(cudaEventRecord(h->t0, st));
     cudaEvent_t *tk = nullptr;  // this chunk's timing events, or NULL

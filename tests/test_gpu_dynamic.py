@@ -71,6 +71,53 @@ def test_dynamic_attempts_match_oracle(cuda_device, M, n, align):
     assert sc.skipped == len(overflow_at)
 
 
+@pytest.mark.parametrize("design", ["two_pass", "pingpong"])
+def test_scaler_growth_refills_hysteresis_like_the_oracle(cuda_device, design):
+    """A sequence that grows the scale with hysteresis left below its full
+    count, then overflows right after the growth: the device scaler follows
+    the oracle's rule (growth refills the hysteresis) attempt by attempt,
+    and the state stays the oracle's."""
+    dev = cuda_device
+    M, n = 2, 4099
+    plan = z.zero1_plan(n, M, 8)
+    P = plan.padded_n
+    policy = z.LossScalePolicy(initial_scale=64.0, factor=2.0, window=2, hysteresis=2, min_scale=1.0)
+    hp = z.AdamW(global_batch=64, step=1)
+    scaler = z.new_scaler(dev)
+    z.zero1_scaler_init(scaler, policy, hp)
+    sc = oracle.Scaler.start(oracle_policy(policy), 1)
+    master, m, v = make_state(n, P, 77, dev)
+    o = [f32(master), f32(m), f32(v)]
+    # parameters consistent with the master weights, as after any earlier
+    # step (the ping-pong design restores them from the master on a skip)
+    o_params = oracle.f32_to_bf16(o[0][:n])
+    params = torch.from_numpy(o_params.view(np.int16).copy()).view(torch.bfloat16).to(dev)
+    sums = torch.empty(P, dtype=torch.float32, device=dev)
+    pairs = [[x, torch.zeros_like(x)] for x in (master, m, v)]
+    ohp = oracle.AdamW(lr=hp.lr, beta1=hp.beta1, beta2=hp.beta2, eps=hp.eps, weight_decay=hp.weight_decay,
+                       global_batch=hp.global_batch)
+    pattern = [1, 0, 0, 1, 1, 0, 0, 1, 0, 0]
+    for attempt, over in enumerate(pattern):
+        grads = [synth.normal_bf16(n, 1e-3 * sc.scale, synth.seed_of(78, attempt, r), dev) for r in range(M)]
+        if over:
+            grads[attempt % M][(13 * attempt) % n] = float("-inf")
+        g_np = [u16(g) for g in grads]
+        if design == "two_pass":
+            z.zero1_step_dynamic(plan, 0, M, grads, master, m, v, params, hp, scaler, policy, sums)
+        else:
+            z.zero1_step_dynamic_pingpong(plan, 0, M, grads, *pairs, params, hp, scaler, policy)
+        torch.cuda.synchronize()
+        assert oracle.zero1_dynamic_attempt(g_np, n, *o, o_params, ohp, sc, oracle_policy(policy)) == over
+        check_scaler(z.scaler_state(scaler), sc, hp)
+        state = [master, m, v] if design == "two_pass" else z.current_state(scaler, *pairs)
+        for x, want, what in zip(state, o, ("master", "m", "v")):
+            assert_f32_bits(f32(x), want, f"{design} {what} attempt {attempt}")
+        assert_bf16_bits(u16(params), o_params, f"{design} params attempt {attempt}")
+    # growth after attempts 1-2 refilled the hysteresis, so attempt 3 did not
+    # back off and attempt 4 did (64 -> 128 -> 64); then 128 and 256
+    assert sc.scale == 256.0 and sc.skipped == 4
+
+
 def test_clean_dynamic_step_equals_fused_step(cuda_device):
     """Without overflow the three-kernel dynamic step is bit for bit the
     fused step with the scaler's S and t."""

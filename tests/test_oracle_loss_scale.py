@@ -48,6 +48,18 @@ def test_hysteresis_two_tolerates_one_overflow():
     assert sc.scale == 1024.0
 
 
+def test_growth_refills_the_hysteresis():
+    """After a full window the scale grows and the hysteresis is back to its
+    full count: one overflow right after growth only uses one unit of it."""
+    pol = LossScalePolicy(initial_scale=16.0, window=2, hysteresis=2)
+    sc = run([1, 0, 0], pol)
+    assert sc.scale == 32.0 and sc.hyst_left == 2 and sc.good == 0
+    sc = run([1, 0, 0, 1], pol)
+    assert sc.scale == 32.0 and sc.hyst_left == 1
+    sc = run([1, 0, 0, 1, 1], pol)
+    assert sc.scale == 16.0 and sc.hyst_left == 2
+
+
 def test_overflow_restarts_the_window():
     pol = LossScalePolicy(initial_scale=16.0, window=4, hysteresis=2)
     assert run([0, 0, 0, 1, 0, 0, 0], pol).scale == 16.0

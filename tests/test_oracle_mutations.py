@@ -36,6 +36,21 @@ MUTANTS = {
     "checksum_index_from_zero": ("        s2 += (uint64_t)(i + 1) * (uint64_t)u[i];", "        s2 += (uint64_t)i * (uint64_t)u[i];"),
     "checksum_drops_units": ("        s1 += (uint64_t)u[i];", "        s1 += (uint64_t)(u[i] & 0xFFFEu);"),
     "scaler_no_floor": ("            sc->scale = down < min_scale ? min_scale : down;", "            sc->scale = down;"),
+    "scaler_growth_keeps_hysteresis": ("            sc->good = 0;\n            sc->hyst_left = hysteresis;\n        }\n    }",
+                                       "            sc->good = 0;\n        }\n    }"),
+    "skip_still_writes": ("weight_decay, sc->scale, B, sc->step, &f, 1);", "weight_decay, sc->scale, B, sc->step, &f, 0);"),
+    "allreduce_reverse_order": ("        float s = orc_bf16_to_f32(in[0][j]);\n        for (int32_t r = 1; r < M; ++r) s = s + orc_bf16_to_f32(in[r][j]);",
+                                "        float s = orc_bf16_to_f32(in[M - 1][j]);\n        for (int32_t r = M - 2; r >= 0; --r) s = s + orc_bf16_to_f32(in[r][j]);"),
+    "allreduce_unscaled": ("        float y = s * scale;", "        float y = s;"),
+    "inv_rounded_in_fp32": ("out[0] = (float)(1.0 / ((double)B * (double)S));", "out[0] = 1.0f / ((float)B * S);"),
+    "sum_in_double": ("            for (int32_t r = 1; r < M; ++r) s = s + orc_bf16_to_f32(grads[r][j]);\n            if (!isfinite(s)) f = 1;",
+                      "            double sd = s;\n            for (int32_t r = 1; r < M; ++r) sd = sd + orc_bf16_to_f32(grads[r][j]);\n            s = (float)sd;\n            if (!isfinite(s)) f = 1;"),
+    "flag_ignores_nan": ("            if (!isfinite(s)) f = 1;\n        }\n        g_out[j]", "            if (isinf(s)) f = 1;\n        }\n        g_out[j]"),
+    "mhat_uses_bc2": ("float mh = m1 / bc1;", "float mh = m1 / bc2;"),
+    "decay_after_update": ("float w = master[j] * cdec - lr * u;", "float w = (master[j] - lr * u) * cdec;"),
+    "subnormal_ulp": ("double ulp = ldexp(1.0, (e == 0 ? 1 : e) - 127 - 7);", "double ulp = ldexp(1.0, e - 127 - 7);"),
+    "segments_shard_offset_from_tensor": ("seg_shard_off[count] = x0 - lo;", "seg_shard_off[count] = x0 - a;"),
+    "memory_state_unsharded": ("*zero1_bytes = 2 * n + 2 * n + 12 * shard;", "*zero1_bytes = 2 * n + 2 * n + 12 * n;"),
 }
 
 

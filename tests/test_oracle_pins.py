@@ -200,6 +200,17 @@ def test_reduce_order_is_rank_order_left_fold():
     assert got[0] == 2.0 ** 24 + 2
 
 
+def test_allreduce_order_is_rank_order_left_fold():
+    """The All-Reduce sums in the same order as the reduce-scatter: an fp32
+    left fold from rank 0, so 2^24 + 1 + 1 stays 2^24 and the reverse order
+    gives 2^24 + 2 (fp32 outputs keep the difference visible)."""
+    grads = [bf16_bits([2.0 ** 24]), bf16_bits([1.0]), bf16_bits([1.0])]
+    got = oracle.allreduce(grads, 1, scale=1.0, out_bf16=False)
+    assert all(float(o[0]) == 2.0 ** 24 for o in got)
+    got = oracle.allreduce(grads[::-1], 1, scale=1.0, out_bf16=False)
+    assert all(float(o[0]) == 2.0 ** 24 + 2 for o in got)
+
+
 def test_reduce_padding_is_zero():
     grads = [bf16_bits([1.0, 2.0, 3.0])] * 2
     got, _ = oracle.reduce_scatter(grads, 2, 5, 0.5)
@@ -474,6 +485,25 @@ def test_overflow_ignores_padding_and_skip_writes_nothing():
     oracle.zero1_step([g[:2].copy() for g in grads], 2, master, m, v, params, AdamW(step=3), flag=flag,
                       skip_if_flag=True)
     assert flag[0] == 0 and not np.array_equal(master, snap[0])
+
+
+def _nearest_f32(x: Fraction) -> np.float32:
+    """The float32 nearest to the exact rational x (ties to the even code)."""
+    c = np.float32(float(x))
+    cands = [np.nextafter(c, np.float32(-np.inf)), c, np.nextafter(c, np.float32(np.inf))]
+    best = min(abs(Fraction(float(y)) - x) for y in cands)
+    near = [y for y in cands if abs(Fraction(float(y)) - x) == best]
+    return min(near, key=lambda y: int(np.array(y, np.float32).view(np.uint32)) & 1)
+
+
+def test_inverse_batch_scale_is_rounded_once():
+    """1/(B*S), evaluated in double and then rounded to fp32, equals the exact
+    quotient rounded once to fp32 on these cases, also where B*S itself has
+    no fp32 representation (2^24 + 1, 3 * (2^24 + 1) * 2^10)."""
+    for B, S in [(2 ** 24 + 1, 1.0), (3 * (2 ** 24 + 1), 1024.0), (1000, 3.0), (1024, 65536.0)]:
+        got = np.float32(oracle.adamw_constants(AdamW(global_batch=B, loss_scale=S))["inv"])
+        want = _nearest_f32(Fraction(1, B) / Fraction(S))
+        assert got.view(np.uint32) == want.view(np.uint32), (B, S)
 
 
 def test_bias_correction_power():

@@ -558,11 +558,13 @@ int zero1_abi_version(void);
  * kernels, the shared-memory staged kernel or the wait self-test).  *kernel_name
  * gets its (mangled) name, owned by the CUDA runtime; *grid the blocks it was
  * launched with; *blocks_per_sm the resident blocks per SM the grid was
- * sized from (one wave = SMs x blocks_per_sm, each kernel's own occupancy);
- * *w32 1 if its vector body moved the fp32 arrays in 32-byte accesses, 0 if
- * in 16-byte ones.  Any pointer may be NULL.  EINVAL if this thread has
- * launched nothing yet; ECUDA if the runtime cannot name the kernel. */
-int zero1_debug_last_launch(const char **kernel_name, int32_t *grid, int32_t *blocks_per_sm, int32_t *w32);
+ * sized from (one wave = SMs x blocks_per_sm: the kernel's occupancy, or the
+ * smaller count of its launch shape); *block the threads per block; *w32 1 if
+ * its vector body moved the fp32 arrays in 32-byte accesses, 0 if in 16-byte
+ * ones.  Any pointer may be NULL.  EINVAL if this thread has launched nothing
+ * yet; ECUDA if the runtime cannot name the kernel. */
+int zero1_debug_last_launch(const char **kernel_name, int32_t *grid, int32_t *blocks_per_sm, int32_t *block,
+                            int32_t *w32);
 
 #ifdef __cplusplus
 }

@@ -39,7 +39,7 @@ def test_header_declares_the_boundary():
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), f"{name} declared in zero1.h but not exported"
-    assert lib.zero1_abi_version() == 2
+    assert lib.zero1_abi_version() == 3
 
 
 @pytest.mark.parametrize("n", [1, 2, 7, 8, 9, 1000, 4099, 10**6 + 3, 1_300_000_000, 7_500_000_000])
@@ -279,7 +279,7 @@ int main(void)
     if (zero1_plan(10, 65, 1, NULL, 0, &p) != ZERO1_ERANGE) return 6;
     if (strcmp(zero1_strerror(ZERO1_ERANGE), "size or replica count out of the supported range") != 0) return 7;
     printf(" | %s\n", zero1_last_error());
-    return zero1_abi_version() == 2 ? 0 : 8;
+    return zero1_abi_version() == 3 ? 0 : 8;
 }
 """
 

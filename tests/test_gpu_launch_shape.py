@@ -29,52 +29,49 @@ def _fused(dev, n, M, state_offset=0):
 
 
 def test_each_kernel_gets_its_own_occupancy(cuda_device):
-    """The small-range kernel (up to four blocks per SM) and the two-deep
-    large-range kernel (one block per SM at M = 8) share a signature; a call
-    of one must not fix the grid of the other."""
+    """The fused kernel on a small range (its full occupancy, blocks of 256)
+    and on a large one (the launch shape of its table: five blocks of 128
+    per SM at M = 8) keep their own grids whatever ran before."""
     dev = cuda_device
     sms = _sms()
-    big, small = 8 << 20, 1 << 16            # 8M elements: large-range shape; 64K: small-range kernel
+    big, small = 8 << 20, 1 << 16            # 8M elements: the table's shape; 64K: full occupancy
     first_big = _fused(dev, big, 8)
     first_small = _fused(dev, small, 8)
     again_big = _fused(dev, big, 8)
-    assert "k_fused_step_wide" in first_small["kernel"] and "k_fused_step_wide" not in first_big["kernel"]
+    assert "k_fused_step" in first_big["kernel"] and "k_fused_step" in first_small["kernel"]
     assert first_big == again_big
-    assert first_big["blocks_per_sm"] == 1
-    assert first_small["blocks_per_sm"] >= 2
-    assert first_big["grid"] == sms * first_big["blocks_per_sm"]
+    assert (first_big["blocks_per_sm"], first_big["block"]) == (5, 128)
+    assert first_big["grid"] == sms * 5
+    assert first_small["block"] == 256 and first_small["blocks_per_sm"] >= 4
     # the small range needs fewer blocks than a wave: one vector of 8 per thread
     assert first_small["grid"] == min(sms * first_small["blocks_per_sm"], -(-small // 8 // 256))
 
 
 def test_large_range_shapes_per_replica_count(cuda_device):
-    """On a large range the fused step runs the one-vector kernel at two
-    blocks per SM for M <= 5 and the two-deep kernel at one block per SM for
-    M = 6..8 (the measured faster shape for each M); the grid is one wave."""
+    """On a large range the fused step runs 16 warps per SM (two blocks of
+    256) for M = 3..5 and 20 warps per SM (five blocks of 128) for M = 1, 2
+    and 6..8, the measured faster shape for each M; the grid is one wave."""
     dev = cuda_device
     sms = _sms()
     big = 8 << 20
-    for M in (1, 3, 5):
+    for M, per_sm, block in ((1, 5, 128), (2, 5, 128), (3, 2, 256), (5, 2, 256), (6, 5, 128), (8, 5, 128)):
         d = _fused(dev, big, M)
-        assert "k_fused_step_wide" in d["kernel"], (M, d)
-        assert d["blocks_per_sm"] == 2 and d["grid"] == 2 * sms, (M, d)
-    for M in (6, 8):
-        d = _fused(dev, big, M)
-        assert "k_fused_step_wide" not in d["kernel"] and "k_fused_step" in d["kernel"], (M, d)
-        assert d["blocks_per_sm"] == 1 and d["grid"] == sms, (M, d)
-    # the same one-vector kernel on a small range keeps its full occupancy
-    d = _fused(dev, 1 << 16, 3)
-    assert "k_fused_step_wide" in d["kernel"] and d["blocks_per_sm"] >= 3, d
+        assert "k_fused_step" in d["kernel"] and "grouped" not in d["kernel"], (M, d)
+        assert (d["blocks_per_sm"], d["block"]) == (per_sm, block) and d["grid"] == per_sm * sms, (M, d)
+    # M > 8: the grouped kernel at its occupancy
+    d = _fused(dev, 1 << 20, 9)
+    assert "k_fused_step_grouped" in d["kernel"] and d["block"] == 256, d
 
 
 def test_allreduce_and_update_shapes(cuda_device):
-    """All-reduce grids follow their per-M table (one-vector kernels at two or
-    three blocks per SM, two-deep at M = 8); the dynamic step's update from
+    """All-reduce grids follow their per-M table (one vector per thread, the
+    blocks per SM and block size of the table); the dynamic step's update from
     the sums runs one vector per thread at two blocks per SM."""
     dev = cuda_device
     sms = _sms()
     n = 4 << 20
-    for M, per_sm, one_vector in ((1, 3, True), (3, 2, True), (4, 3, True), (6, 2, True), (8, None, False)):
+    for M, per_sm, block, one_vector in ((1, 3, 256, True), (2, 5, 128, True), (3, 2, 256, True),
+                                         (4, 5, 128, True), (6, 2, 256, True), (8, 3, 128, True)):
         plan = z.zero1_plan(n, M, 1)
         grads = make_grads(M, n, 1e-3, 5, 1, dev)
         outs = [torch.empty(n, dtype=torch.bfloat16, device=dev) for _ in range(M)]
@@ -83,8 +80,7 @@ def test_allreduce_and_update_shapes(cuda_device):
         assert "k_allreduce" in d["kernel"], d
         # the depth is the kernel's last template argument (mangled: ...ELi<D>EEE)
         assert ("Li1EEE" if one_vector else "Li2EEE") in d["kernel"], (M, d)
-        if per_sm is not None:
-            assert d["blocks_per_sm"] == per_sm and d["grid"] == per_sm * sms, (M, d)
+        assert (d["blocks_per_sm"], d["block"]) == (per_sm, block) and d["grid"] == per_sm * sms, (M, d)
     M = 8
     plan = z.zero1_plan(n, M, 1)
     P = plan.padded_n
@@ -100,10 +96,10 @@ def test_allreduce_and_update_shapes(cuda_device):
     torch.cuda.synchronize()
     d = z.debug_last_launch()
     assert "k_apply_sums" in d["kernel"] and d["blocks_per_sm"] == 2 and d["grid"] == 2 * sms, d
-    # the unfused update: one vector per thread at two blocks per SM
+    # the unfused update: one vector per thread, five blocks of 128 per SM
     z.zero1_adamw_update(plan, 0, M, sums, master, m, v, hp)
     d = z.debug_last_launch()
-    assert "k_adamw" in d["kernel"] and "Li1E" in d["kernel"] and d["grid"] == 2 * sms, d
+    assert "k_adamw" in d["kernel"] and "Li1E" in d["kernel"] and (d["grid"], d["block"]) == (5 * sms, 128), d
     # the overflow check at M = 8: three blocks per SM
     flag = torch.zeros(1, dtype=torch.int32, device=dev)
     z.zero1_overflow_check(plan, 0, M, grads, flag)
@@ -115,6 +111,37 @@ def test_allreduce_and_update_shapes(cuda_device):
     torch.cuda.synchronize()
     d = z.debug_last_launch()
     assert "k_restore_params" in d["kernel"] and d["blocks_per_sm"] == 4 and d["grid"] == 4 * sms, d
+
+
+def test_pingpong_shape_depends_on_where_the_state_lives(cuda_device):
+    """The ping-pong kernel runs the HBM table's shape (one vector per thread,
+    five blocks of 128 per SM at M = 8) on device state and two vectors in
+    flight per thread at its occupancy when both copies are in host memory."""
+    dev = cuda_device
+    sms = _sms()
+    M, n = 8, 4 << 20
+    plan = z.zero1_plan(n, M, 1)
+    P = plan.padded_n
+    grads = make_grads(M, n, 1e-3, 12, 1, dev)
+    policy = z.LossScalePolicy()
+    hp = z.AdamW(global_batch=64)
+    for on_host in (False, True):
+        state = make_state(n, P, 13, dev)
+        if on_host:
+            state = [t.cpu().pin_memory() for t in state]
+        pairs = [[x, torch.empty(x.shape, dtype=x.dtype, pin_memory=True) if on_host else torch.empty_like(x)]
+                 for x in state]
+        params = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+        scaler = z.new_scaler(dev)
+        z.zero1_scaler_init(scaler, policy, hp)
+        z.PingPongBuckets(plan, 0, M, *pairs, params, scaler, policy).bucket(0, P, grads, hp)
+        torch.cuda.synchronize()
+        d = z.debug_last_launch()
+        assert "k_fused_step_pingpong" in d["kernel"], d
+        if on_host:
+            assert "Li2EEE" in d["kernel"] and d["block"] == 256 and d["grid"] == d["blocks_per_sm"] * sms, d
+        else:
+            assert "Li1EEE" in d["kernel"] and (d["blocks_per_sm"], d["block"]) == (5, 128), d
 
 
 def test_grouped_allreduce_runs_two_blocks_per_sm(cuda_device):

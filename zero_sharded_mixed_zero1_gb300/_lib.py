@@ -33,7 +33,7 @@ class Zero1Error(RuntimeError):
 
 
 # zero1_abi_version() of the library this binding is written for.
-ABI_VERSION = 2
+ABI_VERSION = 3
 
 
 class Plan(ctypes.Structure):
@@ -169,7 +169,7 @@ def load() -> ctypes.CDLL:
     lib.zero1_last_error.restype = ctypes.c_char_p
     lib.zero1_abi_version.argtypes = []
     lib.zero1_abi_version.restype = ctypes.c_int
-    lib.zero1_debug_last_launch.argtypes = [ctypes.POINTER(ctypes.c_char_p), vp, vp, vp]
+    lib.zero1_debug_last_launch.argtypes = [ctypes.POINTER(ctypes.c_char_p), vp, vp, vp, vp]
     lib.zero1_debug_last_launch.restype = ctypes.c_int
     if lib.zero1_abi_version() != ABI_VERSION:
         raise ImportError(f"libzero1.so has ABI version {lib.zero1_abi_version()}, the binding expects "
@@ -255,13 +255,14 @@ def zero1_plan_segments(plan: Plan, tensor_numels, shard_index: int):
 def debug_last_launch() -> dict:
     """The last kernel launched by a library call on this host thread: its
     (mangled) name, grid, the resident blocks per SM the grid was sized from,
-    and whether the vector body moved fp32 in 32-byte accesses."""
+    the threads per block, and whether the vector body moved fp32 in 32-byte
+    accesses."""
     name = ctypes.c_char_p()
-    grid, per_sm, w32 = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    grid, per_sm, block, w32 = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
     _check_rc(load().zero1_debug_last_launch(ctypes.byref(name), ctypes.byref(grid), ctypes.byref(per_sm),
-                                             ctypes.byref(w32)))
+                                             ctypes.byref(block), ctypes.byref(w32)))
     return {"kernel": name.value.decode(), "grid": grid.value, "blocks_per_sm": per_sm.value,
-            "w32": bool(w32.value)}
+            "block": block.value, "w32": bool(w32.value)}
 
 
 def zero1_plan_memory(plan: Plan) -> tuple[int, int]:

@@ -31,8 +31,8 @@ __device__ __forceinline__ void add_pair(uint32_t word, int64_t j, uint64_t &s1,
 __global__ void __launch_bounds__(kBlock)
 k_checksum16(const uint16_t *__restrict__ u, const Walk w, unsigned long long *out)
 {
-    const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
-    const int64_t nthr = (int64_t)gridDim.x * kBlock;
+    const int64_t tid = grid_tid();
+    const int64_t nthr = grid_threads();
     uint64_t s1 = 0, s2 = 0;
     for (int64_t i = tid; i < w.nvec; i += nthr) {
         const int64_t j = w.head + i * kVec;

@@ -21,7 +21,12 @@
 namespace {
 
 constexpr int kVec = 8;      // elements per thread per iteration (16 B of bf16)
-constexpr int kBlock = 256;  // threads per block
+constexpr int kBlock = 256;  // threads per block (at most; a launch shape may use fewer)
+
+// This thread's index in the grid and the grid's thread count, whatever the
+// block size of the launch.
+__device__ __forceinline__ int64_t grid_tid() { return (int64_t)blockIdx.x * blockDim.x + threadIdx.x; }
+__device__ __forceinline__ int64_t grid_threads() { return (int64_t)gridDim.x * blockDim.x; }
 
 struct GradPtrs {
     const uint16_t *p[ZERO1_MAX_REPLICAS];
@@ -260,24 +265,30 @@ struct GradLoads {
 #define Z1_BOUNDS(MT, D) __launch_bounds__(kBlock, (MT) == 0 ? 3 : ((D) == 1 ? 4 : 1))
 
 // How a streaming kernel is launched over a large range: D vectors of loads
-// in flight per thread (1 or 2), and a grid of at most per_sm resident blocks
-// per SM (0: as many as fit).
+// in flight per thread (1 or 2), a grid of at most per_sm resident blocks per
+// SM (0: as many as fit), blocks of `block` threads (at most kBlock).
 struct Shape {
     int D, per_sm;
+    int block = kBlock;
 };
 
 // Launch shape of the in-place fused update for M = MT on a large range
-// (k_fused_step_scaled, and the fused step: D = 2 is k_fused_step, D = 1
-// k_fused_step_wide with at most per_sm blocks per SM; MT = 0: M > 8,
-// replicas in groups of 8, where D is not used).  Measured on GB300, fused
-// step on 124M elements, fraction of the measured copy bandwidth (two-deep
-// against one vector at two blocks per SM): M = 1..5 0.925 0.925 0.931 0.958
-// 0.979 against 0.948 0.969 0.998 1.016 1.017; M = 6..8 0.997 1.010 1.022
-// against 0.969 0.960 0.984.  One vector at three or four blocks per SM was
-// slower for every M (0.85-0.97), so the fastest grid is not the fullest one.
+// (k_fused_step and k_fused_step_scaled, one vector of loads per thread;
+// MT = 0: M > 8, replicas in groups of 8, where the shape is not used).
+// Measured on GB300 (fused step, 124M elements, one box, fraction of the
+// measured copy bandwidth), by warps per SM: 20 (five blocks of 128) for
+// M = 1, 2 and 6..8: 0.984 0.977 and 1.017 1.027 1.029; 16 (two blocks of
+// 256) for M = 3..5: 0.993 1.015 1.020, where 20 gave 0.973 0.955 0.939.
+// 12 warps gave 0.79-0.93 and 24 warps 0.85-0.97 for every M.  The two-deep
+// pipeline this replaced (two vectors in flight per thread, 8 warps per SM)
+// reached 0.995 1.007 1.019 at M = 6..8 and 0.93-0.98 at M <= 5.
 constexpr Shape fused_shape(int MT)
 {
-    return MT >= 1 && MT <= 5 ? Shape{1, 2} : Shape{2, 0};
+    switch (MT) {
+    case 3: case 4: case 5: return Shape{1, 2};
+    case 0: return Shape{2, 0};
+    default: return Shape{1, 5, 128};
+    }
 }
 
 // fp32 state loads that do not allocate in L1 (each line is read once) and
@@ -352,15 +363,15 @@ __device__ __forceinline__ F8 ld_plain8(const float *p, bool w32)
     return r;
 }
 
-// Which kernels store fp32 in 32-byte accesses (each passes w32 && its
-// policy as st_stream8's flag).  Measured on GB300 with CUDA events, every
-// other choice equal: 32-byte loads never lost, but 32-byte stores pay only
-// where the writes go to a separate buffer (ping-pong copies, reduce-scatter
-// and all-reduce outputs) or make up about half of an in-place update's
-// traffic (the dynamic step's update from sums; the fused step at M <= 2,
-// +2.5 %); an in-place update that reads far more than it writes ran 1-7 %
-// slower with them (the fused step from M = 4, 7 % at M = 64).
-__host__ __device__ constexpr bool wide_stores_in_place(int MT) { return MT >= 1 && MT <= 2; }
+// Which kernels store fp32 in 32-byte accesses (each passes w32, or false,
+// as st_stream8's flag).  Measured on GB300 with CUDA events, every other
+// choice equal: 32-byte loads never lost, but 32-byte stores pay only where
+// the writes go to a separate buffer (ping-pong copies, reduce-scatter and
+// all-reduce outputs) or make up about half of an in-place update's traffic
+// (the dynamic step's update from sums, AdamW); the in-place fused step (and
+// k_fused_step_scaled) stores in 16-byte accesses: with 32-byte ones it ran
+// 1-9 % slower from M = 3 (7 % at M = 64) and within 0.4 % at M = 1, 2.
+constexpr bool kWideStoresInPlace = false;
 
 // Streaming (.cs) store of 8 floats: one 32-byte access if w32, else two
 // 16-byte ones.
@@ -482,8 +493,8 @@ __global__ void Z1_BOUNDS(MT, D)
 k_reduce_scatter(const __grid_constant__ GradPtrs g, int M, const Walk w, float scale, void *out,
                  uint32_t *flag)
 {
-    const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
-    const int64_t nthr = (int64_t)gridDim.x * kBlock;
+    const int64_t tid = grid_tid();
+    const int64_t nthr = grid_threads();
     bool bad = false;
     if constexpr (MT > 0) {
         pipelined<GradLoads<MT>, D>(
@@ -529,14 +540,20 @@ k_reduce_scatter(const __grid_constant__ GradPtrs g, int M, const Walk w, float 
 
 // Launch shape of k_reduce_scatter for M = MT (MT = 0: M > 8, replicas in
 // groups of 8, where D is not used).  Measured on GB300, fp32 output, 124M
-// elements: for M = 4..7 one vector at three blocks per SM reached 0.987
-// 1.001 1.011 1.010 of the measured copy bandwidth against 0.979 1.000 1.010
-// 0.990 two-deep; for the other M the two were within 0.3 %.  In the dynamic
-// step (followed by k_apply_sums) this table measured within 0.1 % of the
-// best of the uniform shapes for every M.
+// elements, fraction of the measured copy bandwidth: two-deep at full
+// occupancy 0.937 0.949 0.972 0.979 1.000 1.010 0.990 0.995 for M = 1..8;
+// one vector at three blocks of 256 per SM 0.987 1.001 1.011 1.010 for
+// M = 4..7; one vector at 20 warps per SM (five blocks of 128) 0.964 and
+// 1.006 for M = 2 and 8.  This table: 0.931 0.963 0.976 0.990 1.007 1.016
+// 1.016 1.013.  In the dynamic step (followed by k_apply_sums) it measured
+// within 0.1 % of the best of the uniform shapes for every M.
 constexpr Shape rs_shape(int MT)
 {
-    return MT >= 4 && MT <= 7 ? Shape{1, 3} : Shape{2, 0};
+    switch (MT) {
+    case 2: case 8: return Shape{1, 5, 128};
+    case 4: case 5: case 6: case 7: return Shape{1, 3};
+    default: return Shape{2, 0};
+    }
 }
 
 // ------------------------------------------------------------ host side ----
@@ -592,15 +609,15 @@ int64_t work_of(const Walk &w)
     return w.nvec > ns ? w.nvec : ns;
 }
 
-// Resident blocks per SM of one kernel on the current device, from the
-// occupancy API on first use and then from a small table keyed by the
-// kernel's address and the device (kernels of the same signature each get
-// their own entry).
-int blocks_per_sm(const void *kernel)
+// Resident blocks per SM of one kernel launched with `block` threads per
+// block on the current device, from the occupancy API on first use and then
+// from a small table keyed by the kernel's address, the block size and the
+// device (kernels of the same signature each get their own entry).
+int blocks_per_sm(const void *kernel, int block)
 {
     struct Entry {
         const void *kernel;
-        int dev, per_sm;
+        int block, dev, per_sm;
     };
     static std::mutex mu;
     static Entry table[256];
@@ -610,33 +627,33 @@ int blocks_per_sm(const void *kernel)
     {
         std::lock_guard<std::mutex> lock(mu);
         for (int k = 0; k < used; ++k)
-            if (table[k].kernel == kernel && table[k].dev == dev) return table[k].per_sm;
+            if (table[k].kernel == kernel && table[k].block == block && table[k].dev == dev) return table[k].per_sm;
     }
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kBlock, 0) != cudaSuccess || per_sm <= 0) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, block, 0) != cudaSuccess || per_sm <= 0) {
         cudaGetLastError();
         per_sm = 1;
     }
     std::lock_guard<std::mutex> lock(mu);
-    if (used < 256) table[used++] = {kernel, dev, per_sm};
+    if (used < 256) table[used++] = {kernel, block, dev, per_sm};
     return per_sm;
 }
 
-// One resident wave for a walk: SMs x this kernel's resident blocks (at most
-// max_per_sm of them when that is positive), capped by the work.  The launch
-// is noted for zero1_debug_last_launch.
+// One resident wave for a walk: SMs x this kernel's resident blocks of
+// `block` threads (at most max_per_sm of them when that is positive), capped
+// by the work.  The launch is noted for zero1_debug_last_launch.
 template <class K>
-int grid_for(K kernel, const Walk &w, int max_per_sm = 0)
+int grid_for(K kernel, const Walk &w, int max_per_sm = 0, int block = kBlock)
 {
     const void *k = reinterpret_cast<const void *>(kernel);
-    int per_sm = blocks_per_sm(k);
+    int per_sm = blocks_per_sm(k, block);
     if (max_per_sm > 0 && max_per_sm < per_sm) per_sm = max_per_sm;
     const int64_t wave = (int64_t)sm_count() * per_sm;
     const int64_t work = work_of(w);
-    int64_t need = (work + kBlock - 1) / kBlock;
+    int64_t need = (work + block - 1) / block;
     if (need < 1) need = 1;
     const int grid = (int)(need < wave ? need : (wave > 0 ? wave : 1));
-    z1_note_launch(k, grid, per_sm, w.w32);
+    z1_note_launch(k, grid, per_sm, block, w.w32);
     return grid;
 }
 

@@ -110,8 +110,8 @@ k_apply_sums(const float *__restrict__ sums, float *__restrict__ master, float *
     c.inv = sc->inv;
     c.bc1 = sc->bc1;
     c.bc2 = sc->bc2;
-    const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
-    const int64_t nthr = (int64_t)gridDim.x * kBlock;
+    const int64_t tid = grid_tid();
+    const int64_t nthr = grid_threads();
     bool bad = false;  // the flag was already taken by the reduce-scatter
     const bool w32 = w.w32 != 0;
     pipelined<StateLoads, D>(
@@ -177,8 +177,8 @@ __device__ __forceinline__ void pingpong_body(const GradPtrs &g, int M, const Pi
     float *__restrict__ dw = s.master[CUR ^ 1];
     float *__restrict__ dm = s.mom[CUR ^ 1];
     float *__restrict__ dv = s.var[CUR ^ 1];
-    const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
-    const int64_t nthr = (int64_t)gridDim.x * kBlock;
+    const int64_t tid = grid_tid();
+    const int64_t nthr = grid_threads();
     bool bad = false;
     const bool w32 = w.w32 != 0;
     if constexpr (MT > 0) {
@@ -238,15 +238,29 @@ k_fused_step_pingpong(const __grid_constant__ GradPtrs g, int M, const __grid_co
 
 // Launch shape of k_fused_step_pingpong for M = MT (MT = 0: M > 8, replicas
 // in groups of 8, where D is not used).  Measured on GB300, the ping-pong
-// step on 124M elements, fraction of the measured copy bandwidth: M = 1..4
-// two-deep 0.909 0.915 0.932 0.951, one vector at two blocks per SM 0.949
-// 0.975 0.995 1.006; M = 5 two-deep 0.967, one vector at three blocks per SM
-// 0.979 (at two: 0.907); M = 6..8 two-deep 0.981 0.992 1.002, ahead of every
-// one-vector grid.
+// step on 124M elements, fraction of the measured copy bandwidth: two-deep
+// 0.909 0.915 0.932 0.951 0.967 0.981 0.992 1.002 for M = 1..8; one vector
+// at 16 warps per SM 0.949 0.975 0.995 1.006 for M = 1..4 and, at M = 5,
+// 1.003 in blocks of 128 but 0.91 in blocks of 256; one vector at 20 warps
+// per SM (five blocks of 128) 0.966 for M = 1 and 1.009 1.014 1.016 for
+// M = 6..8.  This table: 0.965 0.975 0.998 1.011 1.009 1.014 1.018 1.023.
 constexpr Shape pingpong_shape(int MT)
 {
-    return MT >= 1 && MT <= 4 ? Shape{1, 2} : (MT == 5 ? Shape{1, 3} : Shape{2, 0});
+    switch (MT) {
+    case 2: case 3: case 4: return Shape{1, 2};
+    case 5: return Shape{1, 4, 128};
+    case 0: return Shape{2, 0};
+    default: return Shape{1, 5, 128};
+    }
 }
+
+// The ping-pong kernel's shape when both state copies live in host memory:
+// two vectors in flight per thread at the kernel's occupancy.  Measured on
+// GB300 against the HBM table's shape on one box (M = 8, three runs each,
+// median step): 8.94-8.97 against 9.06-9.15 ms at 124M elements, 94.3-94.4
+// against 94.6-95.6 ms at 1.3B, 63.2-63.4 against 63.6-64.0 ms on the Llama
+// layers.
+constexpr Shape kPingPongHostShape{2, 0};
 
 // The fused step in place, with S and t taken from the scaler, for a range
 // whose overflow flag is already final (an overflow pass over all of the
@@ -265,8 +279,8 @@ k_fused_step_scaled(const __grid_constant__ GradPtrs g, int M, float *__restrict
     c.inv = sc->inv;
     c.bc1 = sc->bc1;
     c.bc2 = sc->bc2;
-    const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
-    const int64_t nthr = (int64_t)gridDim.x * kBlock;
+    const int64_t tid = grid_tid();
+    const int64_t nthr = grid_threads();
     bool bad = false;  // the flag is final already; nothing is reported
     const bool w32 = w.w32 != 0;
     if constexpr (MT > 0) {
@@ -280,7 +294,7 @@ k_fused_step_scaled(const __grid_constant__ GradPtrs g, int M, float *__restrict
 #pragma unroll
                 for (int r = 1; r < MT; ++r) add8(x.q[r], sum);
                 store_vec(sum, x.w, x.m, x.v, master + j, mom + j, var + j, params + j, c, bad,
-                          w32 && wide_stores_in_place(MT));
+                          w32 && kWideStoresInPlace);
             });
     } else {
         for (int64_t i = tid; i < w.nvec; i += nthr) {
@@ -288,7 +302,7 @@ k_fused_step_scaled(const __grid_constant__ GradPtrs g, int M, float *__restrict
             const F8 xw = ld_plain8(master + j, w32), xm = ld_plain8(mom + j, w32), xv = ld_plain8(var + j, w32);
             float sum[kVec];
             sum8<0>(g, M, j, sum);
-            store_vec(sum, xw, xm, xv, master + j, mom + j, var + j, params + j, c, bad, w32 && wide_stores_in_place(0));
+            store_vec(sum, xw, xm, xv, master + j, mom + j, var + j, params + j, c, bad, w32 && kWideStoresInPlace);
         }
     }
     fused_scalar_rest(g, M, master, mom, var, params, w, c, tid, nthr, bad);
@@ -311,8 +325,8 @@ k_restore_params(const PingPong s, uint16_t *__restrict__ params, const Walk w, 
     if (*reinterpret_cast<const volatile uint32_t *>(&sc->overflow) == 0u) return;
     const float *__restrict__ master =
         (*reinterpret_cast<const volatile uint32_t *>(&sc->current) & 1u) ? s.master[1] : s.master[0];
-    const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
-    const int64_t nthr = (int64_t)gridDim.x * kBlock;
+    const int64_t tid = grid_tid();
+    const int64_t nthr = grid_threads();
     const bool w32 = w.w32 != 0;
     for (int64_t i = tid; i < w.nvec; i += nthr) {
         const int64_t j = w.head + i * kVec;
@@ -416,15 +430,15 @@ extern "C" int zero1_step_dynamic(const zero1_plan_t *plan, int32_t shard_begin,
     dispatch_m(M, [&](auto mt) {
         constexpr int MT = decltype(mt)::value;
         constexpr Shape sh = rs_shape(MT);
-        const int grid = grid_for(k_reduce_scatter<MT, false, sh.D>, wr, sh.per_sm);
-        k_reduce_scatter<MT, false, sh.D><<<grid, kBlock, 0, st>>>(g, M, wr, 1.0f, sums, flag);
+        const int grid = grid_for(k_reduce_scatter<MT, false, sh.D>, wr, sh.per_sm, sh.block);
+        k_reduce_scatter<MT, false, sh.D><<<grid, sh.block, 0, st>>>(g, M, wr, 1.0f, sums, flag);
     });
     // 2. the update from the sums (skipped on overflow)
     const ArrayRef ua[5] = {{sums, 4}, {master, 4}, {m, 4}, {v, 4}, {params, 2}};
     const Walk wu = make_walk(r.L, r.nv, ua, 5);
-    const int grid = grid_for(k_apply_sums<kApplyShape.D>, wu, kApplyShape.per_sm);
+    const int grid = grid_for(k_apply_sums<kApplyShape.D>, wu, kApplyShape.per_sm, kApplyShape.block);
     if ((rc = launch_status("dynamic step: reduce-scatter launch")) != ZERO1_OK) return rc;
-    const cudaError_t e = launch_pdl(k_apply_sums<kApplyShape.D>, grid, kBlock, st, (const float *)sums, master, m, v,
+    const cudaError_t e = launch_pdl(k_apply_sums<kApplyShape.D>, grid, kApplyShape.block, st, (const float *)sums, master, m, v,
                                      static_cast<uint16_t *>(params), wu, c, (const zero1_scaler_t *)scaler);
     if (e != cudaSuccess) return pdl_fail(e, "dynamic step: update launch");
     // 3. the scaler advances (only once the update is enqueued)
@@ -486,11 +500,20 @@ int launch_pingpong_range(const zero1_plan_t *plan, int64_t L, int64_t nv, const
     const Walk w = make_walk(L, nv, arr, 7 + M);
     uint16_t *pp = static_cast<uint16_t *>(params);
     cudaError_t e = cudaSuccess;
+    // state copies in host memory: the link, not HBM, sets the pace
+    const bool host = in_host_memory(s.master[0]);
     dispatch_m(M, [&](auto mt) {
         constexpr int MT = decltype(mt)::value;
         constexpr Shape sh = pingpong_shape(MT);
-        const int grid = grid_for(k_fused_step_pingpong<MT, sh.D>, w, sh.per_sm);
-        e = launch_pdl(k_fused_step_pingpong<MT, sh.D>, grid, kBlock, st, g, M, s, pp, w, c, scaler);
+        if (host) {
+            const int grid = grid_for(k_fused_step_pingpong<MT, kPingPongHostShape.D>, w, kPingPongHostShape.per_sm,
+                                      kPingPongHostShape.block);
+            e = launch_pdl(k_fused_step_pingpong<MT, kPingPongHostShape.D>, grid, kPingPongHostShape.block, st, g, M,
+                           s, pp, w, c, scaler);
+        } else {
+            const int grid = grid_for(k_fused_step_pingpong<MT, sh.D>, w, sh.per_sm, sh.block);
+            e = launch_pdl(k_fused_step_pingpong<MT, sh.D>, grid, sh.block, st, g, M, s, pp, w, c, scaler);
+        }
     });
     if (e != cudaSuccess) return pdl_fail(e, what);
     return launch_status(what);
@@ -617,8 +640,8 @@ int z1_scaled_range(const zero1_plan_t *plan, int64_t elem_begin, int64_t elem_e
     dispatch_m(M, [&](auto mt) {
         constexpr int MT = decltype(mt)::value;
         constexpr Shape sh = fused_shape(MT);
-        const int grid = grid_for(k_fused_step_scaled<MT, sh.D>, w, sh.per_sm);
-        k_fused_step_scaled<MT, sh.D><<<grid, kBlock, 0, st>>>(g, M, master, m, v, pp, w, c, scaler);
+        const int grid = grid_for(k_fused_step_scaled<MT, sh.D>, w, sh.per_sm, sh.block);
+        k_fused_step_scaled<MT, sh.D><<<grid, sh.block, 0, st>>>(g, M, master, m, v, pp, w, c, scaler);
     });
     return launch_status("scaled range launch");
 }

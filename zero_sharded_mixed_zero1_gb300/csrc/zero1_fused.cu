@@ -7,13 +7,11 @@
 //   12 B fp32 master/m/v read    ->  AdamW in registers   ->  12 B written
 //                                ->  bf16 parameter, 2 B written once
 //
-// 2M + 26 bytes per parameter, bound by HBM bandwidth.  Four kernels, chosen
-// per call: for M <= 8 on large ranges, two vectors of loads in flight per
-// thread at one block per SM (M = 6..8) or one vector per thread at two
-// blocks per SM (M <= 5), whichever measured faster (fused_shape); one vector
-// per thread at up to four blocks per SM on small ranges; replicas in groups
-// of 8 for M > 8; and four vectors of state loads in flight when master/m/v
-// live in host memory.  Arithmetic uses
+// 2M + 26 bytes per parameter, bound by HBM bandwidth.  Three kernels, chosen
+// per call: for M <= 8 one vector of loads per thread, in the launch shape
+// fused_shape gives for M (at full occupancy on small ranges); replicas in
+// groups of 8 for M > 8; and four vectors of state loads in flight when
+// master/m/v live in host memory.  Arithmetic uses
 // the explicit round-to-nearest intrinsics (__fadd_rn, __fmul_rn, __fdiv_rn,
 // __fsqrt_rn): no contraction, IEEE division and square root, so the results
 // are reproducible bit for bit.
@@ -33,64 +31,28 @@ __device__ __forceinline__ void fused_vec(int64_t j, const VecLoads<MT> &x, floa
     unpack8(x.q[0], s);
 #pragma unroll
     for (int r = 1; r < MT; ++r) add8(x.q[r], s);
-    store_vec(s, x.w, x.m, x.v, master + j, mom + j, var + j, params + j, c, bad, w32 && wide_stores_in_place(MT));
+    store_vec(s, x.w, x.m, x.v, master + j, mom + j, var + j, params + j, c, bad, w32 && kWideStoresInPlace);
 }
 
 // The fused reduce-scatter + AdamW + all-gather for M <= 8 (M = MT known at
-// compile time).
-//
-// Shape chosen by measurement on GB300 (CUDA events through this entry point
-// on the 124M-parameter workload): each thread issues all loads of its next
-// vector before computing the current one, so two vectors - 2 x (16M + 96)
-// bytes - are in flight per thread; the register budget this needs (launch
-// bounds of one block per SM) beat higher occupancy with one vector in flight
-// for M = 6..8.  For M <= 5 k_fused_step_wide at two blocks per SM is faster
-// (fused_shape).  fp32 state is read with L1::no_allocate and every store is
-// .cs.
+// compile time): one vector of loads per thread and iteration, at most 64
+// registers.  On a large range the grid has the shape fused_shape gives for
+// M (warps per SM and block size, measured); on a small range (at most
+// kSmallMaxVec vectors) it runs at its full occupancy, where the chain of
+// dependent iterations per thread, not bandwidth, sets the time.  fp32 state
+// is read with L1::no_allocate and every store is .cs.
+constexpr int64_t kSmallMaxVec = 1 << 18;  // 2M elements
+
 template <int MT>
-__global__ void __launch_bounds__(kBlock, MT <= 2 ? 2 : 1)
+__global__ void __launch_bounds__(kBlock, 4)
 k_fused_step(const __grid_constant__ GradPtrs g, int M, float *__restrict__ master,
              float *__restrict__ mom, float *__restrict__ var, uint16_t *__restrict__ params,
              const Walk w, const Z1Consts c, uint32_t *flag, int skip)
 {
     wait_prior_grid();
     if (skip && *reinterpret_cast<volatile uint32_t *>(flag) != 0u) return;
-    const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
-    const int64_t nthr = (int64_t)gridDim.x * kBlock;
-    bool bad = false;
-    const bool w32 = w.w32 != 0;
-    VecLoads<MT> cur, nxt;
-    int64_t i = tid;
-    if (i < w.nvec) cur.load(g, master, mom, var, w.head + i * kVec, w32);
-    for (; i < w.nvec; i += nthr) {
-        const int64_t j = w.head + i * kVec;
-        const bool more = i + nthr < w.nvec;
-        if (more) nxt.load(g, master, mom, var, j + nthr * kVec, w32);
-        fused_vec<MT>(j, cur, master, mom, var, params, c, bad, w32);
-        if (more) cur = nxt;
-    }
-    fused_scalar_rest(g, M, master, mom, var, params, w, c, tid, nthr, bad);
-    if (flag && !skip) warp_flag(flag, bad);
-}
-
-// The fused step for M <= 8 on small ranges (at most kWideMaxVec vectors):
-// one vector per thread and iteration at up to four blocks per SM.  Few
-// vectors per thread means the two-deep pipeline has nothing to overlap, and
-// the chain of dependent iterations per thread, not bandwidth, sets the time;
-// four times the threads shortens that chain.  The same kernel at two blocks
-// per SM is the large-range shape for M <= 5 (fused_shape).
-constexpr int64_t kWideMaxVec = 1 << 18;  // 2M elements
-
-template <int MT>
-__global__ void __launch_bounds__(kBlock, 4)
-k_fused_step_wide(const __grid_constant__ GradPtrs g, int M, float *__restrict__ master,
-                  float *__restrict__ mom, float *__restrict__ var, uint16_t *__restrict__ params,
-                  const Walk w, const Z1Consts c, uint32_t *flag, int skip)
-{
-    wait_prior_grid();
-    if (skip && *reinterpret_cast<volatile uint32_t *>(flag) != 0u) return;
-    const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
-    const int64_t nthr = (int64_t)gridDim.x * kBlock;
+    const int64_t tid = grid_tid();
+    const int64_t nthr = grid_threads();
     bool bad = false;
     const bool w32 = w.w32 != 0;
     for (int64_t i = tid; i < w.nvec; i += nthr) {
@@ -115,8 +77,8 @@ k_fused_step_grouped(const __grid_constant__ GradPtrs g, int M, float *__restric
 {
     wait_prior_grid();
     if (skip && *reinterpret_cast<volatile uint32_t *>(flag) != 0u) return;
-    const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
-    const int64_t nthr = (int64_t)gridDim.x * kBlock;
+    const int64_t tid = grid_tid();
+    const int64_t nthr = grid_threads();
     bool bad = false;
     const bool w32 = w.w32 != 0;
     for (int64_t i = tid; i < w.nvec; i += nthr) {
@@ -137,7 +99,7 @@ k_fused_step_grouped(const __grid_constant__ GradPtrs g, int M, float *__restric
             for (int k = 0; k < 8; ++k)
                 if (r0 + k < M) add8(q[k], s);
         }
-        store_vec(s, sw, sm, sv, master + j, mom + j, var + j, params + j, c, bad, w32 && wide_stores_in_place(0));
+        store_vec(s, sw, sm, sv, master + j, mom + j, var + j, params + j, c, bad, w32 && kWideStoresInPlace);
     }
     fused_scalar_rest(g, M, master, mom, var, params, w, c, tid, nthr, bad);
     if (flag && !skip) warp_flag(flag, bad);
@@ -163,8 +125,8 @@ k_fused_step_offload(const __grid_constant__ GradPtrs g, int M, float *__restric
 {
     wait_prior_grid();
     if (skip && *reinterpret_cast<volatile uint32_t *>(flag) != 0u) return;
-    const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
-    const int64_t nthr = (int64_t)gridDim.x * kBlock;
+    const int64_t tid = grid_tid();
+    const int64_t nthr = grid_threads();
     bool bad = false;
     const bool w32 = w.w32 != 0;
     for (int64_t i0 = tid; i0 < w.nvec; i0 += kOffloadDepth * nthr) {
@@ -247,22 +209,13 @@ int launch_fused_range(const zero1_plan_t *plan, int64_t L, int64_t nv, const vo
         dispatch_m(M, [&](auto mt) {
             constexpr int MT = decltype(mt)::value;
             if constexpr (MT > 0) {
-                // small ranges: the one-vector kernel at full occupancy
+                // small ranges: the kernel's full occupancy; large ones: fused_shape
                 constexpr Shape sh = fused_shape(MT);
-                const bool small = w.nvec <= kWideMaxVec;
-                if constexpr (sh.D == 1) {
-                    const int grid = grid_for(k_fused_step_wide<MT>, w, small ? 0 : sh.per_sm);
-                    e = launch_pdl(k_fused_step_wide<MT>, grid, kBlock, st, g, M, master, m, v, pp, w, c,
-                                   overflow_flag, skip);
-                } else if (small) {
-                    const int grid = grid_for(k_fused_step_wide<MT>, w);
-                    e = launch_pdl(k_fused_step_wide<MT>, grid, kBlock, st, g, M, master, m, v, pp, w, c,
-                                   overflow_flag, skip);
-                } else {
-                    const int grid = grid_for(k_fused_step<MT>, w, sh.per_sm);
-                    e = launch_pdl(k_fused_step<MT>, grid, kBlock, st, g, M, master, m, v, pp, w, c, overflow_flag,
-                                   skip);
-                }
+                static_assert(sh.D == 1, "the fused kernel keeps one vector per thread");
+                const bool small = w.nvec <= kSmallMaxVec;
+                const int block = small ? kBlock : sh.block;
+                const int grid = grid_for(k_fused_step<MT>, w, small ? 0 : sh.per_sm, block);
+                e = launch_pdl(k_fused_step<MT>, grid, block, st, g, M, master, m, v, pp, w, c, overflow_flag, skip);
             }
         });
     }

@@ -31,18 +31,18 @@ extern "C" const char *zero1_last_error(void) { return g_last_error; }
 namespace {
 struct LastLaunch {
     const void *kernel;
-    int grid, blocks_per_sm, w32;
+    int grid, blocks_per_sm, block, w32;
 };
-thread_local LastLaunch g_last_launch = {nullptr, 0, 0, 0};
+thread_local LastLaunch g_last_launch = {nullptr, 0, 0, 0, 0};
 }  // namespace
 
-void z1_note_launch(const void *kernel, int grid, int blocks_per_sm, int w32)
+void z1_note_launch(const void *kernel, int grid, int blocks_per_sm, int block, int w32)
 {
-    g_last_launch = {kernel, grid, blocks_per_sm, w32};
+    g_last_launch = {kernel, grid, blocks_per_sm, block, w32};
 }
 
 extern "C" int zero1_debug_last_launch(const char **kernel_name, int32_t *grid, int32_t *blocks_per_sm,
-                                       int32_t *w32)
+                                       int32_t *block, int32_t *w32)
 {
     if (!g_last_launch.kernel) return z1_fail(ZERO1_EINVAL, "no kernel launched on this thread yet");
     if (kernel_name) {
@@ -54,11 +54,12 @@ extern "C" int zero1_debug_last_launch(const char **kernel_name, int32_t *grid, 
     }
     if (grid) *grid = g_last_launch.grid;
     if (blocks_per_sm) *blocks_per_sm = g_last_launch.blocks_per_sm;
+    if (block) *block = g_last_launch.block;
     if (w32) *w32 = g_last_launch.w32;
     return ZERO1_OK;
 }
 
-extern "C" int zero1_abi_version(void) { return 2; }
+extern "C" int zero1_abi_version(void) { return 3; }
 
 extern "C" const char *zero1_strerror(int code)
 {

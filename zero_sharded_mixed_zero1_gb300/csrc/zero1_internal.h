@@ -74,4 +74,4 @@ int z1_check_scaler_and_policy(const zero1_scaler_t *scaler, const zero1_loss_sc
 // Record a kernel launch for zero1_debug_last_launch (per host thread): the
 // kernel, its grid, the resident blocks per SM the grid was sized from, and
 // whether the vector body moved fp32 in 32-byte accesses.
-void z1_note_launch(const void *kernel, int grid, int blocks_per_sm, int w32);
+void z1_note_launch(const void *kernel, int grid, int blocks_per_sm, int block, int w32);

@@ -20,8 +20,8 @@ template <int MT>
 __global__ void __launch_bounds__(kBlock, (MT) > 0 ? 5 : 3)
 k_overflow(const __grid_constant__ GradPtrs g, int M, const Walk w, uint32_t *flag)
 {
-    const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
-    const int64_t nthr = (int64_t)gridDim.x * kBlock;
+    const int64_t tid = grid_tid();
+    const int64_t nthr = grid_threads();
     bool bad = false;
     for (int64_t i = tid; i < w.nvec; i += nthr) {
         float s[kVec];
@@ -56,8 +56,8 @@ k_adamw(const float *__restrict__ gin, float *__restrict__ master, float *__rest
         float *__restrict__ var, const Walk w, const Z1Consts c)
 {
     wait_prior_grid();
-    const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
-    const int64_t nthr = (int64_t)gridDim.x * kBlock;
+    const int64_t tid = grid_tid();
+    const int64_t nthr = grid_threads();
     const bool w32 = w.w32 != 0;
     pipelined<StateLoads, D>(
         w.nvec, tid, nthr,
@@ -92,8 +92,8 @@ __global__ void __launch_bounds__(kBlock, D == 1 ? 4 : 1)
 k_all_gather(const float *__restrict__ master, uint16_t *__restrict__ params, const Walk w)
 {
     wait_prior_grid();
-    const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
-    const int64_t nthr = (int64_t)gridDim.x * kBlock;
+    const int64_t tid = grid_tid();
+    const int64_t nthr = grid_threads();
     const bool w32 = w.w32 != 0;
     pipelined<F8, D>(
         w.nvec, tid, nthr, [&](F8 &x, int64_t i) { x = ld_cs8(master + w.head + i * kVec, w32); },
@@ -111,10 +111,11 @@ k_all_gather(const float *__restrict__ master, uint16_t *__restrict__ params, co
 
 // Launch shapes of k_adamw and k_all_gather.  Measured on GB300, 124M
 // elements, fraction of the measured copy bandwidth: k_adamw two-deep at two
-// blocks per SM 0.952, one vector at two blocks per SM 0.982 (three: 0.949,
-// four: 0.921); k_all_gather two-deep at its full occupancy 0.998, one vector
-// at two, three, four blocks per SM 0.748, 0.895, 0.982.
-constexpr Shape kAdamwShape{1, 2};
+// blocks of 256 per SM 0.952, one vector at 12, 16, 20, 24, 32 warps per SM
+// 0.845, 0.973, 1.001, 0.949, 0.921 (20: five blocks of 128); k_all_gather
+// two-deep at its full occupancy 0.998, one vector at 12-32 warps per SM
+// 0.62-0.98.
+constexpr Shape kAdamwShape{1, 5, 128};
 constexpr Shape kAllGatherShape{2, 0};
 
 // All-gather of bf16 shards into M outputs (real elements only).
@@ -122,8 +123,8 @@ __global__ void __launch_bounds__(kBlock)
 k_all_gather_shards(const uint16_t *__restrict__ shards, const __grid_constant__ OutPtrs o, int M,
                     const Walk w)
 {
-    const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
-    const int64_t nthr = (int64_t)gridDim.x * kBlock;
+    const int64_t tid = grid_tid();
+    const int64_t nthr = grid_threads();
     for (int64_t i = tid; i < w.nvec; i += nthr) {
         const int64_t j = w.head + i * kVec;
         const uint4 q = ld_stream_u4(shards + j);
@@ -163,8 +164,8 @@ template <int MT, bool BF16, bool NC, int D>
 __device__ __forceinline__ void allreduce_body(const GradPtrs &g, const OutPtrs &o, int M, const Walk &w,
                                                float scale)
 {
-    const int64_t tid = (int64_t)blockIdx.x * kBlock + threadIdx.x;
-    const int64_t nthr = (int64_t)gridDim.x * kBlock;
+    const int64_t tid = grid_tid();
+    const int64_t nthr = grid_threads();
     const bool w32 = w.w32 != 0;
     if constexpr (MT > 0) {
         // in place, the next vector's loads touch other elements than the
@@ -224,17 +225,20 @@ k_allreduce_inplace(const __grid_constant__ GradPtrs g, const __grid_constant__ 
 // is not used), with separate outputs and in place.  Measured on GB300, bf16
 // outputs, 124M elements, M = 1..8, fraction of the measured copy bandwidth:
 // separate outputs two-deep 0.761 0.951 0.948 0.940 0.933 0.944 0.941 0.952,
-// this table 0.926 0.952 0.970 0.964 0.969 0.975 0.961 0.952; in place
-// two-deep 0.788 0.963 0.954 0.942 0.939 0.944 0.935 0.956, this table 0.789
-// 0.963 0.968 0.969 0.977 0.981 0.965 0.956.  Two or three blocks per SM: the
-// better of the two differs by M, reproducibly across boxes.  M > 8 (16M
-// elements): two blocks per SM 0.942 at M = 16 and 0.948 at M = 64, against
-// 0.922 and 0.929 at the kernel's occupancy of three.
+// this table 0.924 0.957 0.970 0.971 0.967 0.976 0.961 0.979; in place
+// two-deep 0.788 0.963 0.954 0.942 0.939 0.944 0.935 0.956, this table 0.777
+// 0.960 0.966 0.977 0.974 0.982 0.967 0.984.  The one-vector grids tried were
+// 12, 16, 20, 24 and 32 warps per SM (blocks of 128 or 256); the best differs
+// by M, reproducibly across boxes.  M > 8 (16M elements): two blocks of 256
+// per SM 0.942 at M = 16 and 0.948 at M = 64, against 0.922 and 0.929 at the
+// kernel's occupancy of three.
 constexpr Shape allreduce_shape(int MT)
 {
     switch (MT) {
-    case 1: case 4: return Shape{1, 3};
-    case 3: case 5: case 6: case 7: return Shape{1, 2};
+    case 1: return Shape{1, 3};
+    case 2: case 4: return Shape{1, 5, 128};
+    case 3: case 5: case 6: return Shape{1, 2};
+    case 7: case 8: return Shape{1, 3, 128};
     case 0: return Shape{2, 2};
     default: return Shape{2, 0};
     }
@@ -243,8 +247,10 @@ constexpr Shape allreduce_shape(int MT)
 constexpr Shape allreduce_inplace_shape(int MT)
 {
     switch (MT) {
-    case 3: case 4: return Shape{1, 3};
-    case 5: case 6: case 7: return Shape{1, 2};
+    case 3: return Shape{1, 3};
+    case 4: return Shape{1, 5, 128};
+    case 5: case 6: return Shape{1, 2};
+    case 7: case 8: return Shape{1, 3, 128};
     case 0: return Shape{2, 2};
     default: return Shape{2, 0};
     }
@@ -315,14 +321,14 @@ extern "C" int dp_allreduce(const zero1_plan_t *plan, const void *const *grads_i
         constexpr int MT = decltype(mt)::value;
         constexpr Shape sh = allreduce_shape(MT), ish = allreduce_inplace_shape(MT);
         if (osz == 2 && overlap) {
-            const int grid = grid_for(k_allreduce_inplace<MT, ish.D>, w, ish.per_sm);
-            k_allreduce_inplace<MT, ish.D><<<grid, kBlock, 0, st>>>(g, o, M, w, scale);
+            const int grid = grid_for(k_allreduce_inplace<MT, ish.D>, w, ish.per_sm, ish.block);
+            k_allreduce_inplace<MT, ish.D><<<grid, ish.block, 0, st>>>(g, o, M, w, scale);
         } else if (osz == 2) {
-            const int grid = grid_for(k_allreduce<MT, true, sh.D>, w, sh.per_sm);
-            k_allreduce<MT, true, sh.D><<<grid, kBlock, 0, st>>>(g, o, M, w, scale);
+            const int grid = grid_for(k_allreduce<MT, true, sh.D>, w, sh.per_sm, sh.block);
+            k_allreduce<MT, true, sh.D><<<grid, sh.block, 0, st>>>(g, o, M, w, scale);
         } else {
-            const int grid = grid_for(k_allreduce<MT, false, sh.D>, w, sh.per_sm);
-            k_allreduce<MT, false, sh.D><<<grid, kBlock, 0, st>>>(g, o, M, w, scale);
+            const int grid = grid_for(k_allreduce<MT, false, sh.D>, w, sh.per_sm, sh.block);
+            k_allreduce<MT, false, sh.D><<<grid, sh.block, 0, st>>>(g, o, M, w, scale);
         }
     });
     return launch_status("all-reduce launch");
@@ -356,11 +362,11 @@ extern "C" int zero1_reduce_scatter(const zero1_plan_t *plan, int32_t shard_begi
         constexpr int MT = decltype(mt)::value;
         constexpr Shape sh = rs_shape(MT);
         if (osz == 2) {
-            const int grid = grid_for(k_reduce_scatter<MT, true, sh.D>, w, sh.per_sm);
-            k_reduce_scatter<MT, true, sh.D><<<grid, kBlock, 0, st>>>(g, M, w, scale, out, flag);
+            const int grid = grid_for(k_reduce_scatter<MT, true, sh.D>, w, sh.per_sm, sh.block);
+            k_reduce_scatter<MT, true, sh.D><<<grid, sh.block, 0, st>>>(g, M, w, scale, out, flag);
         } else {
-            const int grid = grid_for(k_reduce_scatter<MT, false, sh.D>, w, sh.per_sm);
-            k_reduce_scatter<MT, false, sh.D><<<grid, kBlock, 0, st>>>(g, M, w, scale, out, flag);
+            const int grid = grid_for(k_reduce_scatter<MT, false, sh.D>, w, sh.per_sm, sh.block);
+            k_reduce_scatter<MT, false, sh.D><<<grid, sh.block, 0, st>>>(g, M, w, scale, out, flag);
         }
     });
     return launch_status("reduce-scatter launch");
@@ -386,8 +392,8 @@ extern "C" int zero1_adamw_update(const zero1_plan_t *plan, int32_t shard_begin,
     // every element of the range is updated: walk it as if all were real
     const Walk w = make_walk(r.L, r.L, arr, 4);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const int grid = grid_for(k_adamw<kAdamwShape.D>, w, kAdamwShape.per_sm);
-    const cudaError_t e = launch_pdl(k_adamw<kAdamwShape.D>, grid, kBlock, st, gin, master, m, v, w, c);
+    const int grid = grid_for(k_adamw<kAdamwShape.D>, w, kAdamwShape.per_sm, kAdamwShape.block);
+    const cudaError_t e = launch_pdl(k_adamw<kAdamwShape.D>, grid, kAdamwShape.block, st, gin, master, m, v, w, c);
     if (e != cudaSuccess) return pdl_fail(e, "adamw launch");
     return launch_status("adamw launch");
 }
@@ -407,8 +413,8 @@ extern "C" int zero1_all_gather(const zero1_plan_t *plan, int32_t shard_begin, i
     const ArrayRef arr[2] = {{master, 4}, {params, 2}};
     const Walk w = make_walk(r.nv, r.nv, arr, 2);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const int grid = grid_for(k_all_gather<kAllGatherShape.D>, w, kAllGatherShape.per_sm);
-    const cudaError_t e = launch_pdl(k_all_gather<kAllGatherShape.D>, grid, kBlock, st, master,
+    const int grid = grid_for(k_all_gather<kAllGatherShape.D>, w, kAllGatherShape.per_sm, kAllGatherShape.block);
+    const cudaError_t e = launch_pdl(k_all_gather<kAllGatherShape.D>, grid, kAllGatherShape.block, st, master,
                                      static_cast<uint16_t *>(params), w);
     if (e != cudaSuccess) return pdl_fail(e, "all-gather launch");
     return launch_status("all-gather launch");

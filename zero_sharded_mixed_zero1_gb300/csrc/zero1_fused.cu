@@ -11,18 +11,18 @@
 // per call: for M <= 8 one vector of loads per thread, in the launch shape
 // fused_shape gives for M (at full occupancy on small ranges); replicas in
 // groups of 8 for M > 8; and four vectors of state loads in flight when
-// master/m/v live in host memory.  Arithmetic uses
-// the explicit round-to-nearest intrinsics (__fadd_rn, __fmul_rn, __fdiv_rn,
-// __fsqrt_rn): no contraction, IEEE division and square root, so the results
-// are reproducible bit for bit.
+// master/m/v live in host memory.  Arithmetic uses the explicit
+// round-to-nearest intrinsics (__fadd_rn, __fmul_rn, __fdiv_rn, __fsqrt_rn):
+// no contraction, IEEE division and square root, so the results are
+// reproducible bit for bit.
 
 #include "zero1_device.cuh"
 #include "zero1_checks.h"
 
 namespace {
 
-// One 8-element vector of the fused step for M = MT <= 8 whose loads are in q
-// and the six state registers.
+// One 8-element vector of the fused step for M = MT <= 8 whose gradient and
+// state loads are in x.
 template <int MT>
 __device__ __forceinline__ void fused_vec(int64_t j, const VecLoads<MT> &x, float *master, float *mom, float *var,
                                           uint16_t *params, const Z1Consts &c, bool &bad, bool w32)

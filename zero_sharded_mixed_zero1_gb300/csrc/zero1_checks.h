@@ -1,8 +1,8 @@
 // zero1_checks.h - host-side argument checks and error reporting shared by
 // the library's CUDA sources (library-internal): alignment and overlap of the
-// caller's buffers, where a pointer lives, the gradient pointer array, and
-// launch errors.  Nothing here changes what a kernel does or how it is
-// launched.
+// caller's buffers, where a pointer lives, the gradient pointer array, launch
+// errors, and the compile-time check of the launch-shape tables.  Nothing
+// here changes what a kernel does or how it is launched.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -13,6 +13,14 @@
 #include "zero1_internal.h"
 
 namespace {
+
+// A launch shape the kernels support: one or two vectors in flight per
+// thread, whole warps, at most kBlock threads per block (the kernels' launch
+// bounds), and a non-negative cap on the blocks per SM.
+constexpr bool shape_ok(Shape s)
+{
+    return (s.D == 1 || s.D == 2) && s.per_sm >= 0 && s.block >= 32 && s.block <= kBlock && s.block % 32 == 0;
+}
 
 // A buffer's byte extent, for the overlap checks.
 struct Extent {

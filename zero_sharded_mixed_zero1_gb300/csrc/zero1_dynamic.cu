@@ -430,12 +430,14 @@ extern "C" int zero1_step_dynamic(const zero1_plan_t *plan, int32_t shard_begin,
     dispatch_m(M, [&](auto mt) {
         constexpr int MT = decltype(mt)::value;
         constexpr Shape sh = rs_shape(MT);
+        static_assert(shape_ok(sh), "reduce-scatter shape");
         const int grid = grid_for(k_reduce_scatter<MT, false, sh.D>, wr, sh.per_sm, sh.block);
         k_reduce_scatter<MT, false, sh.D><<<grid, sh.block, 0, st>>>(g, M, wr, 1.0f, sums, flag);
     });
     // 2. the update from the sums (skipped on overflow)
     const ArrayRef ua[5] = {{sums, 4}, {master, 4}, {m, 4}, {v, 4}, {params, 2}};
     const Walk wu = make_walk(r.L, r.nv, ua, 5);
+    static_assert(shape_ok(kApplyShape), "update-from-sums shape");
     const int grid = grid_for(k_apply_sums<kApplyShape.D>, wu, kApplyShape.per_sm, kApplyShape.block);
     if ((rc = launch_status("dynamic step: reduce-scatter launch")) != ZERO1_OK) return rc;
     const cudaError_t e = launch_pdl(k_apply_sums<kApplyShape.D>, grid, kApplyShape.block, st, (const float *)sums, master, m, v,
@@ -505,6 +507,7 @@ int launch_pingpong_range(const zero1_plan_t *plan, int64_t L, int64_t nv, const
     dispatch_m(M, [&](auto mt) {
         constexpr int MT = decltype(mt)::value;
         constexpr Shape sh = pingpong_shape(MT);
+        static_assert(shape_ok(sh) && shape_ok(kPingPongHostShape), "ping-pong shapes");
         if (host) {
             const int grid = grid_for(k_fused_step_pingpong<MT, kPingPongHostShape.D>, w, kPingPongHostShape.per_sm,
                                       kPingPongHostShape.block);
@@ -640,6 +643,7 @@ int z1_scaled_range(const zero1_plan_t *plan, int64_t elem_begin, int64_t elem_e
     dispatch_m(M, [&](auto mt) {
         constexpr int MT = decltype(mt)::value;
         constexpr Shape sh = fused_shape(MT);
+        static_assert(shape_ok(sh), "fused shape");
         const int grid = grid_for(k_fused_step_scaled<MT, sh.D>, w, sh.per_sm, sh.block);
         k_fused_step_scaled<MT, sh.D><<<grid, sh.block, 0, st>>>(g, M, master, m, v, pp, w, c, scaler);
     });

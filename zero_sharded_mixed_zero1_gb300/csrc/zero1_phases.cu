@@ -320,6 +320,7 @@ extern "C" int dp_allreduce(const zero1_plan_t *plan, const void *const *grads_i
     dispatch_m(M, [&](auto mt) {
         constexpr int MT = decltype(mt)::value;
         constexpr Shape sh = allreduce_shape(MT), ish = allreduce_inplace_shape(MT);
+        static_assert(shape_ok(sh) && shape_ok(ish), "all-reduce shapes");
         if (osz == 2 && overlap) {
             const int grid = grid_for(k_allreduce_inplace<MT, ish.D>, w, ish.per_sm, ish.block);
             k_allreduce_inplace<MT, ish.D><<<grid, ish.block, 0, st>>>(g, o, M, w, scale);
@@ -361,6 +362,7 @@ extern "C" int zero1_reduce_scatter(const zero1_plan_t *plan, int32_t shard_begi
     dispatch_m(M, [&](auto mt) {
         constexpr int MT = decltype(mt)::value;
         constexpr Shape sh = rs_shape(MT);
+        static_assert(shape_ok(sh), "reduce-scatter shape");
         if (osz == 2) {
             const int grid = grid_for(k_reduce_scatter<MT, true, sh.D>, w, sh.per_sm, sh.block);
             k_reduce_scatter<MT, true, sh.D><<<grid, sh.block, 0, st>>>(g, M, w, scale, out, flag);
@@ -392,6 +394,7 @@ extern "C" int zero1_adamw_update(const zero1_plan_t *plan, int32_t shard_begin,
     // every element of the range is updated: walk it as if all were real
     const Walk w = make_walk(r.L, r.L, arr, 4);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    static_assert(shape_ok(kAdamwShape), "AdamW shape");
     const int grid = grid_for(k_adamw<kAdamwShape.D>, w, kAdamwShape.per_sm, kAdamwShape.block);
     const cudaError_t e = launch_pdl(k_adamw<kAdamwShape.D>, grid, kAdamwShape.block, st, gin, master, m, v, w, c);
     if (e != cudaSuccess) return pdl_fail(e, "adamw launch");
@@ -413,6 +416,7 @@ extern "C" int zero1_all_gather(const zero1_plan_t *plan, int32_t shard_begin, i
     const ArrayRef arr[2] = {{master, 4}, {params, 2}};
     const Walk w = make_walk(r.nv, r.nv, arr, 2);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    static_assert(shape_ok(kAllGatherShape), "all-gather shape");
     const int grid = grid_for(k_all_gather<kAllGatherShape.D>, w, kAllGatherShape.per_sm, kAllGatherShape.block);
     const cudaError_t e = launch_pdl(k_all_gather<kAllGatherShape.D>, grid, kAllGatherShape.block, st, master,
                                      static_cast<uint16_t *>(params), w);

@@ -389,3 +389,39 @@ def test_pingpong_with_host_state_matches_oracle(cuda_device, M, n, align):
         assert_bf16_bits(u16(params), o_p, f"params attempt {k}")
     st = z.scaler_state(scaler)
     assert (st["step"], st["skipped"]) == (o_sc.step, o_sc.skipped) == (4, 2)
+
+
+@pytest.mark.parametrize("M,n,align", [(8, 100_003, 128), (3, 30_001, 1), (13, 9_999, 8)])
+def test_two_pass_dynamic_step_with_host_state_matches_oracle(cuda_device, M, n, align):
+    """The two-pass dynamically scaled step (reduce-scatter into HBM sums,
+    then the update from the sums) with master/m/v in pinned host memory,
+    updated over the link in place: every attempt bit for bit the oracle's,
+    overflowing ones included."""
+    dev = cuda_device
+    plan = z.zero1_plan(n, M, align)
+    P = plan.padded_n
+    policy = z.LossScalePolicy(initial_scale=1024.0, factor=2.0, window=2, hysteresis=1, min_scale=1.0)
+    hp = z.AdamW(global_batch=max(M, 64), step=1)
+    state = [pinned(t) for t in make_state(n, P, 170 + M, dev, nonzero_moments=True)]
+    o = [f32(t).copy() for t in state]
+    params = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+    o_p = np.zeros(n, np.uint16)
+    sums = torch.empty(P, dtype=torch.float32, device=dev)
+    scaler = z.new_scaler(dev)
+    z.zero1_scaler_init(scaler, policy, hp)
+    o_policy = oracle.LossScalePolicy(initial_scale=policy.initial_scale, factor=policy.factor,
+                                      window=policy.window, hysteresis=policy.hysteresis, min_scale=policy.min_scale)
+    o_sc = oracle.Scaler.start(o_policy, hp.step)
+    for k in range(5):
+        grads = make_grads(M, n, 1e-3 * o_sc.scale, 180 + M, k, dev)
+        if k in (1, 3):
+            grads[k % M][(29 * k) % n] = float("inf")
+        z.zero1_step_dynamic(plan, 0, M, grads, *state, params, hp, scaler, policy, sums)
+        torch.cuda.synchronize()
+        flag = oracle.zero1_dynamic_attempt([u16(g) for g in grads], n, *o, o_p, oracle_hp(hp), o_sc, o_policy)
+        assert flag == (1 if k in (1, 3) else 0)
+        for x, want, what in zip(state, o, ("master", "m", "v")):
+            assert_f32_bits(f32(x), want, f"{what} attempt {k}")
+        assert_bf16_bits(u16(params), o_p, f"params attempt {k}")
+    st = z.scaler_state(scaler)
+    assert (st["step"], st["skipped"]) == (o_sc.step, o_sc.skipped) == (4, 2)

@@ -96,6 +96,13 @@ def test_allreduce_and_update_shapes(cuda_device):
     torch.cuda.synchronize()
     d = z.debug_last_launch()
     assert "k_apply_sums" in d["kernel"] and d["blocks_per_sm"] == 2 and d["grid"] == 2 * sms, d
+    assert "k_apply_sumsILi1E" in d["kernel"], d
+    # state in host memory: the two-deep update at its occupancy
+    host_state = [t.cpu().pin_memory() for t in (master, m, v)]
+    z.zero1_step_dynamic(plan, 0, M, grads, *host_state, params, hp, scaler, policy, sums)
+    torch.cuda.synchronize()
+    d = z.debug_last_launch()
+    assert "k_apply_sumsILi2E" in d["kernel"] and d["grid"] == d["blocks_per_sm"] * sms, d
     # the unfused update: one vector per thread, five blocks of 128 per SM
     z.zero1_adamw_update(plan, 0, M, sums, master, m, v, hp)
     d = z.debug_last_launch()

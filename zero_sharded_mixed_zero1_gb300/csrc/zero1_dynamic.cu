@@ -142,6 +142,13 @@ k_apply_sums(const float *__restrict__ sums, float *__restrict__ master, float *
 // vector per thread at three or four blocks per SM.
 constexpr Shape kApplyShape{1, 2};
 
+// k_apply_sums when master/m/v live in host memory: two vectors in flight per
+// thread at the kernel's occupancy.  Measured on GB300 against kApplyShape on
+// one box (the dynamic step on host-resident state, M = 8, two runs each):
+// 9.16-9.18 against 9.28-9.29 ms at 124M elements, 64.5-64.8 against
+// 64.9-65.1 ms on the Llama layers.
+constexpr Shape kApplyHostShape{2, 0};
+
 // --------------------------------------------------- ping-pong state ------
 //
 // The dynamic step in one pass over the data: master/m/v exist twice, and
@@ -437,11 +444,19 @@ extern "C" int zero1_step_dynamic(const zero1_plan_t *plan, int32_t shard_begin,
     // 2. the update from the sums (skipped on overflow)
     const ArrayRef ua[5] = {{sums, 4}, {master, 4}, {m, 4}, {v, 4}, {params, 2}};
     const Walk wu = make_walk(r.L, r.nv, ua, 5);
-    static_assert(shape_ok(kApplyShape), "update-from-sums shape");
-    const int grid = grid_for(k_apply_sums<kApplyShape.D>, wu, kApplyShape.per_sm, kApplyShape.block);
+    static_assert(shape_ok(kApplyShape) && shape_ok(kApplyHostShape), "update-from-sums shapes");
     if ((rc = launch_status("dynamic step: reduce-scatter launch")) != ZERO1_OK) return rc;
-    const cudaError_t e = launch_pdl(k_apply_sums<kApplyShape.D>, grid, kApplyShape.block, st, (const float *)sums, master, m, v,
-                                     static_cast<uint16_t *>(params), wu, c, (const zero1_scaler_t *)scaler);
+    cudaError_t e;
+    if (in_host_memory(master)) {
+        // the state crosses the host link: the two-deep kernel at its occupancy
+        const int grid = grid_for(k_apply_sums<kApplyHostShape.D>, wu, kApplyHostShape.per_sm, kApplyHostShape.block);
+        e = launch_pdl(k_apply_sums<kApplyHostShape.D>, grid, kApplyHostShape.block, st, (const float *)sums, master,
+                       m, v, static_cast<uint16_t *>(params), wu, c, (const zero1_scaler_t *)scaler);
+    } else {
+        const int grid = grid_for(k_apply_sums<kApplyShape.D>, wu, kApplyShape.per_sm, kApplyShape.block);
+        e = launch_pdl(k_apply_sums<kApplyShape.D>, grid, kApplyShape.block, st, (const float *)sums, master, m, v,
+                       static_cast<uint16_t *>(params), wu, c, (const zero1_scaler_t *)scaler);
+    }
     if (e != cudaSuccess) return pdl_fail(e, "dynamic step: update launch");
     // 3. the scaler advances (only once the update is enqueued)
     const ScalePolicy pol{policy->factor, policy->window, policy->hysteresis, policy->min_scale};

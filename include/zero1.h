@@ -283,9 +283,9 @@ int zero1_staged_timeline(zero1_staged_t *handle, float *ms, int32_t cap, int32_
  * eight consumer warps compute from there.  Same arguments and bit for bit the
  * same results as zero1_reduce_scatter_adamw_allgather; every buffer must be
  * device memory (EINVAL otherwise).  On GB300 this staging measured slower
- * than the direct register-pipelined loads of the fused step (the stream has
- * no reuse), so the fused step does not use it; it is kept so the comparison
- * can be reproduced.  Its waits are bounded: a wait that runs out (1 s) sets
+ * than the direct register loads of the fused step (the stream has no reuse),
+ * so the fused step does not use it; it is kept so the comparison can be
+ * reproduced.  Its waits are bounded: a wait that runs out (1 s) sets
  * bit 0 of the device status (zero1_device_status) and the kernel returns. */
 int zero1_step_tma(const zero1_plan_t *plan, int32_t shard_begin, int32_t shard_end,
                    const void *const *grads, float *master, float *m, float *v, void *params,

@@ -270,7 +270,7 @@ extern "C" int zero1_overflow_check(const zero1_plan_t *plan, int32_t shard_begi
     if (r.nv == 0) return ZERO1_OK;
     GradPtrs g{};
     if ((rc = load_grads(plan, grads, &g, "overflow check")) != ZERO1_OK) return rc;
-    ArrayRef arr[ZERO1_MAX_REPLICAS];
+    ArrayRef arr[ZERO1_MAX_REPLICAS] = {};
     for (int k = 0; k < plan->M; ++k) arr[k] = {grads[k], 2};
     const Walk w = make_walk(r.nv, r.nv, arr, plan->M);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

@@ -298,7 +298,7 @@ extern "C" int dp_allreduce(const zero1_plan_t *plan, const void *const *grads_i
     const int M = plan->M;
     const int osz = out_dtype == ZERO1_DTYPE_BF16 ? 2 : 4;
     OutPtrs o{};
-    ArrayRef arr[2 * ZERO1_MAX_REPLICAS];
+    ArrayRef arr[2 * ZERO1_MAX_REPLICAS] = {};
     bool overlap = false;  // some output overlaps some input
     for (int k = 0; k < M; ++k) {
         if (!outs[k]) return z1_fail(ZERO1_EINVAL, "all-reduce: outs[%d] is NULL", k);

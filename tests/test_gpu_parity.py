@@ -208,6 +208,34 @@ def test_special_values_and_flag(cuda_device):
         assert int(f.item()) == want_f
 
 
+@pytest.mark.parametrize("M", [1, 3, 8, 9])
+def test_subnormal_moments_are_kept(cuda_device, M):
+    """Gradients near 1e-20 give v' = (1 - beta2) g^2 around 1e-41, below the
+    smallest normal fp32, and the state also starts with subnormal m and v:
+    no step may flush them to zero (the oracle keeps them), over the vector
+    body and the per-element tail."""
+    dev = cuda_device
+    n = 20_011
+    plan = z.zero1_plan(n, M, 1)
+    P = plan.padded_n
+    grads = [synth.normal_bf16(n, 1e-20, synth.seed_of(91, r), dev) for r in range(M)]
+    master, m, v = make_state(n, P, 92, dev)
+    m[:n] = synth.normal_f32(n, 1e-39, synth.seed_of(93, 1), dev)
+    v[:n] = synth.normal_f32(n, 1e-39, synth.seed_of(93, 2), dev).abs_()
+    assert bool(((v[:n] > 0) & (v[:n] < 1.1754944e-38)).any())       # subnormal state present
+    params = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+    o = [f32(master), f32(m), f32(v)]
+    hp = z.AdamW(global_batch=M, step=1, eps=1e-30)
+    z.zero1_reduce_scatter_adamw_allgather(plan, 0, M, grads, master, m, v, params, hp)
+    want = oracle_step(plan, [u16(g) for g in grads], *o, oracle_hp(hp))
+    vv = f32(v)[:n]
+    assert ((vv > 0) & (vv < np.float32(1.1754944e-38))).any()          # subnormal results produced
+    assert_f32_bits(f32(master), o[0], "master")
+    assert_f32_bits(f32(m), o[1], "m")
+    assert_f32_bits(f32(v), o[2], "v")
+    assert_bf16_bits(u16(params), want, "params")
+
+
 def test_skip_if_flag_writes_nothing(cuda_device):
     dev = cuda_device
     M, n = 8, 30_011

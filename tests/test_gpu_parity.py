@@ -208,8 +208,9 @@ def test_special_values_and_flag(cuda_device):
         assert int(f.item()) == want_f
 
 
+@pytest.mark.parametrize("entry", ["fused", "dynamic", "pingpong"])
 @pytest.mark.parametrize("M", [1, 3, 8, 9])
-def test_subnormal_moments_are_kept(cuda_device, M):
+def test_subnormal_moments_are_kept(cuda_device, M, entry):
     """Gradients near 1e-20 give v' = (1 - beta2) g^2 around 1e-41, below the
     smallest normal fp32, and the state also starts with subnormal m and v:
     no step may flush them to zero (the oracle keeps them), over the vector
@@ -226,7 +227,20 @@ def test_subnormal_moments_are_kept(cuda_device, M):
     params = torch.zeros(n, dtype=torch.bfloat16, device=dev)
     o = [f32(master), f32(m), f32(v)]
     hp = z.AdamW(global_batch=M, step=1, eps=1e-30)
-    z.zero1_reduce_scatter_adamw_allgather(plan, 0, M, grads, master, m, v, params, hp)
+    if entry == "fused":
+        z.zero1_reduce_scatter_adamw_allgather(plan, 0, M, grads, master, m, v, params, hp)
+    else:
+        # S = 1 and t = 1 from the device scaler: the same constants as hp
+        policy = z.LossScalePolicy(initial_scale=1.0)
+        scaler = z.new_scaler(dev)
+        z.zero1_scaler_init(scaler, policy, hp)
+        if entry == "dynamic":
+            sums = torch.empty(P, dtype=torch.float32, device=dev)
+            z.zero1_step_dynamic(plan, 0, M, grads, master, m, v, params, hp, scaler, policy, sums)
+        else:
+            pairs = [[x, torch.empty_like(x)] for x in (master, m, v)]
+            z.zero1_step_dynamic_pingpong(plan, 0, M, grads, *pairs, params, hp, scaler, policy)
+            master, m, v = z.current_state(scaler, *pairs)
     want = oracle_step(plan, [u16(g) for g in grads], *o, oracle_hp(hp))
     vv = f32(v)[:n]
     assert ((vv > 0) & (vv < np.float32(1.1754944e-38))).any()          # subnormal results produced

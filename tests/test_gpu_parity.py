@@ -250,6 +250,49 @@ def test_subnormal_moments_are_kept(cuda_device, M, entry):
     assert_bf16_bits(u16(params), want, "params")
 
 
+@pytest.mark.parametrize("entry", ["fused", "dynamic", "pingpong"])
+def test_squared_gradient_overflow_without_a_flag(cuda_device, entry):
+    """Finite gradient sums near 1e20 whose squares overflow fp32: the flag
+    stays clear (the sums are finite), v becomes +inf and the update of those
+    elements reduces to the decay; every output against the oracle."""
+    dev = cuda_device
+    M, n = 4, 9_001
+    plan = z.zero1_plan(n, M, 8)
+    P = plan.padded_n
+    grads = [synth.normal_bf16(n, 1e-3 * M, synth.seed_of(94, r), dev) for r in range(M)]
+    for r in range(M):
+        grads[r][::97] = 3.0e19 * (1 if r % 2 == 0 else 0.5)
+    master, m, v = make_state(n, P, 95, dev, nonzero_moments=True)
+    params = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+    o = [f32(master), f32(m), f32(v)]
+    hp = z.AdamW(global_batch=M, step=3)
+    flag = torch.zeros(1, dtype=torch.int32, device=dev)
+    if entry == "fused":
+        z.zero1_reduce_scatter_adamw_allgather(plan, 0, M, grads, master, m, v, params, hp, flag)
+        assert int(flag.item()) == 0
+    else:
+        policy = z.LossScalePolicy(initial_scale=1.0)
+        scaler = z.new_scaler(dev)
+        z.zero1_scaler_init(scaler, policy, hp)
+        if entry == "dynamic":
+            sums = torch.empty(P, dtype=torch.float32, device=dev)
+            z.zero1_step_dynamic(plan, 0, M, grads, master, m, v, params, hp, scaler, policy, sums)
+        else:
+            pairs = [[x, torch.empty_like(x)] for x in (master, m, v)]
+            z.zero1_step_dynamic_pingpong(plan, 0, M, grads, *pairs, params, hp, scaler, policy)
+            master, m, v = z.current_state(scaler, *pairs)
+        st = z.scaler_state(scaler)
+        assert st["skipped"] == 0 and st["step"] == 4
+    oflag = np.zeros(1, np.uint32)
+    want = oracle_step(plan, [u16(g) for g in grads], *o, oracle_hp(hp), flag=oflag)
+    assert int(oflag[0]) == 0
+    assert np.isinf(f32(v)[:n:97]).all()
+    assert_f32_bits(f32(master), o[0], "master")
+    assert_f32_bits(f32(m), o[1], "m")
+    assert_f32_bits(f32(v), o[2], "v")
+    assert_bf16_bits(u16(params), want, "params")
+
+
 def test_skip_if_flag_writes_nothing(cuda_device):
     dev = cuda_device
     M, n = 8, 30_011

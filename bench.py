@@ -551,6 +551,13 @@ def run_ours(args, w) -> None:
     barrier(world)
     wall1 = time.time()
     ms_local = start.elapsed_time(end)
+    # the launch shape of the step's last streaming kernel (the fused kernel for the default op)
+    try:
+        shape = z.debug_last_launch()
+        last_launch = {"grid": shape["grid"], "block": shape["block"], "blocks_per_sm": shape["blocks_per_sm"],
+                       "fp32_32_byte_accesses": shape["w32"]}
+    except z.Zero1Error:
+        last_launch = None
     launch_ms = np.array([evs[2 * i].elapsed_time(evs[2 * i + 1]) for i in range(args.steps)])
     kernel_ms = float(launch_ms.mean())
     clocks = sampler.summary(wall0, wall1) if sampler else None
@@ -711,6 +718,7 @@ def run_ours(args, w) -> None:
         "e2e": e2e if e2e is not None else ({"skipped": e2e_note} if e2e_note else None),
         "e2e_staged": e2e_staged,
         "gpu_launches": args.steps * launches_per_step,
+        "last_launch_shape": last_launch,
         "clocks": clocks,
         "overflow_flag": overflow,
     }

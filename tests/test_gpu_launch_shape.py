@@ -48,13 +48,15 @@ def test_each_kernel_gets_its_own_occupancy(cuda_device):
 
 
 def test_large_range_shapes_per_replica_count(cuda_device):
-    """On a large range the fused step runs 16 warps per SM (two blocks of
-    256) for M = 3..5 and 20 warps per SM (five blocks of 128) for M = 1, 2
-    and 6..8, the measured faster shape for each M; the grid is one wave."""
+    """On a large range the fused step runs 20 warps per SM (five blocks of
+    128) for M = 1 and 6..8, 18 (three blocks of 192) for M = 2, 3 and 16 (two
+    blocks of 256) for M = 4, 5, the measured faster shape for each M; the
+    grid is one wave."""
     dev = cuda_device
     sms = _sms()
     big = 8 << 20
-    for M, per_sm, block in ((1, 5, 128), (2, 5, 128), (3, 2, 256), (5, 2, 256), (6, 5, 128), (8, 5, 128)):
+    for M, per_sm, block in ((1, 5, 128), (2, 3, 192), (3, 3, 192), (4, 2, 256), (5, 2, 256), (6, 5, 128),
+                             (8, 5, 128)):
         d = _fused(dev, big, M)
         assert "k_fused_step" in d["kernel"] and "grouped" not in d["kernel"], (M, d)
         assert (d["blocks_per_sm"], d["block"]) == (per_sm, block) and d["grid"] == per_sm * sms, (M, d)

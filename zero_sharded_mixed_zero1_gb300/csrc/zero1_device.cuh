@@ -277,15 +277,18 @@ struct Shape {
 // MT = 0: M > 8, replicas in groups of 8, where the shape is not used).
 // Measured on GB300 (fused step, 124M elements, one box, fraction of the
 // measured copy bandwidth), by warps per SM: 20 (five blocks of 128) for
-// M = 1, 2 and 6..8: 0.984 0.977 and 1.017 1.027 1.029; 16 (two blocks of
-// 256) for M = 3..5: 0.993 1.015 1.020, where 20 gave 0.973 0.955 0.939.
-// 12 warps gave 0.79-0.93 and 24 warps 0.85-0.97 for every M.  The two-deep
-// pipeline this replaced (two vectors in flight per thread, 8 warps per SM)
-// reached 0.995 1.007 1.019 at M = 6..8 and 0.93-0.98 at M <= 5.
+// M = 1 and 6..8: 0.984 and 1.017 1.027 1.029; 18 (three blocks of 192) for
+// M = 2, 3: 0.995 1.001, where 20 gave 0.977 0.973 and 16 0.978 0.993; 16
+// (two blocks of 256) for M = 4, 5: 1.015 1.020, where 18 gave 0.991 0.971
+// and 20 0.955 0.939.  12 warps gave 0.79-0.93 and 24 warps 0.85-0.97 for
+// every M.  The two-deep pipeline this replaced (two vectors in flight per
+// thread, 8 warps per SM) reached 0.995 1.007 1.019 at M = 6..8 and
+// 0.93-0.98 at M <= 5.
 constexpr Shape fused_shape(int MT)
 {
     switch (MT) {
-    case 3: case 4: case 5: return Shape{1, 2};
+    case 2: case 3: return Shape{1, 3, 192};
+    case 4: case 5: return Shape{1, 2};
     case 0: return Shape{2, 0};
     default: return Shape{1, 5, 128};
     }

@@ -247,14 +247,15 @@ k_fused_step_pingpong(const __grid_constant__ GradPtrs g, int M, const __grid_co
 // in groups of 8, where D is not used).  Measured on GB300, the ping-pong
 // step on 124M elements, fraction of the measured copy bandwidth: two-deep
 // 0.909 0.915 0.932 0.951 0.967 0.981 0.992 1.002 for M = 1..8; one vector
-// at 16 warps per SM 0.949 0.975 0.995 1.006 for M = 1..4 and, at M = 5,
-// 1.003 in blocks of 128 but 0.91 in blocks of 256; one vector at 20 warps
-// per SM (five blocks of 128) 0.966 for M = 1 and 1.009 1.014 1.016 for
-// M = 6..8.  This table: 0.965 0.975 0.998 1.011 1.009 1.014 1.018 1.023.
+// at 18 warps per SM (three blocks of 192) 0.989 0.991 for M = 1, 2 (20
+// warps: 0.966 0.955); at 16 warps per SM 0.995 1.006 for M = 3, 4 and, at
+// M = 5, 1.003 in blocks of 128 but 0.91 in blocks of 256; at 20 warps per
+// SM (five blocks of 128) 1.009 1.014 1.016 for M = 6..8.
 constexpr Shape pingpong_shape(int MT)
 {
     switch (MT) {
-    case 2: case 3: case 4: return Shape{1, 2};
+    case 1: case 2: return Shape{1, 3, 192};
+    case 3: case 4: return Shape{1, 2};
     case 5: return Shape{1, 4, 128};
     case 0: return Shape{2, 0};
     default: return Shape{1, 5, 128};

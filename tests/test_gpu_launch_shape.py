@@ -73,7 +73,8 @@ def test_allreduce_and_update_shapes(cuda_device):
     sms = _sms()
     n = 4 << 20
     for M, per_sm, block, one_vector in ((1, 3, 256, True), (2, 5, 128, True), (3, 2, 256, True),
-                                         (4, 5, 128, True), (6, 2, 256, True), (8, 3, 128, True)):
+                                         (4, 5, 128, True), (5, 3, 192, True), (6, 2, 256, True),
+                                         (8, 3, 128, True)):
         plan = z.zero1_plan(n, M, 1)
         grads = make_grads(M, n, 1e-3, 5, 1, dev)
         outs = [torch.empty(n, dtype=torch.bfloat16, device=dev) for _ in range(M)]
@@ -105,10 +106,10 @@ def test_allreduce_and_update_shapes(cuda_device):
     torch.cuda.synchronize()
     d = z.debug_last_launch()
     assert "k_apply_sumsILi2E" in d["kernel"] and d["grid"] == d["blocks_per_sm"] * sms, d
-    # the unfused update: one vector per thread, five blocks of 128 per SM
+    # the unfused update: one vector per thread, three blocks of 192 per SM
     z.zero1_adamw_update(plan, 0, M, sums, master, m, v, hp)
     d = z.debug_last_launch()
-    assert "k_adamw" in d["kernel"] and "Li1E" in d["kernel"] and (d["grid"], d["block"]) == (5 * sms, 128), d
+    assert "k_adamw" in d["kernel"] and "Li1E" in d["kernel"] and (d["grid"], d["block"]) == (3 * sms, 192), d
     # the overflow check at M = 8: three blocks per SM
     flag = torch.zeros(1, dtype=torch.int32, device=dev)
     z.zero1_overflow_check(plan, 0, M, grads, flag)

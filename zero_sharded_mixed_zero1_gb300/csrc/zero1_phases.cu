@@ -111,11 +111,11 @@ k_all_gather(const float *__restrict__ master, uint16_t *__restrict__ params, co
 
 // Launch shapes of k_adamw and k_all_gather.  Measured on GB300, 124M
 // elements, fraction of the measured copy bandwidth: k_adamw two-deep at two
-// blocks of 256 per SM 0.952, one vector at 12, 16, 20, 24, 32 warps per SM
-// 0.845, 0.973, 1.001, 0.949, 0.921 (20: five blocks of 128); k_all_gather
-// two-deep at its full occupancy 0.998, one vector at 12-32 warps per SM
-// 0.62-0.98.
-constexpr Shape kAdamwShape{1, 5, 128};
+// blocks of 256 per SM 0.952, one vector at 12, 16, 18, 20, 24, 32 warps per
+// SM 0.845, 0.973, 1.007, 1.000, 0.949, 0.921 (18: three blocks of 192, 20:
+// five blocks of 128); k_all_gather two-deep at its full occupancy 0.998,
+// one vector at 12-32 warps per SM 0.62-0.98.
+constexpr Shape kAdamwShape{1, 3, 192};
 constexpr Shape kAllGatherShape{2, 0};
 
 // All-gather of bf16 shards into M outputs (real elements only).
@@ -228,8 +228,9 @@ k_allreduce_inplace(const __grid_constant__ GradPtrs g, const __grid_constant__ 
 // this table 0.924 0.957 0.970 0.971 0.967 0.976 0.961 0.979; in place
 // two-deep 0.788 0.963 0.954 0.942 0.939 0.944 0.935 0.956, this table 0.777
 // 0.960 0.966 0.977 0.974 0.982 0.967 0.984.  The one-vector grids tried were
-// 12, 16, 20, 24 and 32 warps per SM (blocks of 128 or 256); the best differs
-// by M, reproducibly across boxes.  M > 8 (16M elements): two blocks of 256
+// 12, 16, 18, 20, 24 and 32 warps per SM (blocks of 128, 192 or 256); the
+// best differs by M, reproducibly across boxes (at M = 5, 18 warps measured
+// 0.8 % and, in place, 0.5 % above 16).  M > 8 (16M elements): two blocks of 256
 // per SM 0.942 at M = 16 and 0.948 at M = 64, against 0.922 and 0.929 at the
 // kernel's occupancy of three.
 constexpr Shape allreduce_shape(int MT)
@@ -237,7 +238,8 @@ constexpr Shape allreduce_shape(int MT)
     switch (MT) {
     case 1: return Shape{1, 3};
     case 2: case 4: return Shape{1, 5, 128};
-    case 3: case 5: case 6: return Shape{1, 2};
+    case 3: case 6: return Shape{1, 2};
+    case 5: return Shape{1, 3, 192};
     case 7: case 8: return Shape{1, 3, 128};
     case 0: return Shape{2, 2};
     default: return Shape{2, 0};
@@ -249,7 +251,8 @@ constexpr Shape allreduce_inplace_shape(int MT)
     switch (MT) {
     case 3: return Shape{1, 3};
     case 4: return Shape{1, 5, 128};
-    case 5: case 6: return Shape{1, 2};
+    case 5: return Shape{1, 3, 192};
+    case 6: return Shape{1, 2};
     case 7: case 8: return Shape{1, 3, 128};
     case 0: return Shape{2, 2};
     default: return Shape{2, 0};
